@@ -1,0 +1,311 @@
+/*
+ * oracle.c -- plain, slow, single-threaded fp64 CPU oracle for the W4A16 NVFP4
+ * mixture-of-experts FFN layer.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Only the test suite, the smoke check and the
+ * benchmark's CPU-baseline leg load this file.  It shares no code, header,
+ * table or constant with the CUDA library; it reads the same input bytes and
+ * nothing else.
+ *
+ * What it computes, and where that is stated:
+ *  - Atlas article "告别Python堆栈：Atlas用纯Rust重写LLM推理，在GB10上跑赢vLLM"
+ *    (f.mffb.com.cn/a/497905.html), section "编译时内核选择和W4A16 Grouped GEMM":
+ *    an MoE layer with two per-expert projections, gate_up and down, whose
+ *    weights are packed 4-bit NVFP4 codes dequantised to BF16 and multiplied
+ *    against BF16 activations by a BF16 MMA.
+ *  - same article, section "KV Cache量化、MTP推测解码和调试工具链": the MoE layer
+ *    takes gate logits, picks expert IDs, and the routed output is the layer
+ *    output (the article debugs it against a higher-precision oracle, which
+ *    is what this file is).
+ *  - ATOM article "AMD ATOM推理引擎：如何用分页KV缓存和分段编译实现大模型推理性能翻倍"
+ *    (itsolotime.com/archives/33112), section "8.1 MoE 路径：路由、专家并行与
+ *    MORI 通信": MoE = token routing, top-k selection, expert compute and a
+ *    final combine of the expert outputs per token.
+ *  - "Rust 实现深度学习推理引擎：从计算图到异构硬件加速"
+ *    (ybb.press/ai-applications/14151.html), section "三、计算图：节点、边与拓扑排序":
+ *    the SiLU / SwiGLU activation of LLaMA-style FFNs.
+ *
+ * The NVFP4 format itself is not spelled out on those pages (they only name
+ * "nvfp4" and "E2M1"); the decoders below follow the public OCP FP8 / MX
+ * closed forms: E2M1 = 1 sign, 2 exponent (bias 1), 1 mantissa bit;
+ * E4M3 = 1 sign, 4 exponent (bias 7), 3 mantissa bits, no infinities,
+ * S.1111.111 = NaN.  A weight is code * block_scale * global_scale, with one
+ * E4M3 block scale per 16 consecutive elements along K and one fp32 global
+ * scale per expert matrix.
+ *
+ * Readings where the pages are silent (each is also listed in the design doc):
+ *  - packed codes: element 2i in the low nibble, 2i+1 in the high nibble;
+ *  - gate_up rows 0..I-1 are the gate projection, rows I..2I-1 the up
+ *    projection, and SwiGLU = silu(gate) * up;
+ *  - routing selects on the fp32 logits, ties to the lower expert index,
+ *    NaN treated as -infinity; the k gate weights are the softmax over the k
+ *    selected logits (the same as a softmax over all E renormalised over the
+ *    selected k);
+ *  - the intermediate activation h (input of the down projection's BF16 MMA)
+ *    is rounded to bf16, round-to-nearest-even; everything else is fp64.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+/* ---------------------------------------------------------------- decoders */
+
+/* E2M1 code (low 4 bits of `code`) -> value.  sign = bit 3, exponent = bits
+ * 2..1 (bias 1), mantissa = bit 0.  exponent 0 is subnormal: 0.5 * m. */
+double oracle_dec_e2m1(unsigned code)
+{
+    unsigned s = (code >> 3) & 1u, e = (code >> 1) & 3u, m = code & 1u;
+    double mag = (e == 0) ? 0.5 * (double)m : ldexp(1.0 + 0.5 * (double)m, (int)e - 1);
+    return s ? -mag : mag;
+}
+
+/* E4M3 ("fn" variant) code -> value.  sign = bit 7, exponent = bits 6..3
+ * (bias 7), mantissa = bits 2..0.  exponent 0 is subnormal: (m/8) * 2^-6.
+ * exponent 15 with mantissa 7 is NaN; there are no infinities. */
+double oracle_dec_e4m3(unsigned code)
+{
+    unsigned s = (code >> 7) & 1u, e = (code >> 3) & 15u, m = code & 7u;
+    double mag;
+    if (e == 15u && m == 7u) return NAN;
+    if (e == 0u) mag = ldexp((double)m / 8.0, -6);
+    else mag = ldexp(1.0 + (double)m / 8.0, (int)e - 7);
+    return s ? -mag : mag;
+}
+
+/* bf16 bit pattern -> value (exact). */
+double oracle_bf16_to_double(uint16_t b)
+{
+    uint32_t u = (uint32_t)b << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+/* fp64 -> bf16 bit pattern, round to nearest, ties to even, computed on the
+ * value (not on bits): find the two neighbouring bf16 values and pick. */
+uint16_t oracle_bf16_rne(double v)
+{
+    if (isnan(v)) return 0x7FC0u;
+    uint16_t sign = signbit(v) ? 0x8000u : 0u;
+    double a = fabs(v);
+    if (a == 0.0) return sign;
+    /* bf16: 8 significant bits, exponent range of fp32 (normal >= 2^-126,
+     * subnormal quantum 2^-133), max finite (2 - 2^-7) * 2^127. */
+    int ex;
+    frexp(a, &ex);              /* a = f * 2^ex, f in [0.5, 1) */
+    int e = ex - 1;             /* a in [2^e, 2^(e+1)) */
+    if (e < -126) e = -126;     /* subnormal range keeps the quantum fixed */
+    double q = ldexp(1.0, e - 7);
+    double lo = floor(a / q) * q;
+    double hi = lo + q;
+    double r;
+    if (a - lo < hi - a) r = lo;
+    else if (a - lo > hi - a) r = hi;
+    else r = (fmod(lo / q, 2.0) == 0.0) ? lo : hi;
+    if (r > ldexp(2.0 - ldexp(1.0, -7), 127)) return (uint16_t)(sign | 0x7F80u); /* overflow -> inf */
+    float f = (float)r;     /* exact: r has <= 8 significant bits in fp32 range */
+    uint32_t u;
+    memcpy(&u, &f, sizeof u);
+    return (uint16_t)(sign | ((u >> 16) & 0x7FFFu));
+}
+
+static double g_e2m1[16];
+static double g_e4m3[256];
+static int g_tables_ready = 0;
+
+static void tables_init(void)
+{
+    if (g_tables_ready) return;
+    for (unsigned c = 0; c < 16; ++c) g_e2m1[c] = oracle_dec_e2m1(c);
+    for (unsigned c = 0; c < 256; ++c) g_e4m3[c] = oracle_dec_e4m3(c);
+    g_tables_ready = 1;
+}
+
+/* One weight element W[e][n][kk] of a projection with N rows and K columns:
+ * codes [E][N][K/2] (low nibble = even kk), scales [E][N][K/16], gs [E]. */
+double oracle_weight(const uint8_t *codes, const uint8_t *scales, const float *gs,
+                     int N, int K, int e, int n, int kk)
+{
+    tables_init();
+    size_t row = (size_t)e * (size_t)N + (size_t)n;
+    uint8_t byte = codes[row * (size_t)(K / 2) + (size_t)(kk / 2)];
+    unsigned nib = (kk & 1) ? (byte >> 4) : (byte & 15u);
+    uint8_t sc = scales[row * (size_t)(K / 16) + (size_t)(kk / 16)];
+    return g_e2m1[nib] * g_e4m3[sc] * (double)gs[e];
+}
+
+/* Decode a whole weight row into `out[K]` (same formula, one row at a time so
+ * that no full matrix is ever materialised). */
+void oracle_decode_row(const uint8_t *codes, const uint8_t *scales, const float *gs,
+                       int N, int K, int e, int n, double *out)
+{
+    tables_init();
+    size_t row = (size_t)e * (size_t)N + (size_t)n;
+    const uint8_t *c = codes + row * (size_t)(K / 2);
+    const uint8_t *s = scales + row * (size_t)(K / 16);
+    double g = (double)gs[e];
+    for (int kk = 0; kk < K; ++kk) {
+        unsigned nib = (kk & 1) ? (c[kk / 2] >> 4) : (c[kk / 2] & 15u);
+        out[kk] = g_e2m1[nib] * g_e4m3[s[kk / 16]] * g;
+    }
+}
+
+/* ------------------------------------------------------------------ routing */
+
+static double route_key(float v)
+{
+    return isnan(v) ? -INFINITY : (double)v;
+}
+
+/* Top-k routing of every token.  logits fp32 [T][E].  Writes ids [T][k]
+ * (slot order: descending logit, ties to the lower expert index) and the
+ * gate weights w [T][k] in fp64: softmax over the k selected logits.  If the
+ * best selected logit is -infinity (all NaN / -inf), the weights are 1/k. */
+void oracle_route(const float *logits, int T, int E, int k, int32_t *ids, double *w)
+{
+    char *taken = (char *)malloc((size_t)E);
+    for (int t = 0; t < T; ++t) {
+        const float *l = logits + (size_t)t * (size_t)E;
+        memset(taken, 0, (size_t)E);
+        for (int j = 0; j < k; ++j) {
+            int best = -1;
+            double bv = 0.0;
+            for (int e = 0; e < E; ++e) {
+                if (taken[e]) continue;
+                double v = route_key(l[e]);
+                if (best < 0 || v > bv) { best = e; bv = v; }  /* strict: keeps lower index on ties */
+            }
+            taken[best] = 1;
+            ids[(size_t)t * k + j] = best;
+        }
+        double lmax = route_key(l[ids[(size_t)t * k]]);
+        if (lmax == -INFINITY) {
+            for (int j = 0; j < k; ++j) w[(size_t)t * k + j] = 1.0 / (double)k;
+            continue;
+        }
+        double sum = 0.0;
+        for (int j = 0; j < k; ++j) {
+            double z = exp(route_key(l[ids[(size_t)t * k + j]]) - lmax);
+            w[(size_t)t * k + j] = z;
+            sum += z;
+        }
+        for (int j = 0; j < k; ++j) w[(size_t)t * k + j] /= sum;
+    }
+    free(taken);
+}
+
+/* -------------------------------------------------------------- permutation */
+
+/* Group the T*k (token, slot) pairs by expert.  counts[e] = number of pairs
+ * routed to e; offsets = exclusive scan of counts (E+1 entries); the sorted
+ * order lists pairs by (expert, token) -- a token meets an expert at most once
+ * -- so sorted_token[p] is the token of sorted row p and inv_perm[t*k+j] is
+ * the sorted row of pair (t, j). */
+void oracle_permute(const int32_t *ids, int T, int E, int k, int32_t *counts,
+                    int32_t *offsets, int32_t *sorted_token, int32_t *inv_perm)
+{
+    int n = T * k;
+    for (int e = 0; e < E; ++e) counts[e] = 0;
+    for (int i = 0; i < n; ++i) counts[ids[i]] += 1;
+    offsets[0] = 0;
+    for (int e = 0; e < E; ++e) offsets[e + 1] = offsets[e] + counts[e];
+    int32_t *fill = (int32_t *)malloc(sizeof(int32_t) * (size_t)(E > 0 ? E : 1));
+    for (int e = 0; e < E; ++e) fill[e] = offsets[e];
+    for (int i = 0; i < n; ++i) {           /* ascending i = ascending (token, slot) */
+        int e = ids[i];
+        int p = fill[e]++;
+        sorted_token[p] = i / k;
+        inv_perm[i] = p;
+    }
+    free(fill);
+}
+
+/* ------------------------------------------------------------ expert FFN */
+
+/* gate_up + SwiGLU for one activation row.  x: bf16 bits [H].  gate_up
+ * weights have N = 2I rows, K = H.  h_exact [I] (fp64, may be NULL) and
+ * h_bf16 [I] (bf16 bits of h_exact, RNE, may be NULL). */
+void oracle_gate_up_swiglu_row(const uint16_t *x, int H, int I,
+                               const uint8_t *codes, const uint8_t *scales, const float *gs,
+                               int e, double *h_exact, uint16_t *h_bf16)
+{
+    double *xv = (double *)malloc(sizeof(double) * (size_t)H);
+    double *wr = (double *)malloc(sizeof(double) * (size_t)H);
+    for (int i = 0; i < H; ++i) xv[i] = oracle_bf16_to_double(x[i]);
+    for (int f = 0; f < I; ++f) {
+        double g = 0.0, u = 0.0;
+        oracle_decode_row(codes, scales, gs, 2 * I, H, e, f, wr);
+        for (int i = 0; i < H; ++i) g += xv[i] * wr[i];
+        oracle_decode_row(codes, scales, gs, 2 * I, H, e, I + f, wr);
+        for (int i = 0; i < H; ++i) u += xv[i] * wr[i];
+        double h = g / (1.0 + exp(-g)) * u;
+        if (h_exact) h_exact[f] = h;
+        if (h_bf16) h_bf16[f] = oracle_bf16_rne(h);
+    }
+    free(xv);
+    free(wr);
+}
+
+/* down projection for one row.  h: bf16 bits [I].  down weights have N = H
+ * rows, K = I.  y [H] fp64. */
+void oracle_down_row(const uint16_t *h, int H, int I,
+                     const uint8_t *codes, const uint8_t *scales, const float *gs,
+                     int e, double *y)
+{
+    double *hv = (double *)malloc(sizeof(double) * (size_t)I);
+    double *wr = (double *)malloc(sizeof(double) * (size_t)I);
+    for (int i = 0; i < I; ++i) hv[i] = oracle_bf16_to_double(h[i]);
+    for (int n = 0; n < H; ++n) {
+        double acc = 0.0;
+        oracle_decode_row(codes, scales, gs, H, I, e, n, wr);
+        for (int i = 0; i < I; ++i) acc += hv[i] * wr[i];
+        y[n] = acc;
+    }
+    free(hv);
+    free(wr);
+}
+
+/* ------------------------------------------------------------------ layer */
+
+/* Layer output for the tokens listed in rows[0..nrows): out [nrows][H] fp64.
+ * out[r] = sum_j w[t,j] * down_e(bf16(swiglu(gate_up_e(x[t])))), e = id[t,j].
+ * ids / w must come from oracle_route (ids [T][k], w [T][k]). */
+void oracle_layer_rows(const uint16_t *x, const int32_t *ids, const double *w,
+                       const uint8_t *gu_codes, const uint8_t *gu_scales, const float *gu_gs,
+                       const uint8_t *dn_codes, const uint8_t *dn_scales, const float *dn_gs,
+                       int H, int I, int k, const int32_t *rows, int nrows, double *out)
+{
+    uint16_t *h = (uint16_t *)malloc(sizeof(uint16_t) * (size_t)I);
+    double *y = (double *)malloc(sizeof(double) * (size_t)H);
+    for (int r = 0; r < nrows; ++r) {
+        int t = rows[r];
+        double *o = out + (size_t)r * (size_t)H;
+        for (int n = 0; n < H; ++n) o[n] = 0.0;
+        for (int j = 0; j < k; ++j) {
+            int e = ids[(size_t)t * k + j];
+            double wj = w[(size_t)t * k + j];
+            oracle_gate_up_swiglu_row(x + (size_t)t * (size_t)H, H, I, gu_codes, gu_scales, gu_gs,
+                                      e, NULL, h);
+            oracle_down_row(h, H, I, dn_codes, dn_scales, dn_gs, e, y);
+            for (int n = 0; n < H; ++n) o[n] += wj * y[n];
+        }
+    }
+    free(h);
+    free(y);
+}
+
+/* Whole layer: route, then every token.  out [T][H] fp64; ids [T][k] and
+ * w [T][k] are written too. */
+void oracle_layer(const uint16_t *x, const float *logits,
+                  const uint8_t *gu_codes, const uint8_t *gu_scales, const float *gu_gs,
+                  const uint8_t *dn_codes, const uint8_t *dn_scales, const float *dn_gs,
+                  int T, int H, int I, int E, int k, int32_t *ids, double *w, double *out)
+{
+    int32_t *rows = (int32_t *)malloc(sizeof(int32_t) * (size_t)(T > 0 ? T : 1));
+    oracle_route(logits, T, E, k, ids, w);
+    for (int t = 0; t < T; ++t) rows[t] = t;
+    oracle_layer_rows(x, ids, w, gu_codes, gu_scales, gu_gs, dn_codes, dn_scales, dn_gs,
+                      H, I, k, rows, T, out);
+    free(rows);
+}

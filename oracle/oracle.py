@@ -1,0 +1,196 @@
+"""ctypes wrapper around oracle.c -- the fp64 CPU oracle of the W4A16 NVFP4 MoE layer.
+
+TEST INFRASTRUCTURE ONLY: imported by the tests, by the smoke check and by the
+benchmark's CPU-baseline leg; never by the library.  It shares no code with the
+CUDA path.  Every function here is argument marshalling around the C code; the
+arithmetic, and the citations of what it follows, are in oracle.c.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.c")
+_LIB_PATH = os.path.join(_HERE, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+# -std=c11 keeps fp contraction off (also given explicitly) so x86 and Arm
+# hosts produce the same bits; no -ffast-math, no OpenMP, no BLAS.
+CFLAGS = ["-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math", "-fPIC", "-shared"]
+
+
+def build(force: bool = False) -> str:
+    """Compile oracle.c into liboracle.so next to it (gcc, single-threaded code)."""
+    if not force and os.path.exists(_LIB_PATH) and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC):
+        return _LIB_PATH
+    tmp = _LIB_PATH + f".tmp{os.getpid()}"
+    subprocess.check_call(["gcc", *CFLAGS, _SRC, "-o", tmp, "-lm"])
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            build()
+            lib = ctypes.CDLL(_LIB_PATH)
+            P = ctypes.c_void_p
+            i = ctypes.c_int
+            lib.oracle_dec_e2m1.restype = ctypes.c_double
+            lib.oracle_dec_e2m1.argtypes = [ctypes.c_uint]
+            lib.oracle_dec_e4m3.restype = ctypes.c_double
+            lib.oracle_dec_e4m3.argtypes = [ctypes.c_uint]
+            lib.oracle_bf16_rne.restype = ctypes.c_uint16
+            lib.oracle_bf16_rne.argtypes = [ctypes.c_double]
+            lib.oracle_bf16_to_double.restype = ctypes.c_double
+            lib.oracle_bf16_to_double.argtypes = [ctypes.c_uint16]
+            lib.oracle_weight.restype = ctypes.c_double
+            lib.oracle_weight.argtypes = [P, P, P, i, i, i, i, i]
+            lib.oracle_decode_row.restype = None
+            lib.oracle_decode_row.argtypes = [P, P, P, i, i, i, i, P]
+            lib.oracle_route.restype = None
+            lib.oracle_route.argtypes = [P, i, i, i, P, P]
+            lib.oracle_permute.restype = None
+            lib.oracle_permute.argtypes = [P, i, i, i, P, P, P, P]
+            lib.oracle_gate_up_swiglu_row.restype = None
+            lib.oracle_gate_up_swiglu_row.argtypes = [P, i, i, P, P, P, i, P, P]
+            lib.oracle_down_row.restype = None
+            lib.oracle_down_row.argtypes = [P, i, i, P, P, P, i, P]
+            lib.oracle_layer_rows.restype = None
+            lib.oracle_layer_rows.argtypes = [P, P, P, P, P, P, P, P, P, i, i, i, P, i, P]
+            lib.oracle_layer.restype = None
+            lib.oracle_layer.argtypes = [P, P, P, P, P, P, P, P, i, i, i, i, i, P, P, P]
+            _lib = lib
+    return _lib
+
+
+def _ptr(a: np.ndarray):
+    assert a.flags["C_CONTIGUOUS"], "oracle inputs must be C-contiguous"
+    return ctypes.c_void_p(a.ctypes.data)
+
+
+def _c(a, dtype):
+    return np.ascontiguousarray(np.asarray(a), dtype=dtype)
+
+
+# ------------------------------------------------------------------ decoders
+def dec_e2m1(code: int) -> float:
+    return _load().oracle_dec_e2m1(int(code))
+
+
+def dec_e4m3(code: int) -> float:
+    return _load().oracle_dec_e4m3(int(code))
+
+
+def bf16_rne(v: float) -> int:
+    return int(_load().oracle_bf16_rne(float(v)))
+
+
+def bf16_to_float(bits: int) -> float:
+    return _load().oracle_bf16_to_double(int(bits))
+
+
+def weight(codes, scales, gs, N, K, e, n, kk) -> float:
+    codes, scales, gs = _c(codes, np.uint8), _c(scales, np.uint8), _c(gs, np.float32)
+    return _load().oracle_weight(_ptr(codes), _ptr(scales), _ptr(gs), N, K, e, n, kk)
+
+
+def decode_row(codes, scales, gs, N, K, e, n) -> np.ndarray:
+    codes, scales, gs = _c(codes, np.uint8), _c(scales, np.uint8), _c(gs, np.float32)
+    out = np.empty(K, np.float64)
+    _load().oracle_decode_row(_ptr(codes), _ptr(scales), _ptr(gs), N, K, e, n, _ptr(out))
+    return out
+
+
+# ------------------------------------------------------------------- routing
+def route(logits, k: int):
+    """-> (ids int32 [T,k], w float64 [T,k])."""
+    logits = _c(logits, np.float32)
+    T, E = logits.shape
+    ids = np.empty((T, k), np.int32)
+    w = np.empty((T, k), np.float64)
+    _load().oracle_route(_ptr(logits), T, E, k, _ptr(ids), _ptr(w))
+    return ids, w
+
+
+def permute(ids, E: int):
+    """-> (counts [E], offsets [E+1], sorted_token [T*k], inv_perm [T*k]) all int32."""
+    ids = _c(ids, np.int32)
+    T, k = ids.shape
+    counts = np.empty(E, np.int32)
+    offsets = np.empty(E + 1, np.int32)
+    sorted_token = np.empty(T * k, np.int32)
+    inv_perm = np.empty(T * k, np.int32)
+    _load().oracle_permute(_ptr(ids), T, E, k, _ptr(counts), _ptr(offsets), _ptr(sorted_token), _ptr(inv_perm))
+    return counts, offsets, sorted_token, inv_perm
+
+
+# ------------------------------------------------------------- expert stages
+def gate_up_swiglu_rows(x_rows_bf16, experts, gu, I: int):
+    """x_rows_bf16: uint16 [P,H] (bf16 bits); experts: [P] expert per row;
+    gu = (codes [E,2I,H/2], scales [E,2I,H/16], gs [E]).
+    -> (h_exact float64 [P,I], h_bf16 uint16 [P,I])."""
+    x = _c(x_rows_bf16, np.uint16)
+    P_, H = x.shape
+    codes, scales, gs = _c(gu[0], np.uint8), _c(gu[1], np.uint8), _c(gu[2], np.float32)
+    h_exact = np.empty((P_, I), np.float64)
+    h_bf16 = np.empty((P_, I), np.uint16)
+    lib = _load()
+    for p in range(P_):
+        lib.oracle_gate_up_swiglu_row(_ptr(x[p]), H, I, _ptr(codes), _ptr(scales), _ptr(gs), int(experts[p]),
+                                      _ptr(h_exact[p]), _ptr(h_bf16[p]))
+    return h_exact, h_bf16
+
+
+def down_rows(h_rows_bf16, experts, dn, H: int):
+    """h_rows_bf16: uint16 [P,I]; dn = (codes [E,H,I/2], scales [E,H,I/16], gs [E]). -> y float64 [P,H]."""
+    h = _c(h_rows_bf16, np.uint16)
+    P_, I = h.shape
+    codes, scales, gs = _c(dn[0], np.uint8), _c(dn[1], np.uint8), _c(dn[2], np.float32)
+    y = np.empty((P_, H), np.float64)
+    lib = _load()
+    for p in range(P_):
+        lib.oracle_down_row(_ptr(h[p]), H, I, _ptr(codes), _ptr(scales), _ptr(gs), int(experts[p]), _ptr(y[p]))
+    return y
+
+
+# --------------------------------------------------------------------- layer
+def layer(x_bf16, logits, gu, dn, k: int):
+    """Whole layer. x_bf16 uint16 [T,H]; logits f32 [T,E]. -> (out f64 [T,H], ids, w)."""
+    x = _c(x_bf16, np.uint16)
+    logits = _c(logits, np.float32)
+    T, H = x.shape
+    E = logits.shape[1]
+    I = gu[0].shape[1] // 2
+    ids = np.empty((T, k), np.int32)
+    w = np.empty((T, k), np.float64)
+    out = np.empty((T, H), np.float64)
+    a = [_c(gu[0], np.uint8), _c(gu[1], np.uint8), _c(gu[2], np.float32),
+         _c(dn[0], np.uint8), _c(dn[1], np.uint8), _c(dn[2], np.float32)]
+    _load().oracle_layer(_ptr(x), _ptr(logits), *[_ptr(v) for v in a], T, H, I, E, k,
+                         _ptr(ids), _ptr(w), _ptr(out))
+    return out, ids, w
+
+
+def layer_rows(x_bf16, ids, w, gu, dn, rows):
+    """Layer output for a subset of tokens, given the routing. -> out f64 [len(rows), H]."""
+    x = _c(x_bf16, np.uint16)
+    ids = _c(ids, np.int32)
+    w = _c(w, np.float64)
+    rows = _c(rows, np.int32)
+    T, H = x.shape
+    k = ids.shape[1]
+    I = gu[0].shape[1] // 2
+    out = np.empty((len(rows), H), np.float64)
+    a = [_c(gu[0], np.uint8), _c(gu[1], np.uint8), _c(gu[2], np.float32),
+         _c(dn[0], np.uint8), _c(dn[1], np.uint8), _c(dn[2], np.float32)]
+    _load().oracle_layer_rows(_ptr(x), _ptr(ids), _ptr(w), *[_ptr(v) for v in a], H, I, k,
+                              _ptr(rows), len(rows), _ptr(out))
+    return out
