@@ -1,0 +1,382 @@
+"""Benchmark of the W4A16 NVFP4 MoE layer on GB300 (one JSON line on rank 0).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload NAME]
+
+A step is one pass of the whole layer (route -> permute -> gate_up+SwiGLU ->
+down -> combine) over one batch of seeded synthetic input of the decode-shaped
+workload (T=32 tokens, H=2048, I=768, 128 experts, top-8, NVFP4 weights).
+
+ours:      inputs resident in HBM; each timed step is moe_layer_forward_profiled
+           (same kernels as moe_layer_forward) bracketed by CUDA events on the
+           launching stream, the L2 flushed (a 2x-L2 buffer written) between steps
+           outside the events.  `e2e` runs moe_layer_forward_host: pinned host
+           x / logits in, host out back, copies inside the timed region.
+reference: the fp64 CPU oracle (single thread) on a bounded token sample of the
+           same workload; rank 0 only.
+N > 1 ranks run independent replicas (the path needs no exchange between GPUs);
+value = tokens of all ranks / max-over-ranks time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from moe_layer_bit_gb300 import workloads as wk  # noqa: E402
+
+METRIC = "MoE-layer tokens/s at 1 GB300; HBM GB/s (decode) / tensor TFLOP/s (prefill) vs peak"
+UNIT = "tokens/s"
+DEFAULT_WORKLOAD = "decode"
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), float(p["bf16_tflops_sustained"]), "measured"
+    except Exception:
+        return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+# ------------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling while the timed region runs."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.thread.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------ distributed
+def _dist_init(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() and args.impl == "ours" else "gloo"
+        dist.init_process_group(backend=backend)
+        return dist, int(os.environ.get("RANK", "0")), world, int(os.environ.get("LOCAL_RANK", "0"))
+    return None, 0, 1, 0
+
+
+def _max_over_ranks(dist, v: float, device) -> float:
+    if dist is None:
+        return v
+    t = torch.tensor([v], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def _barrier(dist, device=None):
+    if dist is not None:
+        if device is not None and device.type == "cuda":
+            dist.barrier(device_ids=[device.index])
+        else:
+            dist.barrier()
+
+
+# --------------------------------------------------------------- CPU oracle
+def oracle_sample(d, wl, n_tokens: int, seed: int = 0):
+    """Time the fp64 oracle on a seeded token sample; returns (seconds, n_tokens)."""
+    from oracle import oracle as orc
+    rng = np.random.default_rng(seed)
+    rows = np.sort(rng.choice(wl.T, size=min(n_tokens, wl.T), replace=False)).astype(np.int32)
+    xb = d["x"].view(torch.int16).numpy().view(np.uint16)
+    gu = tuple(a.numpy() for a in d["gu"])
+    dn = tuple(a.numpy() for a in d["dn"])
+    t0 = time.perf_counter()
+    ids, w = orc.route(d["logits"].numpy(), wl.k)
+    orc.layer_rows(xb, ids, w, gu, dn, rows)
+    return time.perf_counter() - t0, len(rows)
+
+
+def _oracle_tokens_for(wl, seconds: float) -> int:
+    per_token_macs = wl.k * 3 * wl.H * wl.I
+    est = 5.0e8  # fp64 decode + multiply-add per second on one core (measured order of magnitude)
+    return int(max(1, min(wl.T, round(seconds * est / per_token_macs))))
+
+
+def oracle_baseline(d, wl, budget_s: float):
+    """Repeat seeded oracle samples until about budget_s of CPU time; returns (seconds, tokens, reps, n)."""
+    n = _oracle_tokens_for(wl, min(budget_s, 5.0))
+    total, toks, reps = 0.0, 0, 0
+    while total < budget_s or reps < 1:
+        dt, nt = oracle_sample(d, wl, n, seed=reps)
+        total += dt
+        toks += nt
+        reps += 1
+    return total, toks, reps, n
+
+
+def run_reference(args, wl, dist, rank, world):
+    if rank != 0:
+        return
+    d = wk.generate(wl)
+    n = _oracle_tokens_for(wl, args.ref_step_seconds)
+    for _ in range(min(args.warmup, 1)):
+        oracle_sample(d, wl, max(1, n // 4), seed=99)
+    total, toks = 0.0, 0
+    for s in range(args.steps):
+        dt, nt = oracle_sample(d, wl, n, seed=s)
+        total += dt
+        toks += nt
+    value = toks / total
+    sample = f"{n} of {wl.T} tokens per step (seeded), full routing of all {wl.T} tokens, fp64, 1 thread"
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
+        "config": {"workload": wl.name, "T": wl.T, "H": wl.H, "I": wl.I, "E": wl.E, "k": wl.k,
+                   "parallelism": "replicas" if args.gpus > 1 else "single"},
+        "impl": "reference",
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------ ours
+def _kernel_hash() -> str:
+    h = hashlib.sha256()
+    for f in ("gemm_w4a16.cu", "device_common.cuh"):
+        with open(os.path.join(ROOT, "moe_layer_bit_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def _traffic_from_profile(wl):
+    """Per-launch DRAM bytes of the gate_up kernel from the committed ncu summary, or None if the
+    summary is missing or was taken on a different kernel source."""
+    p = os.path.join(ROOT, "profiles", f"gate_up_{wl.name}.txt")
+    if not os.path.exists(p):
+        return None
+    kv = {}
+    with open(p) as f:
+        for line in f:
+            if ":" in line and not line.startswith("#"):
+                k, v = line.split(":", 1)
+                kv[k.strip()] = v.strip()
+    if kv.get("kernel_source_sha256_16") != _kernel_hash():
+        return None
+    try:
+        return float(kv["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+def run_ours(args, wl, dist, rank, world, local_rank):
+    from moe_layer_bit_gb300 import _lib, build
+    from moe_layer_bit_gb300.layer import MoELayer
+
+    if not torch.cuda.is_available():
+        raise RuntimeError("bench.py --impl ours needs a CUDA device")
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    if rank == 0:
+        build.build()
+    _barrier(dist)
+    _lib.load()
+    d = wk.generate(wl, seed=wl.seed + rank)
+    layer = MoELayer(d["gu"], d["dn"], wl.H, wl.I, wl.E, wl.k, wl.T, dev)
+    x = d["x"].to(dev)
+    logits = d["logits"].to(dev)
+    out = torch.empty(wl.T, wl.H, dtype=torch.bfloat16, device=dev)
+    ids = torch.empty(wl.T, wl.k, dtype=torch.int32, device=dev)
+    tw = torch.empty(wl.T, wl.k, dtype=torch.float32, device=dev)
+    dims = layer.dims(wl.T)
+    l2 = getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 126 * 2 ** 20)
+    flush = torch.empty(2 * l2 // 4 + 1024, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(evs):
+        _lib.moe_layer_forward_profiled(x, logits, layer.w_gate_up.abi, layer.w_down.abi, dims, out, ids, tw,
+                                        layer.ws, layer.ws_bytes, evs, stream)
+
+    warm_evs = [torch.cuda.Event(enable_timing=True) for _ in range(6)]
+    for _ in range(args.warmup):
+        flush.fill_(1.0)
+        step(warm_evs)
+    torch.cuda.synchronize(dev)
+    status = layer.device_status()
+    if status != _lib.MOE_OK:
+        raise RuntimeError(f"device status after warm-up: {_lib.status_string(status)}")
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(args.steps)]
+    # torch only reports elapsed time between events it has recorded itself; record
+    # each once here (the library records them again inside every timed step)
+    for e in evs:
+        for ev in e:
+            ev.record(stream)
+    torch.cuda.synchronize(dev)
+    clocks = ClockSampler(dev.index)
+    clocks.start()
+    _barrier(dist, dev)
+    torch.cuda.synchronize(dev)
+    t_wall0 = time.perf_counter()
+    for s in range(args.steps):
+        flush.fill_(float(s))                       # L2 flush, outside the step's events
+        step(evs[s])
+    torch.cuda.synchronize(dev)
+    t_wall = time.perf_counter() - t_wall0
+    _barrier(dist, dev)
+    clk = clocks.stop()
+    status = layer.device_status()
+    if status != _lib.MOE_OK:
+        raise RuntimeError(f"device status after timing: {_lib.status_string(status)}")
+
+    step_ms = [e[0].elapsed_time(e[5]) for e in evs]
+    stage_ms = np.array([[e[i].elapsed_time(e[i + 1]) for i in range(5)] for e in evs])
+    total_s = sum(step_ms) / 1e3
+    total_s_max = _max_over_ranks(dist, total_s, dev)
+    value = world * wl.T * args.steps / total_s_max
+
+    # ---- roofline of the dominant kernel (gate_up + SwiGLU), algorithmic bytes per launch
+    counts = np.bincount(ids.cpu().numpy().reshape(-1), minlength=wl.E)
+    touched = int(np.count_nonzero(counts))
+    n = wl.T * wl.k
+    gu_bytes = touched * (2 * wl.I * wl.H * 9 // 16 + 4) + n * wl.H * 2 + n * wl.I * 2
+    gu_ms = float(stage_ms[:, 2].mean())
+    hbm_peak, tf_peak, tf_sus, peak_kind = _peaks()
+    achieved = gu_bytes / (gu_ms * 1e-3) / 1e9
+    layer_bytes = wk.algorithmic_bytes(wl.T, wl.H, wl.I, wl.E, wl.k, counts)
+    layer_flops = wk.algorithmic_flops(wl.T, wl.H, wl.I, wl.k)
+    mean_step_ms = total_s * 1e3 / args.steps
+
+    # ---- end to end through the host-buffer entry point
+    xh = d["x"].pin_memory()
+    lh = d["logits"].pin_memory()
+    oh = torch.empty(wl.T, wl.H, dtype=torch.bfloat16).pin_memory()
+    for _ in range(max(3, args.warmup)):
+        layer.forward_host(xh, lh, oh, stream)
+    e2e_times = []
+    for s in range(args.steps):
+        flush.fill_(float(s))
+        torch.cuda.synchronize(dev)
+        t0 = time.perf_counter()
+        layer.forward_host(xh, lh, oh, stream)      # synchronises before returning
+        e2e_times.append(time.perf_counter() - t0)
+    e2e_total = _max_over_ranks(dist, sum(e2e_times), dev)
+    e2e_value = world * wl.T * args.steps / e2e_total
+
+    # ---- CPU oracle baseline on a bounded sample (rank 0, N = 1 only)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        dt, nt, reps, n_tok = oracle_baseline(d, wl, args.cpu_seconds)
+        cpu = {"value": nt / dt, "unit": UNIT, "cores": 1, "kind": "oracle",
+               "sample": f"{reps} x {n_tok} of {wl.T} tokens (seeded) after routing all {wl.T}; fp64, "
+                         f"single thread, {dt:.1f} s"}
+
+    if rank != 0:
+        return
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": mean_step_ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16 x nvfp4 (fp32 accumulate)", "data": "synthetic (seeded, random-init)",
+        "config": {"workload": wl.name, "T": wl.T, "H": wl.H, "I": wl.I, "E": wl.E, "k": wl.k,
+                   "parallelism": f"replicas x{world}" if world > 1 else "single",
+                   "l2": "flushed between steps (2x L2 write, outside the timed events)",
+                   "touched_experts": touched, "layer_bytes": layer_bytes, "layer_flops": layer_flops},
+        "roofline": {"bound": "hbm", "kernel": "w4a16_gemm_kernel (gate_up + SwiGLU)", "achieved": achieved,
+                     "peak": hbm_peak, "unit": "GB/s", "frac": achieved / hbm_peak,
+                     "peak_kind": f"{peak_kind} burst copy bandwidth",
+                     "traffic": _traffic_from_profile(wl), "algorithmic_bytes_per_launch": gu_bytes,
+                     "launch_ms": gu_ms},
+        "layer_roofline": {"achieved_gbs": layer_bytes / (mean_step_ms * 1e-3) / 1e9,
+                           "frac_hbm": layer_bytes / (mean_step_ms * 1e-3) / 1e9 / hbm_peak,
+                           "achieved_tflops": layer_flops / (mean_step_ms * 1e-3) / 1e12},
+        "stages_ms": {nm: float(stage_ms[:, i].mean()) for i, nm in
+                      enumerate(["route", "permute", "gate_up_swiglu", "down", "combine"])},
+        "wall_s_timed_loop": t_wall,
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": wl.T * wl.H * 2 + wl.T * wl.E * 4,
+                "d2h_bytes_per_step": wl.T * wl.H * 2},
+        "cpu_baseline": cpu,
+        "gpu_launches": 7 * args.steps,
+        "clocks": clk,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target length of the CPU oracle sample")
+    ap.add_argument("--ref-step-seconds", type=float, default=1.5)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        ap.error("--warmup must be >= 3")
+    wl = wk.by_name(args.workload)
+    dist, rank, world, local_rank = _dist_init(args)
+    try:
+        if args.impl == "reference":
+            run_reference(args, wl, dist, rank, world)
+        else:
+            run_ours(args, wl, dist, rank, world, local_rank)
+    finally:
+        if dist is not None:
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

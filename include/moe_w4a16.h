@@ -1,0 +1,212 @@
+/*
+ * moe_w4a16.h -- C ABI of libmoe_w4a16.so: a W4A16 NVFP4 mixture-of-experts
+ * FFN layer for NVIDIA GB300 (sm_103a).
+ *
+ * The layer (top-k routing -> permutation grouped by expert -> grouped
+ * gate_up GEMM with SwiGLU -> grouped down GEMM -> weighted combine) is the
+ * MoE layer described by:
+ *   [Atlas]  "告别Python堆栈：Atlas用纯Rust重写LLM推理，在GB10上跑赢vLLM"
+ *            (f.mffb.com.cn/a/497905.html), section "编译时内核选择和W4A16 Grouped
+ *            GEMM": per-expert gate_up and down projections run by ONE grouped
+ *            launch over all experts; packed FP4 weights are dequantised to
+ *            BF16 on chip and fed to a BF16 MMA, with no BF16 weight written
+ *            back to memory.  Section "KV Cache量化、MTP推测解码和调试工具链":
+ *            gate logits -> expert IDs -> routed output.
+ *   [ATOM]   "AMD ATOM推理引擎：如何用分页KV缓存和分段编译实现大模型推理性能翻倍"
+ *            (itsolotime.com/archives/33112), section "8.1 MoE 路径": routing,
+ *            top-k selection, expert compute, combine; section "8.2 量化并非单一
+ *            格式，而是一套执行契约": a quantisation format fixes dtype, scale
+ *            shape and whether weights are pre-shuffled for the kernel.
+ *   [Rust DL] "Rust 实现深度学习推理引擎：从计算图到异构硬件加速"
+ *            (ybb.press/ai-applications/14151.html), section "三、计算图":
+ *            SiLU / SwiGLU activation.
+ *
+ * Conventions for every entry point
+ *  - Shapes: T tokens, H hidden, I expert intermediate, E experts, k top-k.
+ *    Row-major everywhere.  Supported: T >= 0, H % 128 == 0, I % 64 == 0,
+ *    1 <= k <= min(E, 32), 1 <= E <= 1024, T*k < 2^31, H, I <= 65536.
+ *  - bf16 arrays are passed as uint16_t bit patterns.
+ *  - All pointers are DEVICE pointers unless the name says host_; the caller
+ *    owns every buffer.  Device arrays must be 16-byte aligned.
+ *  - Every call is asynchronous on `stream` (a cudaStream_t; NULL = legacy
+ *    default stream) and does not synchronise, except where stated.
+ *  - Arguments are validated before anything is launched; on error nothing
+ *    is launched and no output is touched.
+ *  - Return value: a moe_status.  A launch failure returns MOE_ERR_CUDA and
+ *    clears the CUDA error state (cudaGetLastError).
+ *  - A kernel whose internal wait (a pipeline barrier) runs past about one
+ *    second gives up, records MOE_ERR_DEVICE_TIMEOUT in the workspace's status
+ *    word and returns; moe_get_device_status() reads it.
+ *  - The library keeps no global mutable state and allocates no memory:
+ *    every intermediate lives in the caller's workspace `ws`.
+ */
+#ifndef MOE_W4A16_H
+#define MOE_W4A16_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    MOE_OK = 0,
+    MOE_ERR_INVALID_ARG = 1,        /* null pointer, k > E, k > 32, E > 1024, negative size */
+    MOE_ERR_UNSUPPORTED_SHAPE = 2,  /* H % 128, I % 64, or a size beyond the limits above */
+    MOE_ERR_MISALIGNED = 3,         /* a device pointer not 16-byte aligned */
+    MOE_ERR_WORKSPACE_TOO_SMALL = 4,
+    MOE_ERR_CUDA = 5,               /* a CUDA runtime / driver call failed */
+    MOE_ERR_DEVICE_TIMEOUT = 6      /* a kernel's bounded wait expired (reported by moe_get_device_status) */
+} moe_status;
+
+typedef struct {
+    int32_t T, H, I, E, k;
+} moe_dims;
+
+/* Which projection a packed weight buffer holds. */
+typedef enum {
+    MOE_PROJ_GATE_UP = 0,  /* N = 2I rows (rows 0..I-1 gate, I..2I-1 up), K = H */
+    MOE_PROJ_DOWN = 1      /* N = H rows, K = I */
+} moe_projection;
+
+/* ------------------------------------------------------------------------
+ * NVFP4 weights.
+ * Interchange ("natural") layout of one projection with N rows and K columns
+ * per expert:
+ *   codes   uint8 [E][N][K/2]  E2M1 codes, element 2i in the low nibble,
+ *                              2i+1 in the high nibble;
+ *   scales  uint8 [E][N][K/16] one E4M3 block scale per 16 consecutive K;
+ *   global  float [E]          one fp32 global scale per expert matrix;
+ *   weight[e][n][kk] = e2m1(code) * e4m3(scale) * global[e].
+ * The GEMM entry points read the "packed" layout made once by
+ * moe_prepack_w4 (the pre-shuffle of [ATOM] section 8.2): same bytes,
+ * reordered into 128-row x 64-column tiles so that each pipeline stage is one
+ * contiguous copy.  The packed buffer has exactly E*N*K*9/16 bytes.
+ * ------------------------------------------------------------------------ */
+typedef struct {
+    const void *packed;          /* from moe_prepack_w4, device */
+    const float *global_scale;   /* [E], device */
+} moe_w4;
+
+/* Bytes of a packed buffer for E experts of an N x K projection. */
+size_t moe_packed_w4_bytes(int32_t E, int32_t N, int32_t K);
+
+/* One-time re-layout of natural NVFP4 weights (device codes/scales) into the
+ * packed layout (device `packed`, moe_packed_w4_bytes bytes, must not overlap
+ * the inputs).  `proj` selects the row order: gate_up rows are interleaved
+ * gate/up in groups of 16 so that one 128-row tile holds 64 gate rows and
+ * the 64 matching up rows.  N, K as for `proj` (gate_up: N = 2I, K = H;
+ * down: N = H, K = I); N % 128 == 0, K % 64 == 0.  Pure byte permutation. */
+int moe_prepack_w4(const uint8_t *codes, const uint8_t *scales, int32_t E, int32_t N, int32_t K,
+                   int32_t proj, void *packed, void *stream);
+
+/* ------------------------------------------------------------------------
+ * Workspace.  moe_workspace_bytes(d) is the size that moe_layer_forward and
+ * moe_layer_forward_host need; the stage entry points need at least
+ * moe_stage_workspace_bytes(d).  Device memory, 256-byte aligned, owned by
+ * the caller.  The first 4 bytes are the device status word: zero-fill the
+ * workspace (or at least those bytes) once before its first use; kernels only
+ * ever write a timeout code there, and moe_get_device_status clears it after
+ * reading.  Nothing else in the workspace needs initialisation.
+ * T == 0 is valid everywhere: nothing is launched except that moe_permute
+ * writes zero counts and offsets; token-sized arrays may then be NULL.
+ * ------------------------------------------------------------------------ */
+size_t moe_workspace_bytes(moe_dims d);
+size_t moe_stage_workspace_bytes(moe_dims d);
+
+/* [Atlas] "KV Cache量化…" (gate logits -> expert IDs), [ATOM] 8.1 (top-k).
+ * logits  float [T][E]   router logits (NaN is treated as -infinity)
+ * topk_ids int32 [T][k]  out: selected experts, slot order = descending logit,
+ *                        ties to the lower expert index
+ * topk_w  float [T][k]   out: softmax over the k selected logits (equal to
+ *                        softmax over E renormalised over the k); 1/k each if
+ *                        the best logit is -infinity. */
+int moe_route_topk(const float *logits, moe_dims d, int32_t *topk_ids, float *topk_w, void *stream);
+
+/* Permutation grouped by expert ([Atlas] per-expert M tiles; [ATOM] 8.1).
+ * topk_ids int32 [T][k]; x bf16 [T][H].
+ * counts   int32 [E]    out: pairs (t, j) routed to each expert
+ * offsets  int32 [E+1]  out: exclusive scan of counts, offsets[E] = T*k
+ * sorted_token int32 [T*k] out: token of sorted row p; rows sorted by (expert, token)
+ * inv_perm int32 [T*k]  out: sorted row of pair (t, j) at index t*k+j
+ * x_perm   bf16 [T*k][H] out: x_perm[p] = x[sorted_token[p]]
+ * Deterministic and bit-exact.  Needs moe_stage_workspace_bytes(d) of ws. */
+int moe_permute(const int32_t *topk_ids, const uint16_t *x, moe_dims d, int32_t *counts,
+                int32_t *offsets, int32_t *sorted_token, int32_t *inv_perm, uint16_t *x_perm,
+                void *ws, size_t ws_bytes, void *stream);
+
+/* Grouped gate_up GEMM + SwiGLU, one launch over all experts ([Atlas] W4A16
+ * Grouped GEMM; [Rust DL] SwiGLU).  For expert e and rows p in
+ * [offsets[e], offsets[e+1]):
+ *   g = x_perm[p] . Wgate_e^T,  u = x_perm[p] . Wup_e^T  (fp32 accumulation of
+ *   bf16 x bf16 products; weights dequantised exactly to bf16 on chip),
+ *   h[p] = bf16_rne(silu(g) * u),  silu(z) = z / (1 + exp(-z)).
+ * x_perm bf16 [T*k][H]; offsets int32 [E+1] (from moe_permute);
+ * w_gate_up packed gate_up weights; h bf16 [T*k][I] out. */
+int moe_w4a16_gate_up_swiglu(const uint16_t *x_perm, const int32_t *offsets, moe_w4 w_gate_up,
+                             moe_dims d, uint16_t *h, void *ws, size_t ws_bytes, void *stream);
+
+/* Grouped down GEMM ([Atlas]: the same grouped W4A16 launch for "down").
+ *   y_perm[p] = h[p] . Wdown_e^T   (fp32 accumulation, fp32 result)
+ * h bf16 [T*k][I]; y_perm float [T*k][H] out. */
+int moe_w4a16_down(const uint16_t *h, const int32_t *offsets, moe_w4 w_down, moe_dims d,
+                   float *y_perm, void *ws, size_t ws_bytes, void *stream);
+
+/* Weighted combine back to token order ([ATOM] 8.1 "combine"):
+ *   out[t] = bf16_rne( sum_{j=0..k-1} topk_w[t][j] * y_perm[inv_perm[t*k+j]] ),
+ * fp32 sum in ascending j.  Every element of out is written. */
+int moe_unpermute_combine(const float *y_perm, const int32_t *inv_perm, const float *topk_w,
+                          moe_dims d, uint16_t *out, void *stream);
+
+/* The whole layer: route -> permute -> gate_up+SwiGLU -> down -> combine,
+ * stream-ordered, no host synchronisation.  topk_ids / topk_w may be NULL
+ * (then they live in ws).  Needs moe_workspace_bytes(d) of ws. */
+int moe_layer_forward(const uint16_t *x, const float *logits, moe_w4 w_gate_up, moe_w4 w_down,
+                      moe_dims d, uint16_t *out, int32_t *topk_ids, float *topk_w, void *ws,
+                      size_t ws_bytes, void *stream);
+
+/* moe_layer_forward with per-stage timing: stage_events points to 6
+ * cudaEvent_t handles (created by the caller; any entry may be NULL).
+ * stage_events[i] is recorded on `stream` just before stage i (0 route,
+ * 1 permute, 2 gate_up+SwiGLU, 3 down, 4 combine) and stage_events[5] after
+ * the last, so cudaEventElapsedTime(ev[2], ev[3]) is the gate_up launch.
+ * Same results and launches as moe_layer_forward. */
+int moe_layer_forward_profiled(const uint16_t *x, const float *logits, moe_w4 w_gate_up, moe_w4 w_down,
+                               moe_dims d, uint16_t *out, int32_t *topk_ids, float *topk_w, void *ws,
+                               size_t ws_bytes, void *stream, void *const *stage_events);
+
+/* The whole layer from HOST buffers: copies host_x (bf16 [T][H]) and
+ * host_logits (float [T][E]) into ws, runs moe_layer_forward, copies the
+ * result to host_out (bf16 [T][H]) and synchronises `stream` before returning.
+ * Host buffers should be page-locked for full copy speed.  Weights stay on the
+ * device.  Needs moe_workspace_bytes(d) of ws. */
+int moe_layer_forward_host(const uint16_t *host_x, const float *host_logits, moe_w4 w_gate_up,
+                           moe_w4 w_down, moe_dims d, uint16_t *host_out, void *ws, size_t ws_bytes,
+                           void *stream);
+
+/* Synchronises `stream`, then reads and clears the device status word in ws
+ * (any workspace passed to the calls above).  Returns MOE_OK,
+ * MOE_ERR_DEVICE_TIMEOUT, or MOE_ERR_CUDA. */
+int moe_get_device_status(void *ws, void *stream);
+
+/* Human-readable name of a moe_status. */
+const char *moe_status_string(int status);
+
+/* Test hook: runs the GEMM kernels' on-chip NVFP4 -> bf16 dequantisation on
+ * every (E4M3 scale, E2M1 code) pair and writes out[s*16 + c] =
+ * bf16(e2m1(c) * e4m3(s)) (exact: at most 6 significant bits).
+ * out: device uint16 [256*16]. */
+int moe_debug_dequant_table(uint16_t *out, void *stream);
+
+/* Test hook for failure detection: launches a kernel whose pipeline wait can
+ * never complete (an mbarrier nobody arrives at) with a wait limit of
+ * `limit_ns` nanoseconds.  The wait gives up, records MOE_ERR_DEVICE_TIMEOUT in
+ * the status word at the start of `ws` and the kernel returns; read it with
+ * moe_get_device_status.  Nothing faults and the context stays usable. */
+int moe_debug_timeout_probe(void *ws, uint64_t limit_ns, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_W4A16_H */

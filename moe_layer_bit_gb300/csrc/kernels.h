@@ -1,0 +1,51 @@
+// kernels.h -- host-side launchers of the library's kernels (internal).
+#pragma once
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace moe {
+
+// Packed NVFP4 layout: tiles of 128 weight rows x 64 K elements, 4608 bytes each.
+constexpr int kTileM = 128;
+constexpr int kBlockK = 64;
+constexpr int kWBlockBytes = 4608;
+
+cudaError_t launch_route_topk(const float* logits, int T, int E, int k, int32_t* ids, float* w, cudaStream_t s);
+
+size_t perm_scratch_bytes(int T, int E, int k);
+cudaError_t launch_permute(const int32_t* ids, const uint16_t* x, int T, int H, int E, int k, int32_t* counts,
+                           int32_t* offsets, int32_t* sorted_token, int32_t* inv_perm, uint16_t* x_perm,
+                           int32_t* scratch, cudaStream_t s);
+
+cudaError_t launch_combine(const float* y, const int32_t* inv, const float* w, int T, int H, int k, uint16_t* out,
+                           cudaStream_t s);
+
+cudaError_t launch_prepack(const uint8_t* codes, const uint8_t* scales, int E, int N, int K, int proj,
+                           uint8_t* packed, cudaStream_t s);
+
+cudaError_t launch_dequant_table(uint16_t* out, cudaStream_t s);
+
+// Grouped W4A16 GEMM.  mode 0: gate_up + SwiGLU -> bf16 h [rows][I];
+// mode 1: down -> fp32 y [rows][H].  `act` is the bf16 activation matrix
+// [rows = T*k][K]; N = rows of the weight per expert (2I or H).
+struct GemmArgs {
+  const uint16_t* act;
+  const uint8_t* packed;
+  const float* gscale;
+  const int32_t* offsets;
+  void* out;
+  int* status;
+  int rows;  // T*k
+  int E, N, K;
+  int out_ld;  // I (mode 0) or H (mode 1)
+  int T, k;
+};
+cudaError_t launch_gemm(int mode, const GemmArgs& a, cudaStream_t s);
+
+// Bounded-wait self test: a kernel waits on a barrier nobody arrives at and
+// must give up after `limit_ns`, recording a timeout in `status`.
+cudaError_t launch_timeout_probe(int* status, unsigned long long limit_ns, cudaStream_t s);
+
+}  // namespace moe

@@ -1,0 +1,353 @@
+// moe_abi.cu -- the extern "C" entry points of libmoe_w4a16.so (declared in
+// include/moe_w4a16.h): argument validation, workspace carving and launches.
+#include <cstdint>
+#include <cstdlib>
+#include <cstring>
+#include <initializer_list>
+#include <cuda_runtime.h>
+
+#include "../../include/moe_w4a16.h"
+#include "kernels.h"
+
+namespace moe {
+cudaError_t launch_gemm_simt(int mode, const GemmArgs& a, cudaStream_t s);
+}
+
+namespace {
+
+constexpr size_t kAlign = 256;
+inline size_t align_up(size_t v) { return (v + kAlign - 1) & ~(kAlign - 1); }
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+inline cudaStream_t as_stream(void* s) { return reinterpret_cast<cudaStream_t>(s); }
+
+// Workspace layout: the status word always sits at offset 0.
+struct Layout {
+  size_t status, perm, ids, w, counts, offsets, sorted_token, inv_perm, x_perm, h, y, hx, hlogits, hout, stage_total,
+      total;
+};
+
+Layout layout_of(const moe_dims& d) {
+  Layout L{};
+  const size_t n = (size_t)d.T * d.k;
+  size_t o = 0;
+  L.status = o;
+  o = align_up(o + sizeof(int));
+  L.perm = o;
+  o = align_up(o + moe::perm_scratch_bytes(d.T, d.E, d.k));
+  L.stage_total = o;
+  L.ids = o;
+  o = align_up(o + n * sizeof(int32_t));
+  L.w = o;
+  o = align_up(o + n * sizeof(float));
+  L.counts = o;
+  o = align_up(o + (size_t)d.E * sizeof(int32_t));
+  L.offsets = o;
+  o = align_up(o + (size_t)(d.E + 1) * sizeof(int32_t));
+  L.sorted_token = o;
+  o = align_up(o + n * sizeof(int32_t));
+  L.inv_perm = o;
+  o = align_up(o + n * sizeof(int32_t));
+  L.x_perm = o;
+  o = align_up(o + n * (size_t)d.H * 2);
+  L.h = o;
+  o = align_up(o + n * (size_t)d.I * 2);
+  L.y = o;
+  o = align_up(o + n * (size_t)d.H * sizeof(float));
+  L.hx = o;
+  o = align_up(o + (size_t)d.T * d.H * 2);
+  L.hlogits = o;
+  o = align_up(o + (size_t)d.T * d.E * sizeof(float));
+  L.hout = o;
+  o = align_up(o + (size_t)d.T * d.H * 2);
+  L.total = o;
+  return L;
+}
+
+int check_dims(const moe_dims& d) {
+  if (d.T < 0 || d.H <= 0 || d.I <= 0 || d.E < 1 || d.k < 1) return MOE_ERR_INVALID_ARG;
+  if (d.k > d.E || d.k > 32 || d.E > 1024) return MOE_ERR_INVALID_ARG;
+  if (d.H % 128 != 0 || d.I % 64 != 0) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (d.H > 65536 || d.I > 65536) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if ((long long)d.T * d.k >= (1LL << 31)) return MOE_ERR_UNSUPPORTED_SHAPE;
+  return MOE_OK;
+}
+
+int check_ptrs(std::initializer_list<const void*> ps) {
+  for (const void* p : ps)
+    if (p == nullptr) return MOE_ERR_INVALID_ARG;
+  for (const void* p : ps)
+    if (!aligned16(p)) return MOE_ERR_MISALIGNED;
+  return MOE_OK;
+}
+
+int cuda_status(cudaError_t e) {
+  if (e == cudaSuccess) return MOE_OK;
+  (void)cudaGetLastError();
+  return MOE_ERR_CUDA;
+}
+
+bool use_simt() {
+  static int v = -1;
+  if (v < 0) {
+    const char* s = std::getenv("MOE_GEMM_IMPL");
+    v = (s != nullptr && std::strcmp(s, "simt") == 0) ? 1 : 0;
+  }
+  return v == 1;
+}
+
+cudaError_t run_gemm(int mode, const moe::GemmArgs& a, cudaStream_t s) {
+  return use_simt() ? moe::launch_gemm_simt(mode, a, s) : moe::launch_gemm(mode, a, s);
+}
+
+#define MOE_TRY(expr)            \
+  do {                           \
+    int _rc = (expr);            \
+    if (_rc != MOE_OK) return _rc; \
+  } while (0)
+
+}  // namespace
+
+extern "C" {
+
+size_t moe_packed_w4_bytes(int32_t E, int32_t N, int32_t K) {
+  if (E <= 0 || N <= 0 || K <= 0) return 0;
+  return (size_t)E * (size_t)N * (size_t)K * 9 / 16;
+}
+
+int moe_prepack_w4(const uint8_t* codes, const uint8_t* scales, int32_t E, int32_t N, int32_t K, int32_t proj,
+                   void* packed, void* stream) {
+  if (E < 1 || N <= 0 || K <= 0 || (proj != MOE_PROJ_GATE_UP && proj != MOE_PROJ_DOWN)) return MOE_ERR_INVALID_ARG;
+  if (N % 128 != 0 || K % 64 != 0) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (codes == nullptr || scales == nullptr || packed == nullptr) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(packed)) return MOE_ERR_MISALIGNED;
+  return cuda_status(moe::launch_prepack(codes, scales, E, N, K, proj, static_cast<uint8_t*>(packed),
+                                         as_stream(stream)));
+}
+
+size_t moe_workspace_bytes(moe_dims d) {
+  if (check_dims(d) != MOE_OK) return 0;
+  return layout_of(d).total;
+}
+
+size_t moe_stage_workspace_bytes(moe_dims d) {
+  if (check_dims(d) != MOE_OK) return 0;
+  return layout_of(d).stage_total;
+}
+
+int moe_route_topk(const float* logits, moe_dims d, int32_t* topk_ids, float* topk_w, void* stream) {
+  MOE_TRY(check_dims(d));
+  if (d.T == 0) return MOE_OK;
+  MOE_TRY(check_ptrs({logits, topk_ids, topk_w}));
+  return cuda_status(moe::launch_route_topk(logits, d.T, d.E, d.k, topk_ids, topk_w, as_stream(stream)));
+}
+
+int moe_permute(const int32_t* topk_ids, const uint16_t* x, moe_dims d, int32_t* counts, int32_t* offsets,
+                int32_t* sorted_token, int32_t* inv_perm, uint16_t* x_perm, void* ws, size_t ws_bytes,
+                void* stream) {
+  MOE_TRY(check_dims(d));
+  if (d.T == 0) MOE_TRY(check_ptrs({counts, offsets, ws}));
+  else MOE_TRY(check_ptrs({topk_ids, x, counts, offsets, sorted_token, inv_perm, x_perm, ws}));
+  const Layout L = layout_of(d);
+  if (ws_bytes < L.stage_total) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  return cuda_status(moe::launch_permute(topk_ids, x, d.T, d.H, d.E, d.k, counts, offsets, sorted_token, inv_perm,
+                                         x_perm, reinterpret_cast<int32_t*>(w + L.perm), as_stream(stream)));
+}
+
+int moe_w4a16_gate_up_swiglu(const uint16_t* x_perm, const int32_t* offsets, moe_w4 w_gate_up, moe_dims d,
+                             uint16_t* h, void* ws, size_t ws_bytes, void* stream) {
+  MOE_TRY(check_dims(d));
+  if (d.T == 0) return MOE_OK;
+  MOE_TRY(check_ptrs({x_perm, offsets, w_gate_up.packed, w_gate_up.global_scale, h, ws}));
+  const Layout L = layout_of(d);
+  if (ws_bytes < L.stage_total) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  moe::GemmArgs a{};
+  a.act = x_perm;
+  a.packed = static_cast<const uint8_t*>(w_gate_up.packed);
+  a.gscale = w_gate_up.global_scale;
+  a.offsets = offsets;
+  a.out = h;
+  a.status = reinterpret_cast<int*>(static_cast<uint8_t*>(ws) + L.status);
+  a.rows = d.T * d.k;
+  a.E = d.E;
+  a.N = 2 * d.I;
+  a.K = d.H;
+  a.out_ld = d.I;
+  a.T = d.T;
+  a.k = d.k;
+  return cuda_status(run_gemm(0, a, as_stream(stream)));
+}
+
+int moe_w4a16_down(const uint16_t* h, const int32_t* offsets, moe_w4 w_down, moe_dims d, float* y_perm, void* ws,
+                   size_t ws_bytes, void* stream) {
+  MOE_TRY(check_dims(d));
+  if (d.T == 0) return MOE_OK;
+  MOE_TRY(check_ptrs({h, offsets, w_down.packed, w_down.global_scale, y_perm, ws}));
+  const Layout L = layout_of(d);
+  if (ws_bytes < L.stage_total) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  moe::GemmArgs a{};
+  a.act = h;
+  a.packed = static_cast<const uint8_t*>(w_down.packed);
+  a.gscale = w_down.global_scale;
+  a.offsets = offsets;
+  a.out = y_perm;
+  a.status = reinterpret_cast<int*>(static_cast<uint8_t*>(ws) + L.status);
+  a.rows = d.T * d.k;
+  a.E = d.E;
+  a.N = d.H;
+  a.K = d.I;
+  a.out_ld = d.H;
+  a.T = d.T;
+  a.k = d.k;
+  return cuda_status(run_gemm(1, a, as_stream(stream)));
+}
+
+int moe_unpermute_combine(const float* y_perm, const int32_t* inv_perm, const float* topk_w, moe_dims d,
+                          uint16_t* out, void* stream) {
+  MOE_TRY(check_dims(d));
+  if (d.T == 0) return MOE_OK;
+  MOE_TRY(check_ptrs({y_perm, inv_perm, topk_w, out}));
+  return cuda_status(moe::launch_combine(y_perm, inv_perm, topk_w, d.T, d.H, d.k, out, as_stream(stream)));
+}
+
+}  // extern "C"
+
+namespace {
+
+// The layer, optionally recording ev[0..5] around the five stages
+// (ev[i] before stage i, ev[5] after the last).
+int layer_forward_impl(const uint16_t* x, const float* logits, moe_w4 w_gate_up, moe_w4 w_down, moe_dims d,
+                       uint16_t* out, int32_t* topk_ids, float* topk_w, void* ws, size_t ws_bytes, void* stream,
+                       void* const* ev) {
+  MOE_TRY(check_dims(d));
+  if (d.T == 0) return MOE_OK;
+  MOE_TRY(check_ptrs({x, logits, w_gate_up.packed, w_gate_up.global_scale, w_down.packed, w_down.global_scale, out,
+                      ws}));
+  if ((topk_ids != nullptr && !aligned16(topk_ids)) || (topk_w != nullptr && !aligned16(topk_w)))
+    return MOE_ERR_MISALIGNED;
+  const Layout L = layout_of(d);
+  if (ws_bytes < L.total) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  cudaStream_t s = as_stream(stream);
+  auto mark = [&](int i) -> int {
+    if (ev == nullptr || ev[i] == nullptr) return MOE_OK;
+    return cuda_status(cudaEventRecord(reinterpret_cast<cudaEvent_t>(ev[i]), s));
+  };
+  int32_t* ids = topk_ids ? topk_ids : reinterpret_cast<int32_t*>(w + L.ids);
+  float* wts = topk_w ? topk_w : reinterpret_cast<float*>(w + L.w);
+  int32_t* counts = reinterpret_cast<int32_t*>(w + L.counts);
+  int32_t* offs = reinterpret_cast<int32_t*>(w + L.offsets);
+  int32_t* sorted = reinterpret_cast<int32_t*>(w + L.sorted_token);
+  int32_t* inv = reinterpret_cast<int32_t*>(w + L.inv_perm);
+  uint16_t* xp = reinterpret_cast<uint16_t*>(w + L.x_perm);
+  uint16_t* h = reinterpret_cast<uint16_t*>(w + L.h);
+  float* y = reinterpret_cast<float*>(w + L.y);
+  MOE_TRY(mark(0));
+  MOE_TRY(cuda_status(moe::launch_route_topk(logits, d.T, d.E, d.k, ids, wts, s)));
+  MOE_TRY(mark(1));
+  MOE_TRY(cuda_status(moe::launch_permute(ids, x, d.T, d.H, d.E, d.k, counts, offs, sorted, inv, xp,
+                                          reinterpret_cast<int32_t*>(w + L.perm), s)));
+  MOE_TRY(mark(2));
+  moe::GemmArgs a{};
+  a.offsets = offs;
+  a.status = reinterpret_cast<int*>(w + L.status);
+  a.rows = d.T * d.k;
+  a.E = d.E;
+  a.T = d.T;
+  a.k = d.k;
+  a.act = xp;
+  a.packed = static_cast<const uint8_t*>(w_gate_up.packed);
+  a.gscale = w_gate_up.global_scale;
+  a.out = h;
+  a.N = 2 * d.I;
+  a.K = d.H;
+  a.out_ld = d.I;
+  MOE_TRY(cuda_status(run_gemm(0, a, s)));
+  MOE_TRY(mark(3));
+  a.act = h;
+  a.packed = static_cast<const uint8_t*>(w_down.packed);
+  a.gscale = w_down.global_scale;
+  a.out = y;
+  a.N = d.H;
+  a.K = d.I;
+  a.out_ld = d.H;
+  MOE_TRY(cuda_status(run_gemm(1, a, s)));
+  MOE_TRY(mark(4));
+  MOE_TRY(cuda_status(moe::launch_combine(y, inv, wts, d.T, d.H, d.k, out, s)));
+  return mark(5);
+}
+
+}  // namespace
+
+extern "C" {
+
+int moe_layer_forward(const uint16_t* x, const float* logits, moe_w4 w_gate_up, moe_w4 w_down, moe_dims d,
+                      uint16_t* out, int32_t* topk_ids, float* topk_w, void* ws, size_t ws_bytes, void* stream) {
+  return layer_forward_impl(x, logits, w_gate_up, w_down, d, out, topk_ids, topk_w, ws, ws_bytes, stream, nullptr);
+}
+
+int moe_layer_forward_profiled(const uint16_t* x, const float* logits, moe_w4 w_gate_up, moe_w4 w_down, moe_dims d,
+                               uint16_t* out, int32_t* topk_ids, float* topk_w, void* ws, size_t ws_bytes,
+                               void* stream, void* const* stage_events) {
+  return layer_forward_impl(x, logits, w_gate_up, w_down, d, out, topk_ids, topk_w, ws, ws_bytes, stream,
+                            stage_events);
+}
+
+int moe_layer_forward_host(const uint16_t* host_x, const float* host_logits, moe_w4 w_gate_up, moe_w4 w_down,
+                           moe_dims d, uint16_t* host_out, void* ws, size_t ws_bytes, void* stream) {
+  MOE_TRY(check_dims(d));
+  if (d.T == 0) return MOE_OK;
+  if (host_x == nullptr || host_logits == nullptr || host_out == nullptr) return MOE_ERR_INVALID_ARG;
+  MOE_TRY(check_ptrs({w_gate_up.packed, w_gate_up.global_scale, w_down.packed, w_down.global_scale, ws}));
+  const Layout L = layout_of(d);
+  if (ws_bytes < L.total) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  cudaStream_t s = as_stream(stream);
+  const size_t xb = (size_t)d.T * d.H * 2, lb = (size_t)d.T * d.E * sizeof(float);
+  uint16_t* dx = reinterpret_cast<uint16_t*>(w + L.hx);
+  float* dl = reinterpret_cast<float*>(w + L.hlogits);
+  uint16_t* dout = reinterpret_cast<uint16_t*>(w + L.hout);
+  if (xb) MOE_TRY(cuda_status(cudaMemcpyAsync(dx, host_x, xb, cudaMemcpyHostToDevice, s)));
+  if (lb) MOE_TRY(cuda_status(cudaMemcpyAsync(dl, host_logits, lb, cudaMemcpyHostToDevice, s)));
+  MOE_TRY(moe_layer_forward(dx, dl, w_gate_up, w_down, d, dout, nullptr, nullptr, ws, ws_bytes, stream));
+  if (xb) MOE_TRY(cuda_status(cudaMemcpyAsync(host_out, dout, xb, cudaMemcpyDeviceToHost, s)));
+  return cuda_status(cudaStreamSynchronize(s));
+}
+
+int moe_get_device_status(void* ws, void* stream) {
+  if (ws == nullptr) return MOE_ERR_INVALID_ARG;
+  cudaStream_t s = as_stream(stream);
+  if (cudaStreamSynchronize(s) != cudaSuccess) return cuda_status(cudaErrorUnknown);
+  int v = 0;
+  if (cudaMemcpy(&v, ws, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return cuda_status(cudaErrorUnknown);
+  if (v != 0) {
+    if (cudaMemset(ws, 0, sizeof(int)) != cudaSuccess) return cuda_status(cudaErrorUnknown);
+  }
+  return v == 0 ? MOE_OK : (v == MOE_ERR_DEVICE_TIMEOUT ? MOE_ERR_DEVICE_TIMEOUT : MOE_ERR_CUDA);
+}
+
+const char* moe_status_string(int status) {
+  switch (status) {
+    case MOE_OK: return "MOE_OK";
+    case MOE_ERR_INVALID_ARG: return "MOE_ERR_INVALID_ARG";
+    case MOE_ERR_UNSUPPORTED_SHAPE: return "MOE_ERR_UNSUPPORTED_SHAPE";
+    case MOE_ERR_MISALIGNED: return "MOE_ERR_MISALIGNED";
+    case MOE_ERR_WORKSPACE_TOO_SMALL: return "MOE_ERR_WORKSPACE_TOO_SMALL";
+    case MOE_ERR_CUDA: return "MOE_ERR_CUDA";
+    case MOE_ERR_DEVICE_TIMEOUT: return "MOE_ERR_DEVICE_TIMEOUT";
+    default: return "MOE_ERR_UNKNOWN";
+  }
+}
+
+int moe_debug_dequant_table(uint16_t* out, void* stream) {
+  MOE_TRY(check_ptrs({out}));
+  return cuda_status(moe::launch_dequant_table(out, as_stream(stream)));
+}
+
+int moe_debug_timeout_probe(void* ws, uint64_t limit_ns, void* stream) {
+  MOE_TRY(check_ptrs({ws}));
+  return cuda_status(moe::launch_timeout_probe(static_cast<int*>(ws), (unsigned long long)limit_ns,
+                                               as_stream(stream)));
+}
+
+}  // extern "C"

@@ -1,0 +1,81 @@
+"""Python-side convenience around the C ABI: device weights, workspace, forward.
+
+Marshalling only -- allocation of device buffers with torch and calls into
+libmoe_w4a16.so.  The layer is the W4A16 NVFP4 MoE FFN of the Atlas article
+(f.mffb.com.cn/a/497905.html, section "编译时内核选择和W4A16 Grouped GEMM").
+"""
+from __future__ import annotations
+
+import dataclasses
+
+import torch
+
+from . import _lib
+
+
+@dataclasses.dataclass
+class PackedProjection:
+    packed: torch.Tensor        # uint8, moe_packed_w4_bytes(E, N, K)
+    global_scale: torch.Tensor  # float32 [E]
+    E: int
+    N: int
+    K: int
+
+    @property
+    def abi(self) -> _lib.W4:
+        return _lib.w4(self.packed, self.global_scale)
+
+
+def pack_projection(codes: torch.Tensor, scales: torch.Tensor, global_scale: torch.Tensor, proj: int,
+                    device="cuda", stream=None) -> PackedProjection:
+    """Upload natural-layout NVFP4 weights (codes [E,N,K/2], scales [E,N,K/16], gs [E]) and
+    re-lay them out once with moe_prepack_w4."""
+    E, N, K2 = codes.shape
+    K = 2 * K2
+    c = codes.to(device, non_blocking=False).contiguous()
+    s = scales.to(device).contiguous()
+    out = torch.empty(_lib.moe_packed_w4_bytes(E, N, K), dtype=torch.uint8, device=device)
+    _lib.moe_prepack_w4(c, s, E, N, K, proj, out, stream)
+    gs = global_scale.to(device=device, dtype=torch.float32).contiguous()
+    torch.cuda.current_stream().synchronize() if stream is None else stream.synchronize()
+    del c, s
+    return PackedProjection(out, gs, E, N, K)
+
+
+class MoELayer:
+    """W4A16 NVFP4 MoE FFN layer for up to T_max tokens per call."""
+
+    def __init__(self, gu, dn, H: int, I: int, E: int, k: int, T_max: int, device="cuda"):
+        self.H, self.I, self.E, self.k, self.T_max = H, I, E, k, T_max
+        self.device = torch.device(device)
+        self.w_gate_up = pack_projection(*gu, _lib.MOE_PROJ_GATE_UP, device)
+        self.w_down = pack_projection(*dn, _lib.MOE_PROJ_DOWN, device)
+        d = _lib.dims(T_max, H, I, E, k)
+        self.ws_bytes = _lib.moe_workspace_bytes(d)
+        if self.ws_bytes == 0:
+            raise _lib.MoeError(_lib.MOE_ERR_UNSUPPORTED_SHAPE, "MoELayer")
+        self.ws = torch.zeros(self.ws_bytes, dtype=torch.uint8, device=self.device)  # status word starts at 0
+
+    def dims(self, T: int) -> _lib.Dims:
+        if T > self.T_max:
+            raise ValueError(f"T={T} > T_max={self.T_max}")
+        return _lib.dims(T, self.H, self.I, self.E, self.k)
+
+    def forward(self, x: torch.Tensor, logits: torch.Tensor, out: torch.Tensor | None = None,
+                topk_ids: torch.Tensor | None = None, topk_w: torch.Tensor | None = None, stream=None):
+        T = x.shape[0]
+        if out is None:
+            out = torch.empty(T, self.H, dtype=torch.bfloat16, device=self.device)
+        _lib.moe_layer_forward(x, logits, self.w_gate_up.abi, self.w_down.abi, self.dims(T), out, topk_ids, topk_w,
+                               self.ws, self.ws_bytes, stream)
+        return out
+
+    def forward_host(self, x_host: torch.Tensor, logits_host: torch.Tensor, out_host: torch.Tensor, stream=None):
+        """Host buffers in, host buffer out (copies inside the call; synchronises)."""
+        T = x_host.shape[0]
+        _lib.moe_layer_forward_host(x_host, logits_host, self.w_gate_up.abi, self.w_down.abi, self.dims(T), out_host,
+                                    self.ws, self.ws_bytes, stream)
+        return out_host
+
+    def device_status(self, stream=None) -> int:
+        return _lib.moe_get_device_status(self.ws, stream)

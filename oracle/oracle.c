@@ -266,6 +266,22 @@ void oracle_down_row(const uint16_t *h, int H, int I,
     free(wr);
 }
 
+/* Weighted combine back to token order for rows given in sorted order:
+ * out[t][n] = sum_j w[t][j] * y[inv_perm[t*k+j]][n]  (fp64, ascending j). */
+void oracle_combine(const double *y, const int32_t *inv_perm, const double *w, int T, int H, int k,
+                    double *out)
+{
+    for (int t = 0; t < T; ++t) {
+        double *o = out + (size_t)t * (size_t)H;
+        for (int n = 0; n < H; ++n) o[n] = 0.0;
+        for (int j = 0; j < k; ++j) {
+            const double *yr = y + (size_t)inv_perm[(size_t)t * k + j] * (size_t)H;
+            double wj = w[(size_t)t * k + j];
+            for (int n = 0; n < H; ++n) o[n] += wj * yr[n];
+        }
+    }
+}
+
 /* ------------------------------------------------------------------ layer */
 
 /* Layer output for the tokens listed in rows[0..nrows): out [nrows][H] fp64.

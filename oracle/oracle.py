@@ -63,6 +63,8 @@ def _load():
             lib.oracle_gate_up_swiglu_row.argtypes = [P, i, i, P, P, P, i, P, P]
             lib.oracle_down_row.restype = None
             lib.oracle_down_row.argtypes = [P, i, i, P, P, P, i, P]
+            lib.oracle_combine.restype = None
+            lib.oracle_combine.argtypes = [P, P, P, i, i, i, P]
             lib.oracle_layer_rows.restype = None
             lib.oracle_layer_rows.argtypes = [P, P, P, P, P, P, P, P, P, i, i, i, P, i, P]
             lib.oracle_layer.restype = None
@@ -159,6 +161,18 @@ def down_rows(h_rows_bf16, experts, dn, H: int):
     for p in range(P_):
         lib.oracle_down_row(_ptr(h[p]), H, I, _ptr(codes), _ptr(scales), _ptr(gs), int(experts[p]), _ptr(y[p]))
     return y
+
+
+def combine(y, inv_perm, w):
+    """y f64 [T*k,H] (sorted rows), inv_perm [T*k], w [T,k] -> out f64 [T,H]."""
+    y = _c(y, np.float64)
+    inv_perm = _c(inv_perm, np.int32)
+    w = _c(w, np.float64)
+    T, k = w.shape
+    H = y.shape[1]
+    out = np.empty((T, H), np.float64)
+    _load().oracle_combine(_ptr(y), _ptr(inv_perm), _ptr(w), T, H, k, _ptr(out))
+    return out
 
 
 # --------------------------------------------------------------------- layer

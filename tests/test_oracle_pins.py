@@ -274,3 +274,4 @@ def test_stage_functions_compose_to_layer():
         for j in range(2):
             ref[t] += w[t, j] * y[inv_perm[t * 2 + j]]
     assert np.array_equal(ref, out)
+    assert np.array_equal(orc.combine(y, inv_perm, w), out)
