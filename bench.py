@@ -347,7 +347,9 @@ def run_ours(args, wl, dist, rank, world, local_rank):
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": wl.T * wl.H * 2 + wl.T * wl.E * 4,
                 "d2h_bytes_per_step": wl.T * wl.H * 2},
         "cpu_baseline": cpu,
-        "gpu_launches": 7 * args.steps,
+        # route + permute (one block when T*k <= 1024, else histogram / scan / scatter) + row
+        # gather + gate_up + down + combine
+        "gpu_launches": (1 + (1 if n <= 1024 else 3) + 1 + 1 + 1 + 1) * args.steps,
         "clocks": clk,
     }
     print(json.dumps(line), flush=True)

@@ -40,11 +40,26 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
 }
-__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+// try_wait with a suspend-time hint: a waiting thread sleeps in hardware until
+// the phase completes or about `hint_ns` pass, instead of spinning.
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity, uint32_t hint_ns = 1000000u) {
   uint32_t ok;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+
+// Non-blocking test of a phase: returns at once.
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
       : "r"(bar), "r"(parity)
@@ -52,14 +67,23 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// One lane of the (fully active) warp returns true.
+__device__ __forceinline__ bool elect_one_sync() {
+  uint32_t pred = 0;
+  asm volatile(
+      "{\n\t.reg .b32 r;\n\t.reg .pred p;\n\t"
+      "elect.sync r|p, 0xffffffff;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(pred));
+  return pred != 0;
+}
+
 // Bounded wait for the phase with the given parity to complete.  Returns false
 // if the CTA-wide abort flag is raised or the wait exceeds `limit_ns`; in the
 // latter case it raises the abort flag and records a timeout in `status`.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
                                           int* status, unsigned long long limit_ns = kWaitTimeoutNs) {
-#pragma unroll 1
-  for (int i = 0; i < 128; ++i)
-    if (mbar_try_wait(bar, parity)) return true;
+  if (mbar_test_wait(bar, parity)) return true;
   const unsigned long long t0 = globaltimer_ns();
 #pragma unroll 1
   while (true) {
@@ -135,6 +159,18 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&v)[16
       "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
       : "memory");
 }
+// 32 lanes x 32 columns store.
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&v)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+      "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]),
+      "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]), "r"(v[16]),
+      "r"(v[17]), "r"(v[18]), "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]), "r"(v[24]),
+      "r"(v[25]), "r"(v[26]), "r"(v[27]), "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])
+      : "memory");
+}
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&v)[16]) {
   asm volatile(
       "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
@@ -179,10 +215,13 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
 // 4 significant bits and S' <= 1.75 * 2^127) gives value * scale * 2^-7, exact
 // (<= 6 significant bits, >= 2^-17, normal).  The epilogue multiplies by
 // global_scale * 2^7.
+// Pair j in {0, 1} of a word whose low nibbles (bits 3..0 / 19..16) and next
+// nibbles (7..4 / 23..20) hold pairs 0 and 1: sign to bits 15 / 31, magnitude
+// to bits 8..6 / 24..22.  Only left shifts: pairs 2 and 3 are reached through
+// the word shifted right by 8 once.
 __device__ __forceinline__ uint32_t e2m1_pair_bits(uint32_t q, int j) {
-  // sign bits to 15 / 31, magnitude bits to 8..6 / 24..22
   const uint32_t sgn = q << (12 - 4 * j);
-  const uint32_t mag = (j <= 1) ? (q << (6 - 4 * j)) : (q >> (4 * j - 6));
+  const uint32_t mag = q << (6 - 4 * j);
   return (sgn & 0x80008000u) | (mag & 0x01C001C0u);
 }
 
@@ -205,8 +244,11 @@ __device__ __forceinline__ void e4m3x2_to_scaleprime(uint16_t two, uint32_t& s_l
 
 // Dequantise one packed word (8 elements, one block scale S') into 4 bf16x2 columns.
 __device__ __forceinline__ void dequant_word(uint32_t q, uint32_t sprime, uint32_t* out4) {
-#pragma unroll
-  for (int j = 0; j < 4; ++j) out4[j] = bf16x2_mul(e2m1_pair_bits(q, j), sprime);
+  const uint32_t q8 = q >> 8;
+  out4[0] = bf16x2_mul(e2m1_pair_bits(q, 0), sprime);
+  out4[1] = bf16x2_mul(e2m1_pair_bits(q, 1), sprime);
+  out4[2] = bf16x2_mul(e2m1_pair_bits(q8, 0), sprime);
+  out4[3] = bf16x2_mul(e2m1_pair_bits(q8, 1), sprime);
 }
 
 }  // namespace moe

@@ -31,7 +31,7 @@ __global__ void __launch_bounds__(128) simt_gemm_kernel(const uint16_t* __restri
       const uint8_t* blk = packed + ((size_t)(e * MT + mt) * KB + kb) * kWBlockBytes;
       for (int half = 0; half < 2; ++half) {
         const uint4 cw = *reinterpret_cast<const uint4*>(blk + (half * 128 + r) * 16);
-        const uint16_t sc = *reinterpret_cast<const uint16_t*>(blk + 4096 + (half * 128 + r) * 2);
+        const uint16_t sc = *reinterpret_cast<const uint16_t*>(blk + 4096 + r * 4 + half * 2);
         uint32_t s0, s1, v[16];
         e4m3x2_to_scaleprime(sc, s0, s1);
         dequant_word(cw.x, s0, v + 0);

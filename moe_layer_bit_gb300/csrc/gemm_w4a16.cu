@@ -15,15 +15,20 @@
 //    legal tcgen05 shape and every weight byte is read once per token tile;
 //  * a persistent CTA per SM walks a device-side tile list built from the
 //    expert offsets (no host sync, no empty CTAs);
-//  * warp roles: one producer thread issues a 1-D bulk copy of the packed
-//    weight block (codes + E4M3 scales, 4608 B) and a 2-D TMA copy of the
-//    128-byte-swizzled activation tile per stage; eight dequant warps turn the
-//    codes into exact bf16 (value * 2^-7) and store them straight into tensor
-//    memory as the MMA's A operand (tcgen05.st), so no dequantised weight ever
-//    touches shared memory; one thread issues tcgen05.mma (A from TMEM, B from
-//    shared memory, fp32 accumulator in TMEM, double-buffered); four epilogue
-//    warps read the accumulator (tcgen05.ld), apply global_scale * 2^7, and
-//    write SwiGLU(bf16) or fp32 rows.
+//  * a pipeline stage is SB consecutive 64-column K blocks (a "superstage"),
+//    so the per-stage barrier round trips of the single MMA-issuing warp are
+//    paid once per SB*4 MMAs;
+//  * warp roles: a producer warp issues one 1-D bulk copy of the SB packed
+//    weight blocks (codes + E4M3 scales, SB * 4608 B) and SB 2-D TMA copies of
+//    the 128-byte-swizzled activation tiles per stage; sixteen dequant warps in
+//    four groups (stages round-robin over groups) turn the codes into exact
+//    bf16 (value * 2^-7) and store them straight into tensor memory as the
+//    MMA's A operand (tcgen05.st), so no dequantised weight touches shared
+//    memory; one MMA warp (operands warp-uniform, one elected lane issuing)
+//    runs tcgen05.mma with A from TMEM, B from shared memory and an fp32
+//    accumulator in TMEM, double-buffered across tiles; four epilogue warps
+//    read the accumulator (tcgen05.ld), apply global_scale * 2^7 and write
+//    SwiGLU(bf16) or fp32 rows;
 //  * every barrier wait is bounded (about 1 s); on expiry the CTA records a
 //    timeout in the status word, drains its copies and MMAs and exits.
 #include <cstdint>
@@ -36,33 +41,45 @@
 
 namespace moe {
 
-constexpr int kStages = 8;
 constexpr int kWarpEpi0 = 0;       // warps 0..3: epilogue (TMEM lane quadrant = warp)
-constexpr int kWarpDq0 = 4;        // warps 4..11: dequant (quadrant = warp % 4, K half = (warp-4)/4)
-constexpr int kWarpProducer = 12;  // warp 12: copies
-constexpr int kWarpMma = 13;       // warp 13: TMEM owner + MMA issue
-constexpr int kThreads = 14 * 32;
+constexpr int kWarpDq0 = 4;        // warps 4..19: dequant, 4 groups x 4 quadrants
+constexpr int kDqGroups = 4;       // group g dequantises stages g, g+4, g+8, ...
+constexpr int kWarpProducer = 20;  // warp 20: copies
+constexpr int kWarpMma = 21;       // warp 21: TMEM owner + MMA issue
+constexpr int kThreads = 22 * 32;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kTmemA0 = 256;  // A ring: columns [256, 256 + 32 * kStages)
 constexpr int kMinSmem = 120 * 1024;  // keeps one CTA (one TMEM allocation) per SM
+constexpr int kSmemBudget = 200 * 1024;
 
-template <int BN>
-struct Smem {
-  static constexpr int kBTile = BN * 128;  // BN rows x 64 bf16, 128-byte swizzled
+// Token-tile width BN and SB K blocks per stage: a shared-memory ring of NS
+// stages (SB packed weight blocks + SB activation sub-tiles) and a TMEM ring of
+// NA A-operand slots of 32*SB columns (128 rows x 64*SB bf16) placed after the
+// two BN-column accumulators.
+template <int BN, int SB>
+struct Cfg {
+  static constexpr int kBSub = BN * 128;  // BN rows x 64 bf16, 128-byte swizzled
+  static constexpr int kBTile = SB * kBSub;
+  static constexpr int kWBytes = SB * kWBlockBytes;
+  static constexpr int kStageBytes = kWBytes + kBTile;
+  static constexpr int NS0 = kSmemBudget / kStageBytes;
+  static constexpr int NS = NS0 > 16 ? 16 : (NS0 < 2 ? 2 : NS0);
+  static constexpr int A0 = (2 * BN < 32) ? 32 : 2 * BN;
+  static constexpr int kSlotCols = 32 * SB;
+  static constexpr int NA = (int)(kTmemCols - A0) / kSlotCols;
   static constexpr int kOffB = 0;
-  static constexpr int kOffW = kStages * kBTile;
-  static constexpr int kOffBar = kOffW + kStages * kWBlockBytes;
-  // full[S], empty[S], afull[S], dfull[2], dempty[2], drain
-  static constexpr int kNumBars = 3 * kStages + 5;
+  static constexpr int kOffW = NS * kBTile;
+  static constexpr int kOffBar = kOffW + NS * kWBytes;
+  // full[NS], empty[NS], afull[NA], aempty[NA], dfull[2], dempty[2], drain
+  static constexpr int kNumBars = 2 * NS + 2 * NA + 5;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;  // [0] tmem base, [1] abort, [2] total tiles
   static constexpr int kOffTables = kOffMisc + 16;         // offsets[E+1], prefix[E+1]
+  static_assert(NA >= 1, "TMEM ring needs a slot");
+  static_assert(kOffW % 1024 == 0, "swizzled tiles need 1024-byte alignment");
   static int bytes(int E) {
     int b = kOffTables + 2 * (E + 1) * 4 + 1024;  // + alignment slack
     return b < kMinSmem ? kMinSmem : b;
   }
 };
-
-__device__ __forceinline__ float bf16lo(uint32_t v) { return __uint_as_float(v << 16); }
 
 struct TileCoord {
   int e, mt, nt;
@@ -86,40 +103,65 @@ __device__ __forceinline__ TileCoord decode_tile(int t, const int32_t* prefix, c
   return c;
 }
 
-template <int BN, int MODE>
+// Dequantise one 64-column block of row r (codes at blk + r*16 and blk + 2048 +
+// r*16, scales at blk + 4096 + r*4) into 32 bf16x2 columns.
+__device__ __forceinline__ void dequant_block(const uint8_t* blk, int r, uint32_t (&v)[32]) {
+  const uint4 c0 = *reinterpret_cast<const uint4*>(blk + r * 16);
+  const uint4 c1 = *reinterpret_cast<const uint4*>(blk + 2048 + r * 16);
+  const uint32_t sc = *reinterpret_cast<const uint32_t*>(blk + 4096 + r * 4);
+  uint32_t s0, s1, s2, s3;
+  e4m3x2_to_scaleprime((uint16_t)(sc & 0xFFFFu), s0, s1);
+  e4m3x2_to_scaleprime((uint16_t)(sc >> 16), s2, s3);
+  dequant_word(c0.x, s0, v + 0);
+  dequant_word(c0.y, s0, v + 4);
+  dequant_word(c0.z, s1, v + 8);
+  dequant_word(c0.w, s1, v + 12);
+  dequant_word(c1.x, s2, v + 16);
+  dequant_word(c1.y, s2, v + 20);
+  dequant_word(c1.z, s3, v + 24);
+  dequant_word(c1.w, s3, v + 28);
+}
+
+template <int BN, int SB, int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
     w4a16_gemm_kernel(const __grid_constant__ CUtensorMap tmap_act, const uint8_t* __restrict__ packed,
                       const float* __restrict__ gscale, const int32_t* __restrict__ offsets, void* __restrict__ out,
                       int* __restrict__ status, int E, int N, int K, int out_ld) {
-  using L = Smem<BN>;
+  using C = Cfg<BN, SB>;
+  constexpr int NS = C::NS, NA = C::NA;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
-  const uint32_t sB = sbase + L::kOffB;
-  const uint32_t sW = sbase + L::kOffW;
-  const uint32_t bar0 = sbase + L::kOffBar;
+  const uint32_t sB = sbase + C::kOffB;
+  const uint32_t sW = sbase + C::kOffW;
+  const uint32_t bar0 = sbase + C::kOffBar;
   auto full_bar = [&](int s) { return bar0 + 8u * s; };
-  auto empty_bar = [&](int s) { return bar0 + 8u * (kStages + s); };
-  auto afull_bar = [&](int s) { return bar0 + 8u * (2 * kStages + s); };
-  auto dfull_bar = [&](int d) { return bar0 + 8u * (3 * kStages + d); };
-  auto dempty_bar = [&](int d) { return bar0 + 8u * (3 * kStages + 2 + d); };
-  const uint32_t drain_bar = bar0 + 8u * (3 * kStages + 4);
-  volatile uint32_t* misc = reinterpret_cast<volatile uint32_t*>(smem + L::kOffMisc);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kOffMisc + 4);
-  int32_t* s_off = reinterpret_cast<int32_t*>(smem + L::kOffTables);
+  auto empty_bar = [&](int s) { return bar0 + 8u * (NS + s); };
+  auto afull_bar = [&](int a) { return bar0 + 8u * (2 * NS + a); };
+  auto aempty_bar = [&](int a) { return bar0 + 8u * (2 * NS + NA + a); };
+  auto dfull_bar = [&](int d) { return bar0 + 8u * (2 * NS + 2 * NA + d); };
+  auto dempty_bar = [&](int d) { return bar0 + 8u * (2 * NS + 2 * NA + 2 + d); };
+  const uint32_t drain_bar = bar0 + 8u * (2 * NS + 2 * NA + 4);
+  volatile uint32_t* misc = reinterpret_cast<volatile uint32_t*>(smem + C::kOffMisc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 4);
+  int32_t* s_off = reinterpret_cast<int32_t*>(smem + C::kOffTables);
   int32_t* s_prefix = s_off + (E + 1);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int MT = N / kTileM;
   const int KB = K / kBlockK;
+  const int KS = KB / SB;  // stages per tile
 
   // ---- set-up: barriers, TMEM, tile table
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < NS; ++s) {
       mbar_init(full_bar(s), 1);
-      mbar_init(empty_bar(s), 1);
-      mbar_init(afull_bar(s), 8);
+      mbar_init(empty_bar(s), 4 + 1);  // the stage's 4 dequant warps + the MMA commit
+    }
+    for (int a = 0; a < NA; ++a) {
+      mbar_init(afull_bar(a), 4);
+      mbar_init(aempty_bar(a), 1);
     }
     for (int d = 0; d < 2; ++d) {
       mbar_init(dfull_bar(d), 1);
@@ -131,7 +173,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   if (warp == kWarpProducer && lane == 0) prefetch_tmap(&tmap_act);
   if (warp == kWarpMma) {
-    tmem_alloc(sbase + L::kOffMisc, kTmemCols);
+    tmem_alloc(sbase + C::kOffMisc, kTmemCols);
     tmem_relinquish();
   }
   for (int i = threadIdx.x; i <= E; i += blockDim.x) s_off[i] = __ldg(offsets + i);
@@ -163,112 +205,117 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem_base = misc[0];
   const int total = (int)misc[2];
+  const int my_tiles = total > (int)blockIdx.x ? (total - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x : 0;
+  const int my_stages = my_tiles * KS;
 
   if (warp == kWarpProducer) {
     // ------------------------------------------------------------ producer
-    if (lane == 0) {
-      int stage = 0;
-      uint32_t phase = 0;
-      uint32_t issued = 0, last_par = 0;  // per-stage: issued at least once / parity of the last issue
-      bool ok = true;
-      for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-        const TileCoord c = decode_tile(t, s_prefix, s_off, E, BN);
-        const uint8_t* wsrc = packed + (size_t)(c.e * MT + c.mt) * KB * kWBlockBytes;
-        const int row0 = s_off[c.e] + c.nt * BN;
-        for (int kb = 0; kb < KB; ++kb) {
-          if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, status)) {
-            ok = false;
-            break;
-          }
-          mbar_arrive_expect_tx(full_bar(stage), (uint32_t)(kWBlockBytes + L::kBTile));
-          bulk_copy_g2s(sW + stage * kWBlockBytes, wsrc + (size_t)kb * kWBlockBytes, kWBlockBytes, full_bar(stage));
-          tma_load_2d(sB + stage * L::kBTile, &tmap_act, kb * kBlockK, row0, full_bar(stage));
-          issued |= 1u << stage;
-          last_par = (last_par & ~(1u << stage)) | (phase << stage);
-          if (++stage == kStages) {
-            stage = 0;
-            phase ^= 1u;
-          }
-        }
-      }
-      // drain: every copy this thread issued has landed before the CTA exits
-      for (int s = 0; s < kStages; ++s)
-        if ((issued >> s) & 1u) mbar_wait(full_bar(s), (last_par >> s) & 1u, nullptr, status, kDrainTimeoutNs);
-    }
-  } else if (warp == kWarpMma) {
-    // ---------------------------------------------------------- MMA issue
-    if (lane == 0) {
-      constexpr uint32_t idesc = idesc_bf16_f32(kTileM, BN);
-      int stage = 0;
-      uint32_t phase = 0;
-      bool ok = true;
-      int it = 0;
-      for (int t = blockIdx.x; t < total && ok; t += gridDim.x, ++it) {
-        const int d = it & 1;
-        const uint32_t dph = (uint32_t)(it >> 1) & 1u;
-        if (!mbar_wait(dempty_bar(d), dph ^ 1u, abort_flag, status)) break;
-        tc_fence_after();
-        const uint32_t d_tmem = tmem_base + (uint32_t)(d * BN);
-        for (int kb = 0; kb < KB; ++kb) {
-          if (!mbar_wait(afull_bar(stage), phase, abort_flag, status) ||
-              !mbar_wait(full_bar(stage), phase, abort_flag, status)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t a_tmem = tmem_base + kTmemA0 + (uint32_t)stage * 32u;
-          const uint32_t b_addr = sB + stage * L::kBTile;
-#pragma unroll
-          for (int kk = 0; kk < kBlockK / 16; ++kk)
-            tc_mma_ts(d_tmem, a_tmem + kk * 8u, smem_desc_sw128(b_addr + kk * 32u), idesc, (kb | kk) != 0);
-          tc_commit(empty_bar(stage));
-          if (++stage == kStages) {
-            stage = 0;
-            phase ^= 1u;
-          }
-        }
-        if (ok) tc_commit(dfull_bar(d));
-      }
-      // drain: all MMAs issued by this thread complete before TMEM is freed
-      tc_commit(drain_bar);
-      mbar_wait(drain_bar, 0, nullptr, status, kDrainTimeoutNs);
-    }
-  } else if (warp >= kWarpDq0) {
-    // ------------------------------------------------------------- dequant
-    const int q = warp & 3;
-    const int half = (warp - kWarpDq0) >> 2;
-    const int r = 32 * q + lane;
-    const uint32_t t_row = tmem_base + ((uint32_t)(32 * q) << 16) + kTmemA0 + (uint32_t)(half * 16);
-    int stage = 0;
-    uint32_t phase = 0;
+    // The whole warp walks the schedule (uniform values); one elected lane issues.
+    int i = 0;
     bool ok = true;
     for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-      for (int kb = 0; kb < KB; ++kb) {
-        // every lane waits (each acquires the copied bytes); the warp acts as one
-        if (!__all_sync(0xFFFFFFFFu, mbar_wait(full_bar(stage), phase, abort_flag, status))) {
+      const TileCoord c = decode_tile(t, s_prefix, s_off, E, BN);
+      const uint8_t* wsrc = packed + (size_t)(c.e * MT + c.mt) * KB * kWBlockBytes;
+      const int row0 = s_off[c.e] + c.nt * BN;
+      for (int ks = 0; ks < KS; ++ks, ++i) {
+        const int s = i % NS;
+        const uint32_t ph = (uint32_t)(i / NS) & 1u;
+        if (!__all_sync(0xFFFFFFFFu, mbar_wait(empty_bar(s), ph ^ 1u, abort_flag, status))) {
           ok = false;
           break;
         }
-        const uint8_t* blk = smem + L::kOffW + stage * kWBlockBytes;
-        const uint4 cw = *reinterpret_cast<const uint4*>(blk + (half * 128 + r) * 16);
-        const uint16_t sc = *reinterpret_cast<const uint16_t*>(blk + 4096 + (half * 128 + r) * 2);
-        uint32_t s0, s1;
-        e4m3x2_to_scaleprime(sc, s0, s1);
-        uint32_t v[16];
-        dequant_word(cw.x, s0, v + 0);
-        dequant_word(cw.y, s0, v + 4);
-        dequant_word(cw.z, s1, v + 8);
-        dequant_word(cw.w, s1, v + 12);
-        tmem_st16(t_row + (uint32_t)stage * 32u, v);
-        tc_wait_st();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(afull_bar(stage));
-        if (++stage == kStages) {
-          stage = 0;
-          phase ^= 1u;
+        if (elect_one_sync()) {
+          mbar_arrive_expect_tx(full_bar(s), (uint32_t)C::kStageBytes);
+          bulk_copy_g2s(sW + s * C::kWBytes, wsrc + (size_t)ks * C::kWBytes, C::kWBytes, full_bar(s));
+#pragma unroll
+          for (int b = 0; b < SB; ++b)
+            tma_load_2d(sB + s * C::kBTile + b * C::kBSub, &tmap_act, (ks * SB + b) * kBlockK, row0, full_bar(s));
         }
+        __syncwarp();
       }
+    }
+    // drain: every copy this warp issued has landed before the CTA exits
+    for (int j = (i > NS ? i - NS : 0); j < i; ++j)
+      mbar_wait(full_bar(j % NS), (uint32_t)(j / NS) & 1u, nullptr, status, kDrainTimeoutNs);
+  } else if (warp == kWarpMma) {
+    // ---------------------------------------------------------- MMA issue
+    // The whole warp waits and computes the (uniform) operands; one elected
+    // lane issues the MMAs and commits.
+    constexpr uint32_t idesc = idesc_bf16_f32(kTileM, BN);
+    int i = 0, it = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; t < total && ok; t += gridDim.x, ++it) {
+      const int d = it & 1;
+      if (!__all_sync(0xFFFFFFFFu, mbar_wait(dempty_bar(d), ((uint32_t)(it >> 1) & 1u) ^ 1u, abort_flag, status)))
+        break;
+      tc_fence_after();
+      const uint32_t d_tmem = tmem_base + (uint32_t)(d * BN);
+      for (int ks = 0; ks < KS; ++ks, ++i) {
+        const int s = i % NS, a = i % NA;
+        const bool got = mbar_wait(afull_bar(a), (uint32_t)(i / NA) & 1u, abort_flag, status) &&
+                         mbar_wait(full_bar(s), (uint32_t)(i / NS) & 1u, abort_flag, status);
+        if (!__all_sync(0xFFFFFFFFu, got)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t a_tmem = tmem_base + (uint32_t)(C::A0 + C::kSlotCols * a);
+        const uint64_t b_desc = smem_desc_sw128(sB + s * C::kBTile);
+        if (elect_one_sync()) {
+#pragma unroll
+          for (int b = 0; b < SB; ++b)
+#pragma unroll
+            for (int kk = 0; kk < kBlockK / 16; ++kk)
+              tc_mma_ts(d_tmem, a_tmem + (uint32_t)(32 * b + 8 * kk),
+                        b_desc + (uint64_t)((b * C::kBSub + kk * 32) >> 4), idesc, (ks | b | kk) != 0);
+          tc_commit(aempty_bar(a));
+          tc_commit(empty_bar(s));
+        }
+        __syncwarp();
+      }
+      if (ok) {
+        if (elect_one_sync()) tc_commit(dfull_bar(d));
+        __syncwarp();
+      }
+    }
+    // drain: all MMAs issued by this warp complete before TMEM is freed
+    if (elect_one_sync()) tc_commit(drain_bar);
+    __syncwarp();
+    mbar_wait(drain_bar, 0, nullptr, status, kDrainTimeoutNs);
+  } else if (warp >= kWarpDq0) {
+    // ------------------------------------------------------------- dequant
+    // At most NA groups: a group's wait for slot i % NA (MMA of stage i - NA
+    // done) must never run two phases ahead of that barrier, or its parity
+    // test would alias.  Its own previous stage i - G waited for MMA of stage
+    // i - G - NA, which covers stage i - 2 NA only when G <= NA.
+    constexpr int G = NA < kDqGroups ? NA : kDqGroups;
+    const int q = warp & 3;
+    const int group = (warp - kWarpDq0) >> 2;
+    const int r = 32 * q + lane;
+    const uint32_t t_row = tmem_base + ((uint32_t)(32 * q) << 16) + (uint32_t)C::A0;
+#pragma unroll 1
+    for (int i = group; group < G && i < my_stages; i += G) {
+      const int s = i % NS, a = i % NA;
+      // every lane waits (each acquires the copied bytes); the warp acts as one
+      if (!__all_sync(0xFFFFFFFFu, mbar_wait(full_bar(s), (uint32_t)(i / NS) & 1u, abort_flag, status))) break;
+      if (!__all_sync(0xFFFFFFFFu, mbar_wait(aempty_bar(a), ((uint32_t)(i / NA) & 1u) ^ 1u, abort_flag, status)))
+        break;
+      tc_fence_after();
+      const uint8_t* stage_w = smem + C::kOffW + s * C::kWBytes;
+#pragma unroll 1
+      for (int b = 0; b < SB; ++b) {
+        uint32_t v[32];
+        dequant_block(stage_w + b * kWBlockBytes, r, v);
+        if (b == SB - 1) {
+          __syncwarp();
+          if (lane == 0) mbar_arrive(empty_bar(s));  // codes are in registers: the stage may be refilled
+        }
+        tmem_st32(t_row + (uint32_t)(C::kSlotCols * a + 32 * b), v);
+      }
+      tc_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(afull_bar(a));
     }
   } else {
     // ------------------------------------------------------------ epilogue
@@ -289,6 +336,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t v[16];
         tmem_ld16(t_acc + (uint32_t)(cc * 16), v);
         tc_wait_ld();
+        if (cc * 16 >= nvalid) continue;
         if (MODE == 0) {
           // rows 32q..32q+15 hold gate features f, rows 32q+16.. the matching up rows
           const int f = c.mt * 64 + 16 * q + (lane & 15);
@@ -325,7 +373,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
 
-  // ---- teardown: everyone is here; the MMA thread drained its work
+  // ---- teardown: everyone is here; the MMA warp drained its work
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -350,8 +398,8 @@ static PFN_encodeTiled get_encode_fn() {
   return fn;
 }
 
-template <int BN, int MODE>
-static cudaError_t launch_gemm_bn(const GemmArgs& a, cudaStream_t s) {
+template <int BN, int SB, int MODE>
+static cudaError_t launch_gemm_cfg(const GemmArgs& a, cudaStream_t s) {
   PFN_encodeTiled enc = get_encode_fn();
   if (enc == nullptr) return cudaErrorNotSupported;
   CUtensorMap tmap;
@@ -374,8 +422,8 @@ static cudaError_t launch_gemm_bn(const GemmArgs& a, cudaStream_t s) {
   const long long max_tiles = (long long)MT * (n / BN + (n < a.E ? n : a.E));
   int grid = (int)(max_tiles < sms ? max_tiles : sms);
   if (grid <= 0) return cudaSuccess;
-  const int smem = Smem<BN>::bytes(a.E);
-  auto kern = w4a16_gemm_kernel<BN, MODE>;
+  const int smem = Cfg<BN, SB>::bytes(a.E);
+  auto kern = w4a16_gemm_kernel<BN, SB, MODE>;
   err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (err != cudaSuccess) return err;
   kern<<<grid, kThreads, smem, s>>>(tmap, a.packed, a.gscale, a.offsets, a.out, a.status, a.E, a.N, a.K, a.out_ld);
@@ -391,6 +439,17 @@ static int pick_bn(int rows, int E) {
   if (mean2 <= 32) return 32;
   if (mean2 <= 64) return 64;
   return 128;
+}
+
+// K blocks per stage: 4 for narrow token tiles (decode: amortise the MMA warp's
+// per-stage cost), 2 for wide ones (keeps two TMEM A slots next to 2 x BN
+// accumulator columns), 1 when K/64 is not a multiple.
+template <int BN, int MODE>
+static cudaError_t launch_gemm_bn(const GemmArgs& a, cudaStream_t s) {
+  constexpr int kWide = (BN <= 32) ? 4 : 2;
+  const int KB = a.K / kBlockK;
+  if (KB % kWide == 0) return launch_gemm_cfg<BN, kWide, MODE>(a, s);
+  return launch_gemm_cfg<BN, 1, MODE>(a, s);
 }
 
 cudaError_t launch_gemm(int mode, const GemmArgs& a, cudaStream_t s) {
@@ -413,11 +472,14 @@ cudaError_t launch_gemm(int mode, const GemmArgs& a, cudaStream_t s) {
 }
 
 // ------------------------------------------------------------------ prepack
-// One thread per (expert, 128-row tile, 64-column block, K half, tile row):
-// copies 16 code bytes (32 elements) into the packed word order and the two
-// E4M3 scales of those 32 elements.  Packed word w of a K half holds elements
-// 8w..8w+7: even elements in nibbles 0..3 of the low 16 bits, odd elements in
-// nibbles 0..3 of the high 16 bits.
+// Packed block of a 128-row x 64-column tile (4608 bytes):
+//   codes  [half 0..1][row 0..127][16 B] at (half * 128 + row) * 16: K
+//          elements 32*half .. 32*half+31 of the row as 4 words of 8;
+//   scales [row][4] at 4096 + row * 4: the row's four E4M3 block scales.
+// Packed word w holds elements 8w..8w+7: even elements in nibbles 0..3 of the
+// low 16 bits, odd elements in nibbles 0..3 of the high 16 bits.
+// One thread per (expert, tile, K block, half, row) moves 16 code bytes and
+// the two scales of those 32 elements.
 __global__ void prepack_kernel(const uint8_t* __restrict__ codes, const uint8_t* __restrict__ scales, int E, int N,
                                int K, int proj, uint8_t* __restrict__ packed) {
   const int MT = N / kTileM, KB = K / kBlockK;
@@ -455,8 +517,8 @@ __global__ void prepack_kernel(const uint8_t* __restrict__ codes, const uint8_t*
   uint8_t* dst = packed + blk * kWBlockBytes;
   *reinterpret_cast<uint4*>(dst + (half * 128 + r) * 16) = make_uint4(words[0], words[1], words[2], words[3]);
   const uint8_t* ss = scales + src_row * (K / 16) + kb * 4 + half * 2;
-  dst[4096 + (half * 128 + r) * 2 + 0] = ss[0];
-  dst[4096 + (half * 128 + r) * 2 + 1] = ss[1];
+  dst[4096 + r * 4 + half * 2 + 0] = ss[0];
+  dst[4096 + r * 4 + half * 2 + 1] = ss[1];
 }
 
 cudaError_t launch_prepack(const uint8_t* codes, const uint8_t* scales, int E, int N, int K, int proj,

@@ -6,7 +6,7 @@
 #include <initializer_list>
 #include <cuda_runtime.h>
 
-#include "../../include/moe_w4a16.h"
+#include "moe_w4a16.h"
 #include "kernels.h"
 
 namespace moe {

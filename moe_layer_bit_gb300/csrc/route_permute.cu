@@ -156,27 +156,16 @@ __global__ void __launch_bounds__(1024) perm_scan_kernel(int32_t* __restrict__ c
   }
 }
 
-// One block of kPermChunk threads per chunk; thread i owns pair base + i.
-// After the ranks are known, the block's warps copy the x rows (16-byte
-// vectors) to x_perm.
-__global__ void __launch_bounds__(kPermChunk) perm_scatter_kernel(const int32_t* __restrict__ ids, int n, int E, int k,
-                                                                  int H, const int32_t* __restrict__ chunk_base,
-                                                                  const uint16_t* __restrict__ x,
-                                                                  int32_t* __restrict__ sorted_token,
-                                                                  int32_t* __restrict__ inv_perm,
-                                                                  uint16_t* __restrict__ x_perm) {
-  extern __shared__ int32_t run[];            // [E] running position per expert
-  __shared__ int32_t s_pos[kPermChunk];
-  __shared__ int32_t s_tok[kPermChunk];
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int g = blockIdx.x * kPermChunk + tid;
-  for (int e = tid; e < E; e += blockDim.x) run[e] = chunk_base[(size_t)blockIdx.x * E + e];
-  const bool valid = g < n;
-  const int e = valid ? __ldg(ids + g) : -1 - lane;   // invalid pairs: unique keys
-  const uint32_t peers = __match_any_sync(0xFFFFFFFFu, e);
+// Stable rank of each pair among the block's pairs routed to the same expert:
+// warp w's pairs follow warps 0..w-1 (ascending pair index), and inside a warp
+// match_any + popc orders equal experts by lane.  `run[e]` starts at the first
+// sorted row of expert e available to this block and ends past its last.
+__device__ __forceinline__ int block_stable_position(int e, bool valid, int32_t* run) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int key = valid ? e : -1 - lane;   // invalid pairs: unique keys
+  const uint32_t peers = __match_any_sync(0xFFFFFFFFu, key);
   const int rank = __popc(peers & ((1u << lane) - 1u));
   const int leader = __ffs(peers) - 1;
-  __syncthreads();
   int pos = 0;
   for (int w = 0; w < (int)(blockDim.x >> 5); ++w) {
     if (warp == w && valid) {
@@ -186,21 +175,87 @@ __global__ void __launch_bounds__(kPermChunk) perm_scatter_kernel(const int32_t*
     }
     __syncthreads();
   }
+  return pos;
+}
+
+// One block of kPermChunk threads per chunk; thread i owns pair base + i.
+__global__ void __launch_bounds__(kPermChunk) perm_scatter_kernel(const int32_t* __restrict__ ids, int n, int E, int k,
+                                                                  const int32_t* __restrict__ chunk_base,
+                                                                  int32_t* __restrict__ sorted_token,
+                                                                  int32_t* __restrict__ inv_perm) {
+  extern __shared__ int32_t run[];            // [E] running position per expert
+  const int g = blockIdx.x * kPermChunk + threadIdx.x;
+  for (int e = threadIdx.x; e < E; e += blockDim.x) run[e] = chunk_base[(size_t)blockIdx.x * E + e];
+  const bool valid = g < n;
+  const int e = valid ? __ldg(ids + g) : 0;
+  __syncthreads();
+  const int pos = block_stable_position(e, valid, run);
   if (valid) {
     sorted_token[pos] = g / k;
     inv_perm[g] = pos;
   }
-  s_pos[tid] = valid ? pos : -1;
-  s_tok[tid] = g / k;
+}
+
+// All pairs in one block (T*k <= kPermChunk): histogram, scan and stable
+// scatter in a single launch.
+__global__ void __launch_bounds__(kPermChunk) perm_single_kernel(const int32_t* __restrict__ ids, int n, int E, int k,
+                                                                 int32_t* __restrict__ counts,
+                                                                 int32_t* __restrict__ offsets,
+                                                                 int32_t* __restrict__ sorted_token,
+                                                                 int32_t* __restrict__ inv_perm) {
+  extern __shared__ int32_t run[];            // [E]
+  __shared__ int32_t warp_tot[32];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  for (int e = tid; e < E; e += blockDim.x) run[e] = 0;
   __syncthreads();
-  // gather: one warp per row, 16-byte vectors (H % 128 == 0 -> H*2 % 16 == 0)
-  const int vec_per_row = H / 8;
-  for (int r = warp; r < kPermChunk; r += (blockDim.x >> 5)) {
-    const int p = s_pos[r];
-    if (p < 0) continue;
-    const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)s_tok[r] * H);
-    uint4* dst = reinterpret_cast<uint4*>(x_perm + (size_t)p * H);
-    for (int v = lane; v < vec_per_row; v += 32) dst[v] = __ldg(src + v);
+  const bool valid = tid < n;
+  const int e = valid ? __ldg(ids + tid) : 0;
+  if (valid) atomicAdd(&run[e], 1);
+  __syncthreads();
+  // exclusive scan of the counts (E <= 1024 = blockDim)
+  const int32_t c = tid < E ? run[tid] : 0;
+  int32_t x = c;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int32_t y = __shfl_up_sync(0xFFFFFFFFu, x, off);
+    if (lane >= off) x += y;
+  }
+  if (lane == 31) warp_tot[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    int32_t w = warp_tot[lane];
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int32_t y = __shfl_up_sync(0xFFFFFFFFu, w, off);
+      if (lane >= off) w += y;
+    }
+    warp_tot[lane] = w;
+  }
+  __syncthreads();
+  const int32_t excl = x - c + (warp > 0 ? warp_tot[warp - 1] : 0);
+  if (tid < E) {
+    counts[tid] = c;
+    offsets[tid] = excl;
+    run[tid] = excl;
+    if (tid == E - 1) offsets[E] = excl + c;
+  }
+  __syncthreads();
+  const int pos = block_stable_position(e, valid, run);
+  if (valid) {
+    sorted_token[pos] = tid / k;
+    inv_perm[tid] = pos;
+  }
+}
+
+// x_perm[p] = x[sorted_token[p]]: one thread per 16-byte vector (H % 8 == 0).
+__global__ void __launch_bounds__(256) perm_gather_kernel(const uint16_t* __restrict__ x,
+                                                          const int32_t* __restrict__ sorted_token, long long nvec,
+                                                          int vec_per_row, uint16_t* __restrict__ x_perm) {
+  for (long long v = (long long)blockIdx.x * blockDim.x + threadIdx.x; v < nvec; v += (long long)gridDim.x * blockDim.x) {
+    const long long p = v / vec_per_row;
+    const int c = (int)(v - p * vec_per_row);
+    const int t = __ldg(sorted_token + p);
+    reinterpret_cast<uint4*>(x_perm)[v] = __ldg(reinterpret_cast<const uint4*>(x + (size_t)t * vec_per_row * 8) + c);
   }
 }
 
@@ -215,16 +270,28 @@ cudaError_t launch_permute(const int32_t* ids, const uint16_t* x, int T, int H, 
                            int32_t* scratch, cudaStream_t s) {
   const int n = T * k;
   const int nchunks = (n + kPermChunk - 1) / kPermChunk;
-  if (n > 0) {
+  cudaError_t err;
+  if (nchunks <= 1) {
+    perm_single_kernel<<<1, kPermChunk, E * sizeof(int32_t), s>>>(ids, n, E, k, counts, offsets, sorted_token,
+                                                                   inv_perm);
+    err = cudaGetLastError();
+  } else {
     perm_hist_kernel<<<nchunks, 256, E * sizeof(int32_t), s>>>(ids, n, E, scratch);
-    cudaError_t err = cudaGetLastError();
+    err = cudaGetLastError();
     if (err != cudaSuccess) return err;
+    perm_scan_kernel<<<1, 1024, 0, s>>>(scratch, nchunks, E, counts, offsets);
+    err = cudaGetLastError();
+    if (err != cudaSuccess) return err;
+    perm_scatter_kernel<<<nchunks, kPermChunk, E * sizeof(int32_t), s>>>(ids, n, E, k, scratch, sorted_token,
+                                                                         inv_perm);
+    err = cudaGetLastError();
   }
-  perm_scan_kernel<<<1, 1024, 0, s>>>(scratch, nchunks, E, counts, offsets);
-  cudaError_t err = cudaGetLastError();
   if (err != cudaSuccess || n == 0) return err;
-  perm_scatter_kernel<<<nchunks, kPermChunk, E * sizeof(int32_t), s>>>(ids, n, E, k, H, scratch, x, sorted_token,
-                                                                       inv_perm, x_perm);
+  const int vpr = H / 8;
+  const long long nvec = (long long)n * vpr;
+  long long blocks = (nvec + 255) / 256;
+  if (blocks > 4096) blocks = 4096;
+  perm_gather_kernel<<<(unsigned)blocks, 256, 0, s>>>(x, sorted_token, nvec, vpr, x_perm);
   return cudaGetLastError();
 }
 
