@@ -37,8 +37,9 @@
  *  - A kernel whose internal wait (a pipeline barrier) runs past about one
  *    second gives up, records MOE_ERR_DEVICE_TIMEOUT in the workspace's status
  *    word and returns; moe_get_device_status() reads it.
- *  - The library keeps no global mutable state and allocates no memory:
- *    every intermediate lives in the caller's workspace `ws`.
+ *  - The library allocates no memory: every intermediate lives in the
+ *    caller's workspace `ws`.  Apart from the fixed scratch array of
+ *    moe_permute_noalloc, it keeps no global mutable state.
  */
 #ifndef MOE_W4A16_H
 #define MOE_W4A16_H
@@ -135,6 +136,26 @@ int moe_route_topk(const float *logits, moe_dims d, int32_t *topk_ids, float *to
 int moe_permute(const int32_t *topk_ids, const uint16_t *x, moe_dims d, int32_t *counts,
                 int32_t *offsets, int32_t *sorted_token, int32_t *inv_perm, uint16_t *x_perm,
                 void *ws, size_t ws_bytes, void *stream);
+
+/* moe_permute for callers that cannot allocate device memory: code whose
+ * device memory all belongs to a pool or arena it may not grow, serving loops
+ * that must not allocate after start-up, and plug-ins that are handed only
+ * their input and output buffers.  The pages have no counterpart of this
+ * entry point; it exists only for such callers.
+ * Same arguments, results and rules as moe_permute, minus the workspace: the
+ * per-chunk histogram scratch lives in a fixed array inside the library
+ * (65536 int32 = 256 KiB of device memory, held by every GPU that loads the
+ * library until the process exits).  The call allocates nothing.
+ * Limit: ceil(T*k / 1024) * E <= 65536 (e.g. T*k <= 65536 with E <= 1024);
+ * larger sizes return MOE_ERR_UNSUPPORTED_SHAPE before anything runs.
+ * The first call on each device looks up the array's device address
+ * (cudaGetSymbolAddress) with that device current; make that first call
+ * before any stream capture.  Every call uses the same array, so calls whose
+ * work overlaps on the GPU (other streams, other host threads) race; the
+ * array needs no clearing between calls. */
+int moe_permute_noalloc(const int32_t *topk_ids, const uint16_t *x, moe_dims d, int32_t *counts,
+                        int32_t *offsets, int32_t *sorted_token, int32_t *inv_perm, uint16_t *x_perm,
+                        void *stream);
 
 /* Grouped gate_up GEMM + SwiGLU, one launch over all experts ([Atlas] W4A16
  * Grouped GEMM; [Rust DL] SwiGLU).  For expert e and rows p in

@@ -55,6 +55,7 @@ _SIGS = {
     "moe_stage_workspace_bytes": (SZ, [Dims]),
     "moe_route_topk": (INT, [P, Dims, P, P, P]),
     "moe_permute": (INT, [P, P, Dims, P, P, P, P, P, P, SZ, P]),
+    "moe_permute_noalloc": (INT, [P, P, Dims, P, P, P, P, P, P]),
     "moe_w4a16_gate_up_swiglu": (INT, [P, P, W4, Dims, P, P, SZ, P]),
     "moe_w4a16_down": (INT, [P, P, W4, Dims, P, P, SZ, P]),
     "moe_unpermute_combine": (INT, [P, P, P, Dims, P, P]),
@@ -146,6 +147,11 @@ def moe_route_topk(logits, d, topk_ids, topk_w, stream=None):
 def moe_permute(topk_ids, x, d, counts, offsets, sorted_token, inv_perm, x_perm, ws, ws_bytes, stream=None):
     _check(load().moe_permute(_p(topk_ids), _p(x), d, _p(counts), _p(offsets), _p(sorted_token), _p(inv_perm),
                               _p(x_perm), _p(ws), ws_bytes, _s(stream)), "moe_permute")
+
+
+def moe_permute_noalloc(topk_ids, x, d, counts, offsets, sorted_token, inv_perm, x_perm, stream=None):
+    _check(load().moe_permute_noalloc(_p(topk_ids), _p(x), d, _p(counts), _p(offsets), _p(sorted_token),
+                                      _p(inv_perm), _p(x_perm), _s(stream)), "moe_permute_noalloc")
 
 
 def moe_w4a16_gate_up_swiglu(x_perm, offsets, w_gate_up: W4, d, h, ws, ws_bytes, stream=None):
