@@ -204,25 +204,42 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
 }
 
 // ------------------------------------------------------- NVFP4 dequantiser
-// Packed code word (see the prepack kernel): 8 consecutive K elements e0..e7,
-// low 16 bits hold e0,e2,e4,e6 in nibbles 0..3, high 16 bits hold e1,e3,e5,e7.
-// Output column j (j = 0..3) is the bf16 pair (e_{2j}, e_{2j+1}).
+// An E2M1 code s.e1.e0.m whose sign sits at bf16 bit 15 and whose e1.e0.m sit
+// at bits 8..6 is the bf16 pattern of value * 2^-126 (e1.e0 = exponent field,
+// m = top mantissa bit; exponent 0 is the bf16 subnormal m * 2^-127 =
+// 0.5m * 2^-126).  Multiplying by S' = scale * 2^119 (exact in bf16: the E4M3
+// scale has 4 significant bits and S' <= 1.75 * 2^127) gives
+// value * scale * 2^-7, exact (<= 6 significant bits, >= 2^-17, normal).  The
+// epilogue multiplies by global_scale * 2^7.
 //
-// An E2M1 nibble s.e1.e0.m placed with its sign at bf16 bit 15 and e1.e0.m at
-// bits 8..6 is the bf16 pattern of value * 2^-126 (e1.e0 = exponent field,
-// m = top mantissa bit; exponent 0 is the bf16 subnormal m * 2^-127 = 0.5m *
-// 2^-126).  Multiplying by S' = scale * 2^119 (exact in bf16: the E4M3 scale has
-// 4 significant bits and S' <= 1.75 * 2^127) gives value * scale * 2^-7, exact
-// (<= 6 significant bits, >= 2^-17, normal).  The epilogue multiplies by
-// global_scale * 2^7.
-// Pair j in {0, 1} of a word whose low nibbles (bits 3..0 / 19..16) and next
-// nibbles (7..4 / 23..20) hold pairs 0 and 1: sign to bits 15 / 31, magnitude
-// to bits 8..6 / 24..22.  Only left shifts: pairs 2 and 3 are reached through
-// the word shifted right by 8 once.
-__device__ __forceinline__ uint32_t e2m1_pair_bits(uint32_t q, int j) {
-  const uint32_t sgn = q << (12 - 4 * j);
-  const uint32_t mag = q << (6 - 4 * j);
-  return (sgn & 0x80008000u) | (mag & 0x01C001C0u);
+// Packed word of 8 consecutive K elements e0..e7: the low 16 bits hold the even
+// elements, the high 16 bits the odd ones (element 2j+1 at the same bit
+// positions + 16 as element 2j).  Per half, the four codes sit in slots
+//   A (e0/e1): s 15, e1 8,  e0 7,  m 6    -> already in place
+//   B (e2/e3): s 12, e1 5,  e0 4,  m 3    -> shift left 3
+//   C (e4/e5): s 9,  e1 2,  e0 1,  m 0    -> shift left 6
+//   D (e6/e7): s 11, e1 10, e0 14, m 13   -> from the isolated slot:
+//              sign << 4, e1 >> 2, e0.m >> 7
+// so every output column is one mask of a shifted word, and no shifted copy
+// drops a foreign bit onto a kept position (bits 15, 8..6 of each half).
+constexpr uint32_t kBf16PatternMask = 0x81C081C0u;
+
+__device__ __host__ __forceinline__ uint32_t nvfp4_slot_bits(uint32_t code, int slot) {
+  const uint32_t s = (code >> 3) & 1u, e1 = (code >> 2) & 1u, e0 = (code >> 1) & 1u, m = code & 1u;
+  switch (slot) {
+    case 0: return (s << 15) | (e1 << 8) | (e0 << 7) | (m << 6);
+    case 1: return (s << 12) | (e1 << 5) | (e0 << 4) | (m << 3);
+    case 2: return (s << 9) | (e1 << 2) | (e0 << 1) | m;
+    default: return (s << 11) | (e1 << 10) | (e0 << 14) | (m << 13);
+  }
+}
+
+// Packed word from the 8 codes of elements e0..e7.
+__device__ __host__ __forceinline__ uint32_t nvfp4_pack_word(const uint32_t (&codes)[8]) {
+  uint32_t w = 0;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) w |= nvfp4_slot_bits(codes[2 * j], j) | (nvfp4_slot_bits(codes[2 * j + 1], j) << 16);
+  return w;
 }
 
 __device__ __forceinline__ uint32_t bf16x2_mul(uint32_t a, uint32_t b) {
@@ -242,13 +259,14 @@ __device__ __forceinline__ void e4m3x2_to_scaleprime(uint16_t two, uint32_t& s_l
   asm("cvt.rn.bf16x2.f32 %0, %1, %1;" : "=r"(s_hi) : "f"(f_hi));
 }
 
-// Dequantise one packed word (8 elements, one block scale S') into 4 bf16x2 columns.
+// Dequantise one packed word (8 elements, one block scale S') into 4 bf16x2
+// columns: column j = (e_{2j}, e_{2j+1}).
 __device__ __forceinline__ void dequant_word(uint32_t q, uint32_t sprime, uint32_t* out4) {
-  const uint32_t q8 = q >> 8;
-  out4[0] = bf16x2_mul(e2m1_pair_bits(q, 0), sprime);
-  out4[1] = bf16x2_mul(e2m1_pair_bits(q, 1), sprime);
-  out4[2] = bf16x2_mul(e2m1_pair_bits(q8, 0), sprime);
-  out4[3] = bf16x2_mul(e2m1_pair_bits(q8, 1), sprime);
+  const uint32_t d = q & 0x6C006C00u;  // slot D, isolated
+  out4[0] = bf16x2_mul(q & kBf16PatternMask, sprime);
+  out4[1] = bf16x2_mul((q << 3) & kBf16PatternMask, sprime);
+  out4[2] = bf16x2_mul((q << 6) & kBf16PatternMask, sprime);
+  out4[3] = bf16x2_mul(((d << 4) | (d >> 2) | (d >> 7)) & kBf16PatternMask, sprime);
 }
 
 }  // namespace moe

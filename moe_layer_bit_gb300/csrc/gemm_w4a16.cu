@@ -20,8 +20,8 @@
 //    paid once per SB*4 MMAs;
 //  * warp roles: a producer warp issues one 1-D bulk copy of the SB packed
 //    weight blocks (codes + E4M3 scales, SB * 4608 B) and SB 2-D TMA copies of
-//    the 128-byte-swizzled activation tiles per stage; sixteen dequant warps in
-//    four groups (stages round-robin over groups) turn the codes into exact
+//    the 128-byte-swizzled activation tiles per stage; 16 dequant warps in
+//    groups of four (stages round-robin over groups) turn the codes into exact
 //    bf16 (value * 2^-7) and store them straight into tensor memory as the
 //    MMA's A operand (tcgen05.st), so no dequantised weight touches shared
 //    memory; one MMA warp (operands warp-uniform, one elected lane issuing)
@@ -42,8 +42,8 @@
 namespace moe {
 
 constexpr int kWarpEpi0 = 0;       // warps 0..3: epilogue (TMEM lane quadrant = warp)
-constexpr int kWarpDq0 = 4;        // warps 4..19: dequant, 4 groups x 4 quadrants
-constexpr int kDqGroups = 4;       // group g dequantises stages g, g+4, g+8, ...
+constexpr int kWarpDq0 = 4;        // warps 4..19: dequant (groups of 4 x split warps)
+constexpr int kDqWarps = 16;
 constexpr int kWarpProducer = 20;  // warp 20: copies
 constexpr int kWarpMma = 21;       // warp 21: TMEM owner + MMA issue
 constexpr int kThreads = 22 * 32;
@@ -61,11 +61,29 @@ struct Cfg {
   static constexpr int kBTile = SB * kBSub;
   static constexpr int kWBytes = SB * kWBlockBytes;
   static constexpr int kStageBytes = kWBytes + kBTile;
-  static constexpr int NS0 = kSmemBudget / kStageBytes;
-  static constexpr int NS = NS0 > 16 ? 16 : (NS0 < 2 ? 2 : NS0);
   static constexpr int A0 = (2 * BN < 32) ? 32 : 2 * BN;
   static constexpr int kSlotCols = 32 * SB;
   static constexpr int NA = (int)(kTmemCols - A0) / kSlotCols;
+  // A stage's SB blocks are split over kSplit warps per TMEM lane quadrant,
+  // so a dequant group has 4 * kSplit warps; groups take stages round-robin.
+  static constexpr int kSplit = 1;
+  static constexpr int kGroupWarps = 4 * kSplit;
+  static constexpr int kGroups0 = kDqWarps / kGroupWarps;
+  // Parity waits are exact only while the awaited barrier cannot be two
+  // phases behind the waiter.  A group waits for (a) TMEM slot i % NA to be
+  // free (MMA of stage i - NA done) and (b) smem slot i % NS to hold stage i.
+  // (a) Its own previous stage i - G waited for the MMA of stage i - G - NA,
+  //     which covers stage i - 2 NA only when G <= NA.
+  // (b) Stage i - NS (the slot's previous phase) must have landed.  Copies do
+  //     not complete in issue order, so either G | NS (stage i - NS is the
+  //     group's own, already waited on) or NS >= G + NA (the group's previous
+  //     stage saw the in-order MMA pass stage i - G - NA >= i - NS, and every
+  //     MMA waited for its stage's copy).
+  static constexpr int G = kGroups0 < NA ? kGroups0 : NA;
+  static constexpr int NS0 = kSmemBudget / kStageBytes;
+  static constexpr int NS1 = NS0 > 16 ? 16 : NS0;
+  static constexpr int NS = NS1 >= G + NA ? NS1 : (NS1 < G ? G : (NS1 / G) * G);
+  static_assert(G <= NA && (NS % G == 0 || NS >= G + NA), "dequant groups must fit the TMEM and smem rings");
   static constexpr int kOffB = 0;
   static constexpr int kOffW = NS * kBTile;
   static constexpr int kOffBar = kOffW + NS * kWBytes;
@@ -157,10 +175,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < NS; ++s) {
       mbar_init(full_bar(s), 1);
-      mbar_init(empty_bar(s), 4 + 1);  // the stage's 4 dequant warps + the MMA commit
+      mbar_init(empty_bar(s), C::kGroupWarps + 1);  // the stage's dequant warps + the MMA commit
     }
     for (int a = 0; a < NA; ++a) {
-      mbar_init(afull_bar(a), 4);
+      mbar_init(afull_bar(a), C::kGroupWarps);
       mbar_init(aempty_bar(a), 1);
     }
     for (int d = 0; d < 2; ++d) {
@@ -284,13 +302,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_wait(drain_bar, 0, nullptr, status, kDrainTimeoutNs);
   } else if (warp >= kWarpDq0) {
     // ------------------------------------------------------------- dequant
-    // At most NA groups: a group's wait for slot i % NA (MMA of stage i - NA
-    // done) must never run two phases ahead of that barrier, or its parity
-    // test would alias.  Its own previous stage i - G waited for MMA of stage
-    // i - G - NA, which covers stage i - 2 NA only when G <= NA.
-    constexpr int G = NA < kDqGroups ? NA : kDqGroups;
-    const int q = warp & 3;
-    const int group = (warp - kWarpDq0) >> 2;
+    constexpr int G = C::G, kBlocksPerWarp = SB / C::kSplit;
+    const int dw = warp - kWarpDq0;
+    const int q = warp & 3;  // TMEM lane quadrant this warp may access
+    const int group = dw / C::kGroupWarps;
+    const int part = (dw % C::kGroupWarps) >> 2;
     const int r = 32 * q + lane;
     const uint32_t t_row = tmem_base + ((uint32_t)(32 * q) << 16) + (uint32_t)C::A0;
 #pragma unroll 1
@@ -303,10 +319,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const uint8_t* stage_w = smem + C::kOffW + s * C::kWBytes;
 #pragma unroll 1
-      for (int b = 0; b < SB; ++b) {
+      for (int bb = 0; bb < kBlocksPerWarp; ++bb) {
+        const int b = part * kBlocksPerWarp + bb;
         uint32_t v[32];
         dequant_block(stage_w + b * kWBlockBytes, r, v);
-        if (b == SB - 1) {
+        if (bb == kBlocksPerWarp - 1) {
           __syncwarp();
           if (lane == 0) mbar_arrive(empty_bar(s));  // codes are in registers: the stage may be refilled
         }
@@ -441,12 +458,13 @@ static int pick_bn(int rows, int E) {
   return 128;
 }
 
-// K blocks per stage: 4 for narrow token tiles (decode: amortise the MMA warp's
-// per-stage cost), 2 for wide ones (keeps two TMEM A slots next to 2 x BN
-// accumulator columns), 1 when K/64 is not a multiple.
+// K blocks per stage: 4 for the narrowest token tile (decode: amortise the MMA
+// warp's per-stage cost), 2 otherwise (keeps enough TMEM A slots next to the
+// 2 x BN accumulator columns and a deep enough shared-memory ring), 1 when K/64
+// is not a multiple.
 template <int BN, int MODE>
 static cudaError_t launch_gemm_bn(const GemmArgs& a, cudaStream_t s) {
-  constexpr int kWide = (BN <= 32) ? 4 : 2;
+  constexpr int kWide = (BN <= 16) ? 4 : 2;
   const int KB = a.K / kBlockK;
   if (KB % kWide == 0) return launch_gemm_cfg<BN, kWide, MODE>(a, s);
   return launch_gemm_cfg<BN, 1, MODE>(a, s);
@@ -476,8 +494,8 @@ cudaError_t launch_gemm(int mode, const GemmArgs& a, cudaStream_t s) {
 //   codes  [half 0..1][row 0..127][16 B] at (half * 128 + row) * 16: K
 //          elements 32*half .. 32*half+31 of the row as 4 words of 8;
 //   scales [row][4] at 4096 + row * 4: the row's four E4M3 block scales.
-// Packed word w holds elements 8w..8w+7: even elements in nibbles 0..3 of the
-// low 16 bits, odd elements in nibbles 0..3 of the high 16 bits.
+// Packed word w holds elements 8w..8w+7 in the slot placement of
+// nvfp4_pack_word (device_common.cuh).
 // One thread per (expert, tile, K block, half, row) moves 16 code bytes and
 // the two scales of those 32 elements.
 __global__ void prepack_kernel(const uint8_t* __restrict__ codes, const uint8_t* __restrict__ scales, int E, int N,
@@ -505,14 +523,14 @@ __global__ void prepack_kernel(const uint8_t* __restrict__ codes, const uint8_t*
   uint32_t words[4];
 #pragma unroll
   for (int w = 0; w < 4; ++w) {
-    uint32_t o = 0;
+    uint32_t c8[8];
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-      const uint32_t b = cs[4 * w + j];
-      o |= (b & 0xFu) << (4 * j);
-      o |= (b >> 4) << (16 + 4 * j);
+      const uint32_t b = cs[4 * w + j];  // elements 8w+2j (low nibble) and 8w+2j+1 (high nibble)
+      c8[2 * j] = b & 0xFu;
+      c8[2 * j + 1] = b >> 4;
     }
-    words[w] = o;
+    words[w] = nvfp4_pack_word(c8);
   }
   uint8_t* dst = packed + blk * kWBlockBytes;
   *reinterpret_cast<uint4*>(dst + (half * 128 + r) * 16) = make_uint4(words[0], words[1], words[2], words[3]);
@@ -543,11 +561,9 @@ __global__ void dequant_table_kernel(uint16_t* __restrict__ out) {
   uint32_t s_lo, s_hi;
   e4m3x2_to_scaleprime(pair, s_lo, s_hi);
   for (int w = 0; w < 2; ++w) {
-    uint32_t q = 0;
-    for (int j = 0; j < 4; ++j) {
-      q |= (uint32_t)(8 * w + 2 * j) << (4 * j);
-      q |= (uint32_t)(8 * w + 2 * j + 1) << (16 + 4 * j);
-    }
+    uint32_t c8[8];
+    for (int j = 0; j < 8; ++j) c8[j] = (uint32_t)(8 * w + j);
+    const uint32_t q = nvfp4_pack_word(c8);
     uint32_t lo[4], hi[4];
     dequant_word(q, s_lo, lo);
     dequant_word(q, s_hi, hi);

@@ -9,10 +9,6 @@
 #include "moe_w4a16.h"
 #include "kernels.h"
 
-namespace moe {
-cudaError_t launch_gemm_simt(int mode, const GemmArgs& a, cudaStream_t s);
-}
-
 namespace {
 
 constexpr size_t kAlign = 256;
@@ -86,18 +82,7 @@ int cuda_status(cudaError_t e) {
   return MOE_ERR_CUDA;
 }
 
-bool use_simt() {
-  static int v = -1;
-  if (v < 0) {
-    const char* s = std::getenv("MOE_GEMM_IMPL");
-    v = (s != nullptr && std::strcmp(s, "simt") == 0) ? 1 : 0;
-  }
-  return v == 1;
-}
-
-cudaError_t run_gemm(int mode, const moe::GemmArgs& a, cudaStream_t s) {
-  return use_simt() ? moe::launch_gemm_simt(mode, a, s) : moe::launch_gemm(mode, a, s);
-}
+cudaError_t run_gemm(int mode, const moe::GemmArgs& a, cudaStream_t s) { return moe::launch_gemm(mode, a, s); }
 
 #define MOE_TRY(expr)            \
   do {                           \
