@@ -342,14 +342,14 @@ def run_ours(args, wl, dist, rank, world, local_rank):
                            "frac_hbm": layer_bytes / (mean_step_ms * 1e-3) / 1e9 / hbm_peak,
                            "achieved_tflops": layer_flops / (mean_step_ms * 1e-3) / 1e12},
         "stages_ms": {nm: float(stage_ms[:, i].mean()) for i, nm in
-                      enumerate(["route", "permute", "gate_up_swiglu", "down", "combine"])},
+                      enumerate(["route_group", "gather", "gate_up_swiglu", "down", "combine"])},
         "wall_s_timed_loop": t_wall,
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": wl.T * wl.H * 2 + wl.T * wl.E * 4,
                 "d2h_bytes_per_step": wl.T * wl.H * 2},
         "cpu_baseline": cpu,
-        # route + permute (one block when T*k <= 1024, else histogram / scan / scatter) + row
-        # gather + gate_up + down + combine
-        "gpu_launches": (1 + (1 if n <= 1024 else 3) + 1 + 1 + 1 + 1) * args.steps,
+        # routing + grouping (one fused block when T*k <= 1024, else route / histogram /
+        # scan / scatter) + row gather + gate_up + down + combine
+        "gpu_launches": ((1 if n <= 1024 else 4) + 1 + 1 + 1 + 1) * args.steps,
         "clocks": clk,
     }
     print(json.dumps(line), flush=True)

@@ -189,8 +189,10 @@ int moe_layer_forward(const uint16_t *x, const float *logits, moe_w4 w_gate_up, 
 
 /* moe_layer_forward with per-stage timing: stage_events points to 6
  * cudaEvent_t handles (created by the caller; any entry may be NULL).
- * stage_events[i] is recorded on `stream` just before stage i (0 route,
- * 1 permute, 2 gate_up+SwiGLU, 3 down, 4 combine) and stage_events[5] after
+ * stage_events[i] is recorded on `stream` just before stage i (0 routing and
+ * grouping: top-k ids and weights, counts, offsets, sorted_token, inv_perm;
+ * 1 the row gather into x_perm; 2 gate_up+SwiGLU, 3 down, 4 combine) and
+ * stage_events[5] after
  * the last, so cudaEventElapsedTime(ev[2], ev[3]) is the gate_up launch.
  * Same results and launches as moe_layer_forward. */
 int moe_layer_forward_profiled(const uint16_t *x, const float *logits, moe_w4 w_gate_up, moe_w4 w_down,

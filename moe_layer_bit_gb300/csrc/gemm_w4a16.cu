@@ -18,9 +18,11 @@
 //  * a pipeline stage is SB consecutive 64-column K blocks (a "superstage"),
 //    so the per-stage barrier round trips of the single MMA-issuing warp are
 //    paid once per SB*4 MMAs;
-//  * warp roles: a producer warp issues one 1-D bulk copy of the SB packed
-//    weight blocks (codes + E4M3 scales, SB * 4608 B) and SB 2-D TMA copies of
-//    the 128-byte-swizzled activation tiles per stage; 16 dequant warps in
+//  * warp roles: one producer warp issues one 1-D bulk copy of the SB packed
+//    weight blocks (codes + E4M3 scales, SB * 4608 B) per stage into a weight
+//    ring that is freed as soon as the codes are in registers; a second one
+//    issues SB 2-D TMA copies of the 128-byte-swizzled activation tiles into a
+//    ring freed by the MMA commit; 16 dequant warps in
 //    groups of four (stages round-robin over groups) turn the codes into exact
 //    bf16 (value * 2^-7) and store them straight into tensor memory as the
 //    MMA's A operand (tcgen05.st), so no dequantised weight touches shared
@@ -44,23 +46,23 @@ namespace moe {
 constexpr int kWarpEpi0 = 0;       // warps 0..3: epilogue (TMEM lane quadrant = warp)
 constexpr int kWarpDq0 = 4;        // warps 4..19: dequant (groups of 4 x split warps)
 constexpr int kDqWarps = 16;
-constexpr int kWarpProducer = 20;  // warp 20: copies
+constexpr int kWarpProducer = 20;  // warp 20: weight copies
 constexpr int kWarpMma = 21;       // warp 21: TMEM owner + MMA issue
-constexpr int kThreads = 22 * 32;
+constexpr int kWarpProducerB = 22; // warp 22: activation-tile copies
+constexpr int kThreads = 23 * 32;
 constexpr uint32_t kTmemCols = 512;
 constexpr int kMinSmem = 120 * 1024;  // keeps one CTA (one TMEM allocation) per SM
 constexpr int kSmemBudget = 200 * 1024;
 
-// Token-tile width BN and SB K blocks per stage: a shared-memory ring of NS
-// stages (SB packed weight blocks + SB activation sub-tiles) and a TMEM ring of
-// NA A-operand slots of 32*SB columns (128 rows x 64*SB bf16) placed after the
-// two BN-column accumulators.
+// Token-tile width BN and SB K blocks per stage: shared-memory rings of NSW
+// weight stages (SB packed blocks) and NSB activation stages (SB sub-tiles),
+// and a TMEM ring of NA A-operand slots of 32*SB columns (128 rows x 64*SB
+// bf16) placed after the two BN-column accumulators.
 template <int BN, int SB>
 struct Cfg {
   static constexpr int kBSub = BN * 128;  // BN rows x 64 bf16, 128-byte swizzled
   static constexpr int kBTile = SB * kBSub;
   static constexpr int kWBytes = SB * kWBlockBytes;
-  static constexpr int kStageBytes = kWBytes + kBTile;
   static constexpr int A0 = (2 * BN < 32) ? 32 : 2 * BN;
   static constexpr int kSlotCols = 32 * SB;
   static constexpr int NA = (int)(kTmemCols - A0) / kSlotCols;
@@ -69,26 +71,31 @@ struct Cfg {
   static constexpr int kSplit = 1;
   static constexpr int kGroupWarps = 4 * kSplit;
   static constexpr int kGroups0 = kDqWarps / kGroupWarps;
+  static constexpr int G = kGroups0 < NA ? kGroups0 : NA;
+  // Two shared-memory rings: NSB activation tiles (freed by the MMA commit)
+  // and NSW weight blocks (freed as soon as the dequant warps hold the codes in
+  // registers, so weight prefetch depth does not wait on the MMA).
+  static constexpr int NSB = 4;
+  static constexpr int NSW0 = (kSmemBudget - NSB * kBTile) / kWBytes;
+  static constexpr int NSW1 = NSW0 > 12 ? 12 : NSW0;
   // Parity waits are exact only while the awaited barrier cannot be two
-  // phases behind the waiter.  A group waits for (a) TMEM slot i % NA to be
-  // free (MMA of stage i - NA done) and (b) smem slot i % NS to hold stage i.
+  // phases behind the waiter.  A dequant group waits for (a) TMEM slot i % NA
+  // to be free (MMA of stage i - NA done) and (b) weight slot i % NSW to hold
+  // stage i.
   // (a) Its own previous stage i - G waited for the MMA of stage i - G - NA,
   //     which covers stage i - 2 NA only when G <= NA.
-  // (b) Stage i - NS (the slot's previous phase) must have landed.  Copies do
-  //     not complete in issue order, so either G | NS (stage i - NS is the
-  //     group's own, already waited on) or NS >= G + NA (the group's previous
-  //     stage saw the in-order MMA pass stage i - G - NA >= i - NS, and every
-  //     MMA waited for its stage's copy).
-  static constexpr int G = kGroups0 < NA ? kGroups0 : NA;
-  static constexpr int NS0 = kSmemBudget / kStageBytes;
-  static constexpr int NS1 = NS0 > 16 ? 16 : NS0;
-  static constexpr int NS = NS1 >= G + NA ? NS1 : (NS1 < G ? G : (NS1 / G) * G);
-  static_assert(G <= NA && (NS % G == 0 || NS >= G + NA), "dequant groups must fit the TMEM and smem rings");
+  // (b) Stage i - NSW (the slot's previous phase) must have landed; copies do
+  //     not complete in issue order, so G | NSW makes it the group's own,
+  //     already waited on.
+  // The activation ring is only waited on by the in-order MMA warp.
+  static constexpr int NSW = NSW1 < G ? G : (NSW1 / G) * G;
+  static_assert(G <= NA && NSW % G == 0, "dequant groups must fit the TMEM and weight rings");
   static constexpr int kOffB = 0;
-  static constexpr int kOffW = NS * kBTile;
-  static constexpr int kOffBar = kOffW + NS * kWBytes;
-  // full[NS], empty[NS], afull[NA], aempty[NA], dfull[2], dempty[2], drain
-  static constexpr int kNumBars = 2 * NS + 2 * NA + 5;
+  static constexpr int kOffW = NSB * kBTile;
+  static constexpr int kOffBar = kOffW + NSW * kWBytes;
+  // fullw[NSW], emptyw[NSW], fullb[NSB], emptyb[NSB], afull[NA], aempty[NA],
+  // dfull[2], dempty[2], drain
+  static constexpr int kNumBars = 2 * NSW + 2 * NSB + 2 * NA + 5;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;  // [0] tmem base, [1] abort, [2] total tiles
   static constexpr int kOffTables = kOffMisc + 16;         // offsets[E+1], prefix[E+1]
   static_assert(NA >= 1, "TMEM ring needs a slot");
@@ -121,23 +128,34 @@ __device__ __forceinline__ TileCoord decode_tile(int t, const int32_t* prefix, c
   return c;
 }
 
-// Dequantise one 64-column block of row r (codes at blk + r*16 and blk + 2048 +
-// r*16, scales at blk + 4096 + r*4) into 32 bf16x2 columns.
-__device__ __forceinline__ void dequant_block(const uint8_t* blk, int r, uint32_t (&v)[32]) {
-  const uint4 c0 = *reinterpret_cast<const uint4*>(blk + r * 16);
-  const uint4 c1 = *reinterpret_cast<const uint4*>(blk + 2048 + r * 16);
-  const uint32_t sc = *reinterpret_cast<const uint32_t*>(blk + 4096 + r * 4);
+// One 64-column block of row r: codes at blk + r*16 and blk + 2048 + r*16,
+// the four block scales at blk + 4096 + r*4.
+struct BlockCodes {
+  uint4 c0, c1;
+  uint32_t sc;
+};
+
+__device__ __forceinline__ BlockCodes load_block(const uint8_t* blk, int r) {
+  BlockCodes b;
+  b.c0 = *reinterpret_cast<const uint4*>(blk + r * 16);
+  b.c1 = *reinterpret_cast<const uint4*>(blk + 2048 + r * 16);
+  b.sc = *reinterpret_cast<const uint32_t*>(blk + 4096 + r * 4);
+  return b;
+}
+
+// Dequantise a loaded block into 32 bf16x2 columns.
+__device__ __forceinline__ void dequant_block(const BlockCodes& b, uint32_t (&v)[32]) {
   uint32_t s0, s1, s2, s3;
-  e4m3x2_to_scaleprime((uint16_t)(sc & 0xFFFFu), s0, s1);
-  e4m3x2_to_scaleprime((uint16_t)(sc >> 16), s2, s3);
-  dequant_word(c0.x, s0, v + 0);
-  dequant_word(c0.y, s0, v + 4);
-  dequant_word(c0.z, s1, v + 8);
-  dequant_word(c0.w, s1, v + 12);
-  dequant_word(c1.x, s2, v + 16);
-  dequant_word(c1.y, s2, v + 20);
-  dequant_word(c1.z, s3, v + 24);
-  dequant_word(c1.w, s3, v + 28);
+  e4m3x2_to_scaleprime((uint16_t)(b.sc & 0xFFFFu), s0, s1);
+  e4m3x2_to_scaleprime((uint16_t)(b.sc >> 16), s2, s3);
+  dequant_word(b.c0.x, s0, v + 0);
+  dequant_word(b.c0.y, s0, v + 4);
+  dequant_word(b.c0.z, s1, v + 8);
+  dequant_word(b.c0.w, s1, v + 12);
+  dequant_word(b.c1.x, s2, v + 16);
+  dequant_word(b.c1.y, s2, v + 20);
+  dequant_word(b.c1.z, s3, v + 24);
+  dequant_word(b.c1.w, s3, v + 28);
 }
 
 template <int BN, int SB, int MODE>
@@ -146,20 +164,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                       const float* __restrict__ gscale, const int32_t* __restrict__ offsets, void* __restrict__ out,
                       int* __restrict__ status, int E, int N, int K, int out_ld) {
   using C = Cfg<BN, SB>;
-  constexpr int NS = C::NS, NA = C::NA;
+  constexpr int NSW = C::NSW, NSB = C::NSB, NA = C::NA;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
   const uint32_t sB = sbase + C::kOffB;
   const uint32_t sW = sbase + C::kOffW;
   const uint32_t bar0 = sbase + C::kOffBar;
-  auto full_bar = [&](int s) { return bar0 + 8u * s; };
-  auto empty_bar = [&](int s) { return bar0 + 8u * (NS + s); };
-  auto afull_bar = [&](int a) { return bar0 + 8u * (2 * NS + a); };
-  auto aempty_bar = [&](int a) { return bar0 + 8u * (2 * NS + NA + a); };
-  auto dfull_bar = [&](int d) { return bar0 + 8u * (2 * NS + 2 * NA + d); };
-  auto dempty_bar = [&](int d) { return bar0 + 8u * (2 * NS + 2 * NA + 2 + d); };
-  const uint32_t drain_bar = bar0 + 8u * (2 * NS + 2 * NA + 4);
+  auto fullw_bar = [&](int s) { return bar0 + 8u * s; };
+  auto emptyw_bar = [&](int s) { return bar0 + 8u * (NSW + s); };
+  auto fullb_bar = [&](int s) { return bar0 + 8u * (2 * NSW + s); };
+  auto emptyb_bar = [&](int s) { return bar0 + 8u * (2 * NSW + NSB + s); };
+  auto afull_bar = [&](int a) { return bar0 + 8u * (2 * NSW + 2 * NSB + a); };
+  auto aempty_bar = [&](int a) { return bar0 + 8u * (2 * NSW + 2 * NSB + NA + a); };
+  auto dfull_bar = [&](int d) { return bar0 + 8u * (2 * NSW + 2 * NSB + 2 * NA + d); };
+  auto dempty_bar = [&](int d) { return bar0 + 8u * (2 * NSW + 2 * NSB + 2 * NA + 2 + d); };
+  const uint32_t drain_bar = bar0 + 8u * (2 * NSW + 2 * NSB + 2 * NA + 4);
   volatile uint32_t* misc = reinterpret_cast<volatile uint32_t*>(smem + C::kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 4);
   int32_t* s_off = reinterpret_cast<int32_t*>(smem + C::kOffTables);
@@ -173,9 +193,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   // ---- set-up: barriers, TMEM, tile table
   if (threadIdx.x == 0) {
-    for (int s = 0; s < NS; ++s) {
-      mbar_init(full_bar(s), 1);
-      mbar_init(empty_bar(s), C::kGroupWarps + 1);  // the stage's dequant warps + the MMA commit
+    for (int s = 0; s < NSW; ++s) {
+      mbar_init(fullw_bar(s), 1);
+      mbar_init(emptyw_bar(s), C::kGroupWarps);  // the stage's dequant warps
+    }
+    for (int s = 0; s < NSB; ++s) {
+      mbar_init(fullb_bar(s), 1);
+      mbar_init(emptyb_bar(s), 1);  // the MMA commit
     }
     for (int a = 0; a < NA; ++a) {
       mbar_init(afull_bar(a), C::kGroupWarps);
@@ -189,7 +213,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     *abort_flag = 0;
     fence_barrier_init();
   }
-  if (warp == kWarpProducer && lane == 0) prefetch_tmap(&tmap_act);
+  if (warp == kWarpProducerB && lane == 0) prefetch_tmap(&tmap_act);
   if (warp == kWarpMma) {
     tmem_alloc(sbase + C::kOffMisc, kTmemCols);
     tmem_relinquish();
@@ -226,9 +250,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int my_tiles = total > (int)blockIdx.x ? (total - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x : 0;
   const int my_stages = my_tiles * KS;
 
-  if (warp == kWarpProducer) {
-    // ------------------------------------------------------------ producer
-    // The whole warp walks the schedule (uniform values); one elected lane issues.
+  if (warp == kWarpProducer || warp == kWarpProducerB) {
+    // ----------------------------------------------------------- producers
+    // One warp streams the packed weight blocks, the other the activation
+    // tiles; each walks the schedule with uniform values and one elected lane
+    // issues the copies.
+    const bool is_w = warp == kWarpProducer;
+    const int ring = is_w ? NSW : NSB;
     int i = 0;
     bool ok = true;
     for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
@@ -236,25 +264,31 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint8_t* wsrc = packed + (size_t)(c.e * MT + c.mt) * KB * kWBlockBytes;
       const int row0 = s_off[c.e] + c.nt * BN;
       for (int ks = 0; ks < KS; ++ks, ++i) {
-        const int s = i % NS;
-        const uint32_t ph = (uint32_t)(i / NS) & 1u;
-        if (!__all_sync(0xFFFFFFFFu, mbar_wait(empty_bar(s), ph ^ 1u, abort_flag, status))) {
+        const int s = i % ring;
+        const uint32_t ph = (uint32_t)(i / ring) & 1u;
+        const uint32_t ebar = is_w ? emptyw_bar(s) : emptyb_bar(s);
+        if (!__all_sync(0xFFFFFFFFu, mbar_wait(ebar, ph ^ 1u, abort_flag, status))) {
           ok = false;
           break;
         }
         if (elect_one_sync()) {
-          mbar_arrive_expect_tx(full_bar(s), (uint32_t)C::kStageBytes);
-          bulk_copy_g2s(sW + s * C::kWBytes, wsrc + (size_t)ks * C::kWBytes, C::kWBytes, full_bar(s));
+          if (is_w) {
+            mbar_arrive_expect_tx(fullw_bar(s), (uint32_t)C::kWBytes);
+            bulk_copy_g2s(sW + s * C::kWBytes, wsrc + (size_t)ks * C::kWBytes, C::kWBytes, fullw_bar(s));
+          } else {
+            mbar_arrive_expect_tx(fullb_bar(s), (uint32_t)C::kBTile);
 #pragma unroll
-          for (int b = 0; b < SB; ++b)
-            tma_load_2d(sB + s * C::kBTile + b * C::kBSub, &tmap_act, (ks * SB + b) * kBlockK, row0, full_bar(s));
+            for (int b = 0; b < SB; ++b)
+              tma_load_2d(sB + s * C::kBTile + b * C::kBSub, &tmap_act, (ks * SB + b) * kBlockK, row0, fullb_bar(s));
+          }
         }
         __syncwarp();
       }
     }
     // drain: every copy this warp issued has landed before the CTA exits
-    for (int j = (i > NS ? i - NS : 0); j < i; ++j)
-      mbar_wait(full_bar(j % NS), (uint32_t)(j / NS) & 1u, nullptr, status, kDrainTimeoutNs);
+    for (int j = (i > ring ? i - ring : 0); j < i; ++j)
+      mbar_wait(is_w ? fullw_bar(j % ring) : fullb_bar(j % ring), (uint32_t)(j / ring) & 1u, nullptr, status,
+                kDrainTimeoutNs);
   } else if (warp == kWarpMma) {
     // ---------------------------------------------------------- MMA issue
     // The whole warp waits and computes the (uniform) operands; one elected
@@ -269,9 +303,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const uint32_t d_tmem = tmem_base + (uint32_t)(d * BN);
       for (int ks = 0; ks < KS; ++ks, ++i) {
-        const int s = i % NS, a = i % NA;
+        const int s = i % NSB, a = i % NA;
         const bool got = mbar_wait(afull_bar(a), (uint32_t)(i / NA) & 1u, abort_flag, status) &&
-                         mbar_wait(full_bar(s), (uint32_t)(i / NS) & 1u, abort_flag, status);
+                         mbar_wait(fullb_bar(s), (uint32_t)(i / NSB) & 1u, abort_flag, status);
         if (!__all_sync(0xFFFFFFFFu, got)) {
           ok = false;
           break;
@@ -287,7 +321,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               tc_mma_ts(d_tmem, a_tmem + (uint32_t)(32 * b + 8 * kk),
                         b_desc + (uint64_t)((b * C::kBSub + kk * 32) >> 4), idesc, (ks | b | kk) != 0);
           tc_commit(aempty_bar(a));
-          tc_commit(empty_bar(s));
+          tc_commit(emptyb_bar(s));
         }
         __syncwarp();
       }
@@ -311,23 +345,28 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t t_row = tmem_base + ((uint32_t)(32 * q) << 16) + (uint32_t)C::A0;
 #pragma unroll 1
     for (int i = group; group < G && i < my_stages; i += G) {
-      const int s = i % NS, a = i % NA;
+      const int s = i % NSW, a = i % NA;
       // every lane waits (each acquires the copied bytes); the warp acts as one
-      if (!__all_sync(0xFFFFFFFFu, mbar_wait(full_bar(s), (uint32_t)(i / NS) & 1u, abort_flag, status))) break;
+      if (!__all_sync(0xFFFFFFFFu, mbar_wait(fullw_bar(s), (uint32_t)(i / NSW) & 1u, abort_flag, status))) break;
       if (!__all_sync(0xFFFFFFFFu, mbar_wait(aempty_bar(a), ((uint32_t)(i / NA) & 1u) ^ 1u, abort_flag, status)))
         break;
       tc_fence_after();
-      const uint8_t* stage_w = smem + C::kOffW + s * C::kWBytes;
+      const uint8_t* stage_w = smem + C::kOffW + s * C::kWBytes + part * kBlocksPerWarp * kWBlockBytes;
+      // software-pipelined: the next block's codes are loaded while this one is
+      // converted, hiding the shared-memory latency
+      BlockCodes cur = load_block(stage_w, r);
 #pragma unroll 1
       for (int bb = 0; bb < kBlocksPerWarp; ++bb) {
-        const int b = part * kBlocksPerWarp + bb;
-        uint32_t v[32];
-        dequant_block(stage_w + b * kWBlockBytes, r, v);
-        if (bb == kBlocksPerWarp - 1) {
+        BlockCodes nxt = cur;
+        if (bb + 1 < kBlocksPerWarp) nxt = load_block(stage_w + (bb + 1) * kWBlockBytes, r);
+        if (bb + 1 == kBlocksPerWarp) {
           __syncwarp();
-          if (lane == 0) mbar_arrive(empty_bar(s));  // codes are in registers: the stage may be refilled
+          if (lane == 0) mbar_arrive(emptyw_bar(s));  // codes are in registers: the slot may be refilled
         }
-        tmem_st32(t_row + (uint32_t)(C::kSlotCols * a + 32 * b), v);
+        uint32_t v[32];
+        dequant_block(cur, v);
+        tmem_st32(t_row + (uint32_t)(C::kSlotCols * a + 32 * (part * kBlocksPerWarp + bb)), v);
+        cur = nxt;
       }
       tc_wait_st();
       tc_fence_before();

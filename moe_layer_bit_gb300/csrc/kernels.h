@@ -19,6 +19,16 @@ cudaError_t launch_permute(const int32_t* ids, const uint16_t* x, int T, int H, 
                            int32_t* offsets, int32_t* sorted_token, int32_t* inv_perm, uint16_t* x_perm,
                            int32_t* scratch, cudaStream_t s);
 
+// Routing and grouping of the layer: top-k routing, then counts, offsets,
+// sorted_token and inv_perm.  T*k <= 1024 runs as one fused single-block
+// launch; larger batches as routing + histogram + scan + scatter.
+cudaError_t launch_route_group(const float* logits, int T, int E, int k, int32_t* ids, float* w, int32_t* counts,
+                               int32_t* offsets, int32_t* sorted_token, int32_t* inv_perm, int32_t* scratch,
+                               cudaStream_t s);
+// x_perm[p] = x[sorted_token[p]] for p < n.
+cudaError_t launch_gather(const uint16_t* x, const int32_t* sorted_token, int n, int H, uint16_t* x_perm,
+                          cudaStream_t s);
+
 cudaError_t launch_combine(const float* y, const int32_t* inv, const float* w, int T, int H, int k, uint16_t* out,
                            cudaStream_t s);
 

@@ -228,10 +228,10 @@ int layer_forward_impl(const uint16_t* x, const float* logits, moe_w4 w_gate_up,
   uint16_t* h = reinterpret_cast<uint16_t*>(w + L.h);
   float* y = reinterpret_cast<float*>(w + L.y);
   MOE_TRY(mark(0));
-  MOE_TRY(cuda_status(moe::launch_route_topk(logits, d.T, d.E, d.k, ids, wts, s)));
+  MOE_TRY(cuda_status(moe::launch_route_group(logits, d.T, d.E, d.k, ids, wts, counts, offs, sorted, inv,
+                                              reinterpret_cast<int32_t*>(w + L.perm), s)));
   MOE_TRY(mark(1));
-  MOE_TRY(cuda_status(moe::launch_permute(ids, x, d.T, d.H, d.E, d.k, counts, offs, sorted, inv, xp,
-                                          reinterpret_cast<int32_t*>(w + L.perm), s)));
+  MOE_TRY(cuda_status(moe::launch_gather(x, sorted, d.T * d.k, d.H, xp, s)));
   MOE_TRY(mark(2));
   moe::GemmArgs a{};
   a.offsets = offs;

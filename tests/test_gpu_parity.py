@@ -229,6 +229,7 @@ def test_layer_parity(name):
     assert np.array_equal(got, bits(out2)), "layer output not deterministic"
     rids, rw = orc.route(d["logits"].numpy(), wl.k)
     assert np.array_equal(ids.cpu().numpy(), rids)
+    assert np.abs(w.cpu().numpy() - rw).max() <= 2e-6
     if LAYER_SAMPLE[name] is None:
         rows = np.arange(wl.T, dtype=np.int32)
     else:
@@ -263,6 +264,33 @@ def test_layer_edge_shapes(T, H, I, E, k):
     assert layer.device_status() == _lib.MOE_OK
     ref, _, _ = orc.layer(bits(d["x"]), d["logits"].numpy(), gu, dn, k)
     check_layer(bits(out), ref, f"T{T} H{H} I{I} E{E} k{k}")
+
+
+@pytest.mark.parametrize("T,E,k", [
+    (1, 4, 1), (33, 1024, 31), (128, 8, 8),   # one fused routing + grouping block (T*k <= 1024)
+    (129, 8, 8), (300, 96, 5),                # routing, then histogram / scan / scatter
+])
+def test_layer_routing_and_grouping_outputs(T, E, k):
+    # the layer's own top-k ids and weights, NaN and tied logits included
+    H, I = 128, 64
+    d = wk.generate_dims(T, H, I, E, k, seed=T + 31 * E)
+    logits = d["logits"].clone()
+    logits[0, : min(E, 3)] = float("nan")
+    if T > 2:
+        logits[1, :] = float("nan")
+        logits[2, :] = 0.5
+    layer = MoELayer(d["gu"], d["dn"], H, I, E, k, T, DEV)
+    ids = torch.empty(T, k, dtype=torch.int32, device=DEV)
+    w = torch.empty(T, k, dtype=torch.float32, device=DEV)
+    out = layer.forward(d["x"].to(DEV), logits.to(DEV), topk_ids=ids, topk_w=w)
+    assert layer.device_status() == _lib.MOE_OK
+    rids, rw = orc.route(logits.numpy(), k)
+    assert np.array_equal(ids.cpu().numpy(), rids)
+    assert np.abs(w.cpu().numpy() - rw).max() <= 2e-6
+    gu, dn = numpy_weights(d)
+    rows = np.arange(min(T, 16), dtype=np.int32)
+    ref = orc.layer_rows(bits(d["x"]), rids, rw, gu, dn, rows)
+    check_layer(bits(out)[rows], ref, f"T{T} E{E} k{k}")
 
 
 def test_layer_zero_tokens():
