@@ -8,7 +8,8 @@ workload (T=32 tokens, H=2048, I=768, 128 experts, top-8, NVFP4 weights).
 
 ours:      inputs resident in HBM; each timed step is moe_layer_forward_profiled
            (same kernels as moe_layer_forward) bracketed by CUDA events on the
-           launching stream, the L2 flushed (a 2x-L2 buffer written) between steps
+           launching stream, the L2 flushed between steps (a 2x-L2 buffer written, then a
+           second 2x-L2 buffer read so that the flush's own write-backs finish before the step)
            outside the events.  `e2e` runs moe_layer_forward_host: pinned host
            x / logits in, host out back, copies inside the timed region.
 reference: the fp64 CPU oracle (single thread) on a bounded token sample of the
@@ -52,22 +53,78 @@ def _peaks():
 
 # ------------------------------------------------------------------- clocks
 class ClockSampler:
-    """nvidia-smi clock / throttle sampling while the timed region runs."""
+    """SM clock and clock-event (throttle) reasons sampled while the timed region runs.
+
+    Read-only NVML queries (nvmlDeviceGetClockInfo / GetCurrentClocksEventReasons)
+    every ~1 ms from a thread, so even a timed region of a few milliseconds gets
+    samples; falls back to `nvidia-smi -lms 100` when NVML cannot be loaded."""
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    # nvmlClocksEventReason* bits
+    REASON_BITS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+                   0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
 
-    def __init__(self, index: int):
-        self.index = index
+    def __init__(self, device):
+        self.device = device
         self.proc = None
         self.lines = []
         self.thread = None
+        self.nvml = None
+        self.handle = None
+        self.samples = []
+        self.stop_flag = threading.Event()
+
+    def _open_nvml(self):
+        import ctypes
+        try:
+            lib = ctypes.CDLL("libnvidia-ml.so.1")
+        except OSError:
+            return False
+        if lib.nvmlInit_v2() != 0:
+            return False
+        h = ctypes.c_void_p()
+        ok = False
+        try:
+            u = str(torch.cuda.get_device_properties(self.device).uuid)
+            u = u if u.startswith("GPU-") else "GPU-" + u
+            ok = lib.nvmlDeviceGetHandleByUUID(u.encode(), ctypes.byref(h)) == 0
+        except Exception:
+            ok = False
+        if not ok:
+            vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+            idx = self.device.index or 0
+            if vis and vis.split(",")[idx].strip().isdigit():
+                idx = int(vis.split(",")[idx])
+            ok = lib.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(idx), ctypes.byref(h)) == 0
+        if not ok:
+            return False
+        self.reasons_fn = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            getattr(lib, "nvmlDeviceGetCurrentClocksThrottleReasons")
+        self.nvml, self.handle = lib, h
+        return True
+
+    def _poll(self):
+        import ctypes
+        clk, mx, rs = ctypes.c_uint(), ctypes.c_uint(), ctypes.c_ulonglong()
+        while not self.stop_flag.is_set():
+            a = self.nvml.nvmlDeviceGetClockInfo(self.handle, 1, ctypes.byref(clk))        # NVML_CLOCK_SM
+            b = self.nvml.nvmlDeviceGetMaxClockInfo(self.handle, 1, ctypes.byref(mx))
+            c = self.reasons_fn(self.handle, ctypes.byref(rs))
+            if a == 0 and b == 0 and c == 0:
+                self.samples.append((clk.value, mx.value, rs.value))
+            time.sleep(0.001)
 
     def start(self):
+        if self._open_nvml():
+            self.thread = threading.Thread(target=self._poll, daemon=True)
+            self.thread.start()
+            return
         try:
             self.proc = subprocess.Popen(
-                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                ["nvidia-smi", "-i", str(self.device.index or 0), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
             return
@@ -79,30 +136,42 @@ class ClockSampler:
             self.lines.append(line.strip())
 
     def stop(self):
-        if self.proc is None:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
-        self.proc.terminate()
-        try:
-            self.proc.wait(timeout=5)
-        except subprocess.TimeoutExpired:
-            self.proc.kill()
-        self.thread.join(timeout=2)
         sm, smax, reasons = [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
-            parts = [p.strip() for p in ln.split(",")]
-            if len(parts) < 9:
-                continue
+        if self.nvml is not None:
+            self.stop_flag.set()
+            self.thread.join(timeout=2)
+            for c, m, r in self.samples:
+                sm.append(float(c))
+                smax.append(float(m))
+                for bit, nm in self.REASON_BITS.items():
+                    if r & bit:
+                        reasons.add(nm)
+            src = "nvml"
+        elif self.proc is not None:
+            self.proc.terminate()
             try:
-                sm.append(float(parts[1]))
-                smax.append(float(parts[2]))
-            except ValueError:
-                continue
-            for nm, v in zip(names, parts[5:9]):
-                if v.lower() == "active":
-                    reasons.add(nm)
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.thread.join(timeout=2)
+            names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+            for ln in self.lines:
+                parts = [p.strip() for p in ln.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for nm, v in zip(names, parts[5:9]):
+                    if v.lower() == "active":
+                        reasons.add(nm)
+            src = "nvidia-smi"
+        else:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no clock source"], "samples": 0}
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
-                "reasons": sorted(reasons), "samples": len(sm)}
+                "reasons": sorted(reasons), "samples": len(sm), "source": src}
 
 
 # ------------------------------------------------------------ distributed
@@ -243,6 +312,15 @@ def run_ours(args, wl, dist, rank, world, local_rank):
     dims = layer.dims(wl.T)
     l2 = getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 126 * 2 ** 20)
     flush = torch.empty(2 * l2 // 4 + 1024, dtype=torch.float32, device=dev)
+    clean = torch.ones(2 * l2 // 4 + 1024, dtype=torch.float32, device=dev)
+
+    def flush_l2(v):
+        # Write a 2x-L2 buffer (evicts everything the layer touched), then read
+        # another 2x-L2 buffer, so the written lines are back in HBM before the
+        # next step instead of being written back during it.
+        flush.fill_(v)
+        return clean.sum()
+
     stream = torch.cuda.current_stream(dev)
 
     def step(evs):
@@ -251,38 +329,52 @@ def run_ours(args, wl, dist, rank, world, local_rank):
 
     warm_evs = [torch.cuda.Event(enable_timing=True) for _ in range(6)]
     for _ in range(args.warmup):
-        flush.fill_(1.0)
+        flush_l2(1.0)
         step(warm_evs)
     torch.cuda.synchronize(dev)
     status = layer.device_status()
     if status != _lib.MOE_OK:
         raise RuntimeError(f"device status after warm-up: {_lib.status_string(status)}")
 
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(args.steps)]
-    # torch only reports elapsed time between events it has recorded itself; record
-    # each once here (the library records them again inside every timed step)
-    for e in evs:
-        for ev in e:
-            ev.record(stream)
+    def new_events():
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(args.steps)]
+        # torch only reports elapsed time between events it has recorded itself; record
+        # each once here (the library records them again inside every timed step)
+        for e in evs:
+            for ev in e:
+                ev.record(stream)
+        return evs
+
+    def timed_region(evs, stage_marks):
+        """K steps; the L2 flush sits between steps, outside the events.  With
+        stage_marks False only the step's first and last events are recorded, so
+        nothing separates the layer's kernels (their programmatic launch overlap
+        is kept); with True all six are, for the per-stage times."""
+        _barrier(dist, dev)
+        torch.cuda.synchronize(dev)
+        t0 = time.perf_counter()
+        for s in range(args.steps):
+            flush_l2(float(s))
+            e = evs[s] if stage_marks else [evs[s][0], None, None, None, None, evs[s][5]]
+            step(e)
+        torch.cuda.synchronize(dev)
+        _barrier(dist, dev)
+        return time.perf_counter() - t0
+
+    evs = new_events()
+    stage_evs = new_events()
     torch.cuda.synchronize(dev)
-    clocks = ClockSampler(dev.index)
+    clocks = ClockSampler(dev)
     clocks.start()
-    _barrier(dist, dev)
-    torch.cuda.synchronize(dev)
-    t_wall0 = time.perf_counter()
-    for s in range(args.steps):
-        flush.fill_(float(s))                       # L2 flush, outside the step's events
-        step(evs[s])
-    torch.cuda.synchronize(dev)
-    t_wall = time.perf_counter() - t_wall0
-    _barrier(dist, dev)
+    t_wall = timed_region(evs, False)          # the measured steps
+    t_wall_stages = timed_region(stage_evs, True)  # the same steps again, with per-stage events
     clk = clocks.stop()
     status = layer.device_status()
     if status != _lib.MOE_OK:
         raise RuntimeError(f"device status after timing: {_lib.status_string(status)}")
 
     step_ms = [e[0].elapsed_time(e[5]) for e in evs]
-    stage_ms = np.array([[e[i].elapsed_time(e[i + 1]) for i in range(5)] for e in evs])
+    stage_ms = np.array([[e[i].elapsed_time(e[i + 1]) for i in range(5)] for e in stage_evs])
     total_s = sum(step_ms) / 1e3
     total_s_max = _max_over_ranks(dist, total_s, dev)
     value = world * wl.T * args.steps / total_s_max
@@ -295,6 +387,22 @@ def run_ours(args, wl, dist, rank, world, local_rank):
     gu_ms = float(stage_ms[:, 2].mean())
     hbm_peak, tf_peak, tf_sus, peak_kind = _peaks()
     achieved = gu_bytes / (gu_ms * 1e-3) / 1e9
+    gu_flops = 2 * n * (2 * wl.I) * wl.H
+    achieved_tf = gu_flops / (gu_ms * 1e-3) / 1e12
+    # the bound is whichever roof the kernel is closer to: HBM for decode-sized
+    # batches, the bf16 tensor pipe for prefill-sized ones
+    if achieved_tf / tf_peak > achieved / hbm_peak:
+        roofline = {"bound": "tensor", "achieved": achieved_tf, "peak": tf_peak, "unit": "TFLOP/s",
+                    "frac": achieved_tf / tf_peak, "peak_kind": f"{peak_kind} burst cuBLAS bf16 GEMM",
+                    "algorithmic_flops_per_launch": gu_flops}
+    else:
+        roofline = {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
+                    "frac": achieved / hbm_peak, "peak_kind": f"{peak_kind} burst copy bandwidth",
+                    "algorithmic_bytes_per_launch": gu_bytes}
+    roofline.update({"kernel": "w4a16_gemm_kernel (gate_up + SwiGLU)", "traffic": _traffic_from_profile(wl),
+                     "launch_ms": gu_ms,
+                     "other_roof_frac": (achieved / hbm_peak) if roofline["bound"] == "tensor"
+                     else (achieved_tf / tf_peak)})
     layer_bytes = wk.algorithmic_bytes(wl.T, wl.H, wl.I, wl.E, wl.k, counts)
     layer_flops = wk.algorithmic_flops(wl.T, wl.H, wl.I, wl.k)
     mean_step_ms = total_s * 1e3 / args.steps
@@ -307,7 +415,7 @@ def run_ours(args, wl, dist, rank, world, local_rank):
         layer.forward_host(xh, lh, oh, stream)
     e2e_times = []
     for s in range(args.steps):
-        flush.fill_(float(s))
+        flush_l2(float(s))
         torch.cuda.synchronize(dev)
         t0 = time.perf_counter()
         layer.forward_host(xh, lh, oh, stream)      # synchronises before returning
@@ -331,19 +439,17 @@ def run_ours(args, wl, dist, rank, world, local_rank):
         "vs_baseline": None, "dtype": "bf16 x nvfp4 (fp32 accumulate)", "data": "synthetic (seeded, random-init)",
         "config": {"workload": wl.name, "T": wl.T, "H": wl.H, "I": wl.I, "E": wl.E, "k": wl.k,
                    "parallelism": f"replicas x{world}" if world > 1 else "single",
-                   "l2": "flushed between steps (2x L2 write, outside the timed events)",
+                   "l2": "flushed between steps, outside the timed events: a 2x-L2 buffer written, then "
+                         "another 2x-L2 buffer read (the flush's dirty lines reach HBM before the step)",
                    "touched_experts": touched, "layer_bytes": layer_bytes, "layer_flops": layer_flops},
-        "roofline": {"bound": "hbm", "kernel": "w4a16_gemm_kernel (gate_up + SwiGLU)", "achieved": achieved,
-                     "peak": hbm_peak, "unit": "GB/s", "frac": achieved / hbm_peak,
-                     "peak_kind": f"{peak_kind} burst copy bandwidth",
-                     "traffic": _traffic_from_profile(wl), "algorithmic_bytes_per_launch": gu_bytes,
-                     "launch_ms": gu_ms},
+        "roofline": roofline,
         "layer_roofline": {"achieved_gbs": layer_bytes / (mean_step_ms * 1e-3) / 1e9,
                            "frac_hbm": layer_bytes / (mean_step_ms * 1e-3) / 1e9 / hbm_peak,
                            "achieved_tflops": layer_flops / (mean_step_ms * 1e-3) / 1e12},
         "stages_ms": {nm: float(stage_ms[:, i].mean()) for i, nm in
                       enumerate(["route_group", "gather", "gate_up_swiglu", "down", "combine"])},
         "wall_s_timed_loop": t_wall,
+        "wall_s_stage_loop": t_wall_stages,
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": wl.T * wl.H * 2 + wl.T * wl.E * 4,
                 "d2h_bytes_per_step": wl.T * wl.H * 2},
         "cpu_baseline": cpu,

@@ -114,6 +114,11 @@ int moe_prepack_w4(const uint8_t *codes, const uint8_t *scales, int32_t E, int32
  * writes zero counts and offsets; token-sized arrays may then be NULL.
  * ------------------------------------------------------------------------ */
 size_t moe_workspace_bytes(moe_dims d);
+
+/* Number of kernels one moe_layer_forward call with these dims launches on
+ * its stream (0 for T == 0); minus a moe_status code if d is invalid.  Host
+ * only: touches no device. */
+int moe_layer_kernel_launches(moe_dims d);
 size_t moe_stage_workspace_bytes(moe_dims d);
 
 /* [Atlas] "KV Cache量化…" (gate logits -> expert IDs), [ATOM] 8.1 (top-k).

@@ -52,6 +52,7 @@ _SIGS = {
     "moe_packed_w4_bytes": (SZ, [I32, I32, I32]),
     "moe_prepack_w4": (INT, [P, P, I32, I32, I32, I32, P, P]),
     "moe_workspace_bytes": (SZ, [Dims]),
+    "moe_layer_kernel_launches": (ctypes.c_int, [Dims]),
     "moe_stage_workspace_bytes": (SZ, [Dims]),
     "moe_route_topk": (INT, [P, Dims, P, P, P]),
     "moe_permute": (INT, [P, P, Dims, P, P, P, P, P, P, SZ, P]),
@@ -134,6 +135,10 @@ def moe_prepack_w4(codes, scales, E, N, K, proj, packed, stream=None):
 
 def moe_workspace_bytes(d: Dims) -> int:
     return int(load().moe_workspace_bytes(d))
+
+
+def moe_layer_kernel_launches(d: Dims) -> int:
+    return int(load().moe_layer_kernel_launches(d))
 
 
 def moe_stage_workspace_bytes(d: Dims) -> int:

@@ -27,6 +27,17 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
+// ------------------------------------------------- programmatic dependent launch
+// A kernel launched with programmatic stream serialization may begin while the
+// kernel before it in the stream is still running.  pdl_wait() blocks until
+// that predecessor grid has completed and its memory writes are visible (it
+// returns at once when there is no programmatic predecessor); every kernel of
+// the library calls it before its first global-memory access, so the overlap
+// covers only launch and on-chip set-up.  pdl_trigger() lets the successor
+// start launching once every CTA of this grid has called it or exited.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // ------------------------------------------------------------------ mbarrier
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
@@ -81,13 +92,19 @@ __device__ __forceinline__ bool elect_one_sync() {
 // Bounded wait for the phase with the given parity to complete.  Returns false
 // if the CTA-wide abort flag is raised or the wait exceeds `limit_ns`; in the
 // latter case it raises the abort flag and records a timeout in `status`.
+// try_wait gives up after a short hardware-chosen time, so a long wait loops;
+// a waiter off the critical path passes `sleep_ns` to yield its issue slots
+// between polls, and the abort flag and clock are read every 16th poll only.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                          int* status, unsigned long long limit_ns = kWaitTimeoutNs) {
+                                          int* status, unsigned long long limit_ns = kWaitTimeoutNs,
+                                          uint32_t sleep_ns = 0) {
   if (mbar_test_wait(bar, parity)) return true;
   const unsigned long long t0 = globaltimer_ns();
 #pragma unroll 1
-  while (true) {
+  for (uint32_t n = 1;; ++n) {
     if (mbar_try_wait(bar, parity)) return true;
+    if (sleep_ns != 0) __nanosleep(sleep_ns);
+    if ((n & 15u) != 0) continue;
     if (abort_flag != nullptr && *abort_flag) return false;
     if (globaltimer_ns() - t0 > limit_ns) {
       if (abort_flag != nullptr) *abort_flag = 1;
@@ -113,6 +130,24 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tmap, int3
 }
 __device__ __forceinline__ void prefetch_tmap(const void* tmap) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(tmap) : "memory");
+}
+
+// 16-byte cp.async into shared memory through L2 (no L1 allocation); the
+// bytes past `src_bytes` (0 or 16) are zero-filled and not read.  Completion
+// is tracked per thread with commit / wait groups.
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+// Waits until at most N of this thread's committed groups are still in flight.
+template <int N>
+__device__ __forceinline__ void cp_async_wait_group() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+// Makes this thread's completed generic-proxy shared-memory writes (plain
+// stores, cp.async) visible to later async-proxy reads (tcgen05.mma operands).
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
 // ------------------------------------------------------------------ tcgen05

@@ -21,8 +21,10 @@
 //  * warp roles: one producer warp issues one 1-D bulk copy of the SB packed
 //    weight blocks (codes + E4M3 scales, SB * 4608 B) per stage into a weight
 //    ring that is freed as soon as the codes are in registers; a second one
-//    issues SB 2-D TMA copies of the 128-byte-swizzled activation tiles into a
-//    ring freed by the MMA commit; 16 dequant warps in
+//    fills a ring of 128-byte-swizzled activation tiles, freed by the MMA
+//    commit: SB 2-D TMA copies of a permuted copy of the rows for wide token
+//    tiles, and for narrow ones (16 or 32 rows: decode) 16-byte cp.async of
+//    row sorted_token[p] of x itself, so no permuted copy is written; 16 dequant warps in
 //    groups of four (stages round-robin over groups) turn the codes into exact
 //    bf16 (value * 2^-7) and store them straight into tensor memory as the
 //    MMA's A operand (tcgen05.st), so no dequantised weight touches shared
@@ -34,11 +36,13 @@
 //  * every barrier wait is bounded (about 1 s); on expiry the CTA records a
 //    timeout in the status word, drains its copies and MMAs and exits.
 #include <cstdint>
+#include <cstring>
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
 #include "device_common.cuh"
+#include "gemm_common.cuh"
 #include "kernels.h"
 
 namespace moe {
@@ -52,7 +56,8 @@ constexpr int kWarpProducerB = 22; // warp 22: activation-tile copies
 constexpr int kThreads = 23 * 32;
 constexpr uint32_t kTmemCols = 512;
 constexpr int kMinSmem = 120 * 1024;  // keeps one CTA (one TMEM allocation) per SM
-constexpr int kSmemBudget = 200 * 1024;
+constexpr int kSmemBudget = 216 * 1024;  // rings; the tile table (<= 8 KiB) and alignment slack on top
+constexpr int kBInFlight = 2;  // activation stages a gathering producer lane keeps in flight
 
 // Token-tile width BN and SB K blocks per stage: shared-memory rings of NSW
 // weight stages (SB packed blocks) and NSB activation stages (SB sub-tiles),
@@ -75,7 +80,13 @@ struct Cfg {
   // Two shared-memory rings: NSB activation tiles (freed by the MMA commit)
   // and NSW weight blocks (freed as soon as the dequant warps hold the codes in
   // registers, so weight prefetch depth does not wait on the MMA).
-  static constexpr int NSB = 4;
+  // Narrow token tiles (BN <= 32: decode-sized batches) gather their
+  // activation rows with cp.async (row sorted_token[p] of x, or row p); an
+  // activation stage is then released kBInFlight stages after it was issued,
+  // so that ring is deeper.  Wider tiles read permuted rows with TMA.
+  static constexpr bool kGatherB = BN <= 32;
+  static constexpr int NSB = kGatherB ? 4 + kBInFlight : 4;
+  static_assert(!kGatherB || NSB > kBInFlight, "the gathering producer must not wait on a stage it has not released");
   static constexpr int NSW0 = (kSmemBudget - NSB * kBTile) / kWBytes;
   static constexpr int NSW1 = NSW0 > 12 ? 12 : NSW0;
   // Parity waits are exact only while the awaited barrier cannot be two
@@ -106,61 +117,10 @@ struct Cfg {
   }
 };
 
-struct TileCoord {
-  int e, mt, nt;
-};
-
-// Largest e with prefix[e] <= t (experts with no tiles have prefix[e] == prefix[e+1]).
-__device__ __forceinline__ TileCoord decode_tile(int t, const int32_t* prefix, const int32_t* offs, int E, int BN) {
-  int lo = 0, hi = E;
-  while (hi - lo > 1) {
-    const int mid = (lo + hi) >> 1;
-    if (prefix[mid] <= t) lo = mid;
-    else hi = mid;
-  }
-  const int cnt = offs[lo + 1] - offs[lo];
-  const int nt_count = (cnt + BN - 1) / BN;
-  const int local = t - prefix[lo];
-  TileCoord c;
-  c.e = lo;
-  c.mt = local / nt_count;
-  c.nt = local - c.mt * nt_count;
-  return c;
-}
-
-// One 64-column block of row r: codes at blk + r*16 and blk + 2048 + r*16,
-// the four block scales at blk + 4096 + r*4.
-struct BlockCodes {
-  uint4 c0, c1;
-  uint32_t sc;
-};
-
-__device__ __forceinline__ BlockCodes load_block(const uint8_t* blk, int r) {
-  BlockCodes b;
-  b.c0 = *reinterpret_cast<const uint4*>(blk + r * 16);
-  b.c1 = *reinterpret_cast<const uint4*>(blk + 2048 + r * 16);
-  b.sc = *reinterpret_cast<const uint32_t*>(blk + 4096 + r * 4);
-  return b;
-}
-
-// Dequantise a loaded block into 32 bf16x2 columns.
-__device__ __forceinline__ void dequant_block(const BlockCodes& b, uint32_t (&v)[32]) {
-  uint32_t s0, s1, s2, s3;
-  e4m3x2_to_scaleprime((uint16_t)(b.sc & 0xFFFFu), s0, s1);
-  e4m3x2_to_scaleprime((uint16_t)(b.sc >> 16), s2, s3);
-  dequant_word(b.c0.x, s0, v + 0);
-  dequant_word(b.c0.y, s0, v + 4);
-  dequant_word(b.c0.z, s1, v + 8);
-  dequant_word(b.c0.w, s1, v + 12);
-  dequant_word(b.c1.x, s2, v + 16);
-  dequant_word(b.c1.y, s2, v + 20);
-  dequant_word(b.c1.z, s3, v + 24);
-  dequant_word(b.c1.w, s3, v + 28);
-}
-
 template <int BN, int SB, int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
-    w4a16_gemm_kernel(const __grid_constant__ CUtensorMap tmap_act, const uint8_t* __restrict__ packed,
+    w4a16_gemm_kernel(const __grid_constant__ CUtensorMap tmap_act, const uint16_t* __restrict__ act,
+                      const int32_t* __restrict__ gather_rows, const uint8_t* __restrict__ packed,
                       const float* __restrict__ gscale, const int32_t* __restrict__ offsets, void* __restrict__ out,
                       int* __restrict__ status, int E, int N, int K, int out_ld) {
   using C = Cfg<BN, SB>;
@@ -213,35 +173,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     *abort_flag = 0;
     fence_barrier_init();
   }
-  if (warp == kWarpProducerB && lane == 0) prefetch_tmap(&tmap_act);
+  if (!C::kGatherB && warp == kWarpProducerB && lane == 0) prefetch_tmap(&tmap_act);
   if (warp == kWarpMma) {
     tmem_alloc(sbase + C::kOffMisc, kTmemCols);
     tmem_relinquish();
   }
-  for (int i = threadIdx.x; i <= E; i += blockDim.x) s_off[i] = __ldg(offsets + i);
-  __syncthreads();
-  if (warp == 0) {
-    // prefix[e] = first tile of expert e; tiles of e = ceil(count/BN) * MT
-    const int per = (E + 31) / 32;
-    const int e0 = lane * per;
-    int sum = 0;
-    for (int e = e0; e < e0 + per && e < E; ++e) sum += ((s_off[e + 1] - s_off[e] + BN - 1) / BN) * MT;
-    int incl = sum;
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-      const int y = __shfl_up_sync(0xFFFFFFFFu, incl, off);
-      if (lane >= off) incl += y;
-    }
-    int run = incl - sum;
-    for (int e = e0; e < e0 + per && e < E; ++e) {
-      s_prefix[e] = run;
-      run += ((s_off[e + 1] - s_off[e] + BN - 1) / BN) * MT;
-    }
-    if (lane == 31) {
-      s_prefix[E] = incl;
-      misc[2] = (uint32_t)incl;
-    }
-  }
+  // everything above is on-chip; the expert offsets come from the kernel before
+  pdl_wait();
+  pdl_trigger();
+  build_tile_table(offsets, E, BN, MT, s_off, s_prefix, misc + 2);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -250,11 +190,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int my_tiles = total > (int)blockIdx.x ? (total - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x : 0;
   const int my_stages = my_tiles * KS;
 
-  if (warp == kWarpProducer || warp == kWarpProducerB) {
+  if (warp == kWarpProducer || (warp == kWarpProducerB && !C::kGatherB)) {
     // ----------------------------------------------------------- producers
-    // One warp streams the packed weight blocks, the other the activation
-    // tiles; each walks the schedule with uniform values and one elected lane
-    // issues the copies.
+    // One warp streams the packed weight blocks, the other (wide token
+    // tiles) the permuted activation tiles by TMA; each walks the schedule with
+    // uniform values and one elected lane issues the copies.
     const bool is_w = warp == kWarpProducer;
     const int ring = is_w ? NSW : NSB;
     int i = 0;
@@ -289,6 +229,56 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int j = (i > ring ? i - ring : 0); j < i; ++j)
       mbar_wait(is_w ? fullw_bar(j % ring) : fullb_bar(j % ring), (uint32_t)(j / ring) & 1u, nullptr, status,
                 kDrainTimeoutNs);
+  } else if (warp == kWarpProducerB) {
+    // ------------------------------------- activation rows, gathered (BN <= 32)
+    // Lane -> (row r, 16-byte chunks c0 .. c0 + kChunks - 1 of every 64-column
+    // block); chunk c of row r lands at r * 128 + ((c ^ (r & 7)) * 16), the
+    // 128-byte swizzle the MMA's shared-memory descriptor expects.  Rows past
+    // the expert's last token are zero-filled, not read.
+    constexpr int kChunks = BN == 16 ? 4 : 8;
+    const int r = BN == 16 ? (lane & 15) : lane;
+    const int c0 = BN == 16 ? (lane >> 4) * 4 : 0;
+    uint32_t dst_off[kChunks];
+#pragma unroll
+    for (int j = 0; j < kChunks; ++j) dst_off[j] = (uint32_t)(r * 128 + (((c0 + j) ^ (r & 7)) * 16));
+    int i = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+      const TileCoord c = decode_tile(t, s_prefix, s_off, E, BN);
+      const int p0 = s_off[c.e] + c.nt * BN;
+      const bool valid = r < s_off[c.e + 1] - p0;
+      const size_t src_row = valid ? (size_t)(gather_rows != nullptr ? gather_rows[p0 + r] : p0 + r) : 0;
+      const uint16_t* rowp = act + src_row * (size_t)K + c0 * 8;
+      const uint32_t nbytes = valid ? 16u : 0u;
+      for (int ks = 0; ks < KS; ++ks, ++i) {
+        const int s = i % NSB;
+        if (!__all_sync(0xFFFFFFFFu, mbar_wait(emptyb_bar(s), ((uint32_t)(i / NSB) & 1u) ^ 1u, abort_flag, status))) {
+          ok = false;
+          break;
+        }
+        const uint32_t dst = sB + s * C::kBTile;
+#pragma unroll
+        for (int b = 0; b < SB; ++b) {
+          const uint16_t* src = rowp + (ks * SB + b) * kBlockK;
+#pragma unroll
+          for (int j = 0; j < kChunks; ++j) cp_async16(dst + b * C::kBSub + dst_off[j], src + j * 8, nbytes);
+        }
+        cp_async_commit();
+        if (i >= kBInFlight) {
+          // stage i - kBInFlight has landed for this lane; after the proxy
+          // fence and the warp sync it is complete for the MMA to read
+          cp_async_wait_group<kBInFlight>();
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(fullb_bar((i - kBInFlight) % NSB));
+        }
+      }
+    }
+    cp_async_wait_group<0>();
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (ok && lane == 0)
+      for (int j = (i > kBInFlight ? i - kBInFlight : 0); j < i; ++j) mbar_arrive(fullb_bar(j % NSB));
   } else if (warp == kWarpMma) {
     // ---------------------------------------------------------- MMA issue
     // The whole warp waits and computes the (uniform) operands; one elected
@@ -456,17 +446,21 @@ static PFN_encodeTiled get_encode_fn() {
 
 template <int BN, int SB, int MODE>
 static cudaError_t launch_gemm_cfg(const GemmArgs& a, cudaStream_t s) {
-  PFN_encodeTiled enc = get_encode_fn();
-  if (enc == nullptr) return cudaErrorNotSupported;
   CUtensorMap tmap;
-  const cuuint64_t gdim[2] = {(cuuint64_t)a.K, (cuuint64_t)a.rows};
-  const cuuint64_t gstride[1] = {(cuuint64_t)a.K * 2};
-  const cuuint32_t box[2] = {(cuuint32_t)kBlockK, (cuuint32_t)BN};
-  const cuuint32_t estride[2] = {1, 1};
-  CUresult r = enc(&tmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(a.act), gdim, gstride, box,
-                   estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+  memset(&tmap, 0, sizeof(tmap));
+  if (!Cfg<BN, SB>::kGatherB) {
+    if (a.gather_rows != nullptr) return cudaErrorInvalidValue;  // TMA tiles read permuted rows only
+    PFN_encodeTiled enc = get_encode_fn();
+    if (enc == nullptr) return cudaErrorNotSupported;
+    const cuuint64_t gdim[2] = {(cuuint64_t)a.K, (cuuint64_t)a.rows};
+    const cuuint64_t gstride[1] = {(cuuint64_t)a.K * 2};
+    const cuuint32_t box[2] = {(cuuint32_t)kBlockK, (cuuint32_t)BN};
+    const cuuint32_t estride[2] = {1, 1};
+    CUresult r = enc(&tmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(a.act), gdim, gstride, box,
+                     estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+  }
 
   int dev = 0, sms = 0;
   cudaError_t err = cudaGetDevice(&dev);
@@ -482,8 +476,8 @@ static cudaError_t launch_gemm_cfg(const GemmArgs& a, cudaStream_t s) {
   auto kern = w4a16_gemm_kernel<BN, SB, MODE>;
   err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (err != cudaSuccess) return err;
-  kern<<<grid, kThreads, smem, s>>>(tmap, a.packed, a.gscale, a.offsets, a.out, a.status, a.E, a.N, a.K, a.out_ld);
-  return cudaGetLastError();
+  return launch_pdl(kern, dim3(grid), dim3(kThreads), smem, s, tmap, a.act, a.gather_rows, a.packed, a.gscale,
+                    a.offsets, a.out, a.status, a.E, a.N, a.K, a.out_ld);
 }
 
 // Token tile width: the smallest of 16/32/64/128 that covers about twice the
@@ -508,6 +502,8 @@ static cudaError_t launch_gemm_bn(const GemmArgs& a, cudaStream_t s) {
   if (KB % kWide == 0) return launch_gemm_cfg<BN, kWide, MODE>(a, s);
   return launch_gemm_cfg<BN, 1, MODE>(a, s);
 }
+
+bool gemm_gathers_rows(int rows, int E, int /*K*/) { return pick_bn(rows, E) <= 32; }
 
 cudaError_t launch_gemm(int mode, const GemmArgs& a, cudaStream_t s) {
   if (a.rows == 0) return cudaSuccess;

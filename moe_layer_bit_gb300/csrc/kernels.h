@@ -4,8 +4,28 @@
 #include <cstdint>
 #include <cuda.h>
 #include <cuda_runtime.h>
+#include <utility>
 
 namespace moe {
+
+// Launches `kern` with programmatic stream serialization: it may start its
+// on-chip set-up while the previous kernel in `s` finishes (the kernels call
+// pdl_wait() before touching global memory).
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                              Args&&... args) {
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
 
 // Packed NVFP4 layout: tiles of 128 weight rows x 64 K elements, 4608 bytes each.
 constexpr int kTileM = 128;
@@ -20,8 +40,9 @@ cudaError_t launch_permute(const int32_t* ids, const uint16_t* x, int T, int H, 
                            int32_t* scratch, cudaStream_t s);
 
 // Routing and grouping of the layer: top-k routing, then counts, offsets,
-// sorted_token and inv_perm.  T*k <= 1024 runs as one fused single-block
-// launch; larger batches as routing + histogram + scan + scatter.
+// sorted_token and inv_perm.  T*k <= 1024 with T*E <= 32768 runs as one
+// single-block launch; otherwise routing, then one grouping block
+// (T*k <= 1024) or histogram + scan + scatter.
 cudaError_t launch_route_group(const float* logits, int T, int E, int k, int32_t* ids, float* w, int32_t* counts,
                                int32_t* offsets, int32_t* sorted_token, int32_t* inv_perm, int32_t* scratch,
                                cudaStream_t s);
@@ -42,6 +63,9 @@ cudaError_t launch_dequant_table(uint16_t* out, cudaStream_t s);
 // [rows = T*k][K]; N = rows of the weight per expert (2I or H).
 struct GemmArgs {
   const uint16_t* act;
+  // nullptr: activation row p is act row p (a permuted copy); otherwise it is
+  // act row gather_rows[p] (narrow token tiles only, see gemm_gathers_rows)
+  const int32_t* gather_rows;
   const uint8_t* packed;
   const float* gscale;
   const int32_t* offsets;
@@ -53,6 +77,13 @@ struct GemmArgs {
   int T, k;
 };
 cudaError_t launch_gemm(int mode, const GemmArgs& a, cudaStream_t s);
+
+// True when launch_gemm picks narrow token tiles (16 or 32 rows) for these
+// sizes; those gather activation rows themselves (GemmArgs::gather_rows).
+bool gemm_gathers_rows(int rows, int E, int K);
+
+// Kernel launches made by launch_route_group for these sizes.
+int route_group_launches(int T, int E, int k);
 
 // Bounded-wait self test: a kernel waits on a barrier nobody arrives at and
 // must give up after `limit_ns`, recording a timeout in `status`.

@@ -90,6 +90,12 @@ cudaError_t run_gemm(int mode, const moe::GemmArgs& a, cudaStream_t s) { return 
     if (_rc != MOE_OK) return _rc; \
   } while (0)
 
+#define MOE_TRY_NEG(expr)           \
+  do {                              \
+    int _rc = (expr);               \
+    if (_rc != MOE_OK) return -_rc; \
+  } while (0)
+
 }  // namespace
 
 extern "C" {
@@ -112,6 +118,13 @@ int moe_prepack_w4(const uint8_t* codes, const uint8_t* scales, int32_t E, int32
 size_t moe_workspace_bytes(moe_dims d) {
   if (check_dims(d) != MOE_OK) return 0;
   return layout_of(d).total;
+}
+
+int moe_layer_kernel_launches(moe_dims d) {
+  MOE_TRY_NEG(check_dims(d));
+  if (d.T == 0) return 0;
+  const bool gemm_gathers = moe::gemm_gathers_rows(d.T * d.k, d.E, d.H);
+  return moe::route_group_launches(d.T, d.E, d.k) + (gemm_gathers ? 0 : 1) + 3;
 }
 
 size_t moe_stage_workspace_bytes(moe_dims d) {
@@ -231,7 +244,9 @@ int layer_forward_impl(const uint16_t* x, const float* logits, moe_w4 w_gate_up,
   MOE_TRY(cuda_status(moe::launch_route_group(logits, d.T, d.E, d.k, ids, wts, counts, offs, sorted, inv,
                                               reinterpret_cast<int32_t*>(w + L.perm), s)));
   MOE_TRY(mark(1));
-  MOE_TRY(cuda_status(moe::launch_gather(x, sorted, d.T * d.k, d.H, xp, s)));
+  // the narrow-tile GEMM gathers the rows of x itself; the wide one reads x_perm
+  const bool gemm_gathers = moe::gemm_gathers_rows(d.T * d.k, d.E, d.H);
+  if (!gemm_gathers) MOE_TRY(cuda_status(moe::launch_gather(x, sorted, d.T * d.k, d.H, xp, s)));
   MOE_TRY(mark(2));
   moe::GemmArgs a{};
   a.offsets = offs;
@@ -240,7 +255,8 @@ int layer_forward_impl(const uint16_t* x, const float* logits, moe_w4 w_gate_up,
   a.E = d.E;
   a.T = d.T;
   a.k = d.k;
-  a.act = xp;
+  a.act = gemm_gathers ? x : xp;
+  a.gather_rows = gemm_gathers ? sorted : nullptr;
   a.packed = static_cast<const uint8_t*>(w_gate_up.packed);
   a.gscale = w_gate_up.global_scale;
   a.out = h;
@@ -250,6 +266,7 @@ int layer_forward_impl(const uint16_t* x, const float* logits, moe_w4 w_gate_up,
   MOE_TRY(cuda_status(run_gemm(0, a, s)));
   MOE_TRY(mark(3));
   a.act = h;
+  a.gather_rows = nullptr;
   a.packed = static_cast<const uint8_t*>(w_down.packed);
   a.gscale = w_down.global_scale;
   a.out = y;

@@ -13,61 +13,67 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include "device_common.cuh"
 #include "kernels.h"
 
 namespace moe {
 
+// Kernels here read what the kernel before them wrote, after pdl_wait(), so
+// their loads use the coherent path (no ld.global.nc).
+
 // --------------------------------------------------------------- routing
+// Order-preserving map of a logit to an unsigned key: NaN ranks as -inf and
+// -0 as +0 (they compare equal), every real logit maps above 0, and 0 marks
+// an expert that is already chosen or does not exist.
+__device__ __forceinline__ uint32_t logit_key(float v) {
+  if (isnan(v)) v = -INFINITY;
+  if (v == 0.0f) v = 0.0f;
+  const uint32_t u = __float_as_uint(v);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ float key_logit(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
+}
+
 // One warp routes one token.  Lane l holds experts l, l+32, ..., NV per lane
-// (NV * 32 >= E).  k rounds of a warp arg-max with (key desc, index asc)
-// order, key = logit with NaN mapped to -inf.  Gate weights: softmax over the
-// k selected keys, fp32 with expf, summed in slot order.  Lane j < k returns
-// slot j's expert and weight.
+// (NV * 32 >= E).  k rounds of a warp arg-max in (key desc, index asc) order:
+// each lane's best (strict > over ascending experts keeps the lower index),
+// then a warp max of the keys and a warp min of the indices holding it.  Gate
+// weights: softmax over the k selected logits, fp32 with expf, summed in slot
+// order.  Lane j < k returns slot j's expert and weight.
 template <int NV>
 __device__ __forceinline__ void route_token(const float* __restrict__ row, int E, int k, int& out_id, float& out_w) {
   const int lane = threadIdx.x & 31;
-  float key[NV];
-  uint32_t taken = 0;
+  uint32_t key[NV];
 #pragma unroll
   for (int i = 0; i < NV; ++i) {
     const int e = lane + 32 * i;
-    float v = -INFINITY;
-    if (e < E) {
-      v = __ldg(row + e);
-      if (isnan(v)) v = -INFINITY;
-    } else {
-      taken |= 1u << i;  // not a real expert
-    }
-    key[i] = v;
+    key[i] = e < E ? logit_key(row[e]) : 0u;
   }
-  float sel_key = -INFINITY;  // lane j keeps the key of slot j
+  uint32_t sel = 0;  // lane j keeps slot j's key and expert
   int sel_id = 0;
   for (int j = 0; j < k; ++j) {
-    float bv = -INFINITY;
-    int bi = 0x7FFFFFFF;
+    uint32_t best = 0, bi = 0xFFFFFFFFu;
 #pragma unroll
     for (int i = 0; i < NV; ++i) {
-      const bool ok = !((taken >> i) & 1u);
-      if (ok && (bi == 0x7FFFFFFF || key[i] > bv)) {  // ascending e: strict > keeps the lower index
-        bv = key[i];
-        bi = lane + 32 * i;
+      if (key[i] > best) {
+        best = key[i];
+        bi = (uint32_t)(lane + 32 * i);
       }
     }
+    const uint32_t m = __reduce_max_sync(0xFFFFFFFFu, best);  // > 0: k <= E real experts
+    const uint32_t e_sel = __reduce_min_sync(0xFFFFFFFFu, best == m ? bi : 0xFFFFFFFFu);
+    if ((int)(e_sel & 31u) == lane) {
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-      const float ov = __shfl_xor_sync(0xFFFFFFFFu, bv, off);
-      const int oi = __shfl_xor_sync(0xFFFFFFFFu, bi, off);
-      if (oi != 0x7FFFFFFF && (bi == 0x7FFFFFFF || ov > bv || (ov == bv && oi < bi))) {
-        bv = ov;
-        bi = oi;
-      }
+      for (int i = 0; i < NV; ++i)
+        if (i == (int)(e_sel >> 5)) key[i] = 0u;
     }
-    if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
     if (lane == j) {
-      sel_key = bv;
-      sel_id = bi;
+      sel = m;
+      sel_id = (int)e_sel;
     }
   }
+  const float sel_key = key_logit(sel);
   const float kmax = __shfl_sync(0xFFFFFFFFu, sel_key, 0);
   float z = 0.f;
   if (lane < k) z = (kmax == -INFINITY) ? 1.f : expf(sel_key - kmax);
@@ -85,6 +91,8 @@ __global__ void __launch_bounds__(kRouteWarps * 32) route_topk_kernel(const floa
                                                                        float* __restrict__ wts) {
   const int lane = threadIdx.x & 31;
   const int t = blockIdx.x * kRouteWarps + (threadIdx.x >> 5);
+  pdl_wait();
+  pdl_trigger();
   if (t >= T) return;
   int id;
   float w;
@@ -116,8 +124,10 @@ static int route_nv(int E) {
 cudaError_t launch_route_topk(const float* logits, int T, int E, int k, int32_t* ids, float* w, cudaStream_t s) {
   if (T == 0) return cudaSuccess;
   const int blocks = (T + kRouteWarps - 1) / kRouteWarps;
-  MOE_DISPATCH_NV(route_nv(E), (route_topk_kernel<NV><<<blocks, kRouteWarps * 32, 0, s>>>(logits, T, E, k, ids, w)));
-  return cudaGetLastError();
+  cudaError_t err;
+  MOE_DISPATCH_NV(route_nv(E), err = launch_pdl(route_topk_kernel<NV>, dim3(blocks), dim3(kRouteWarps * 32), 0, s,
+                                                logits, T, E, k, ids, w));
+  return err;
 }
 
 // ------------------------------------------------------------ permutation
@@ -130,40 +140,53 @@ cudaError_t launch_route_topk(const float* logits, int T, int E, int k, int32_t*
 // independent of scheduling.
 constexpr int kPermChunk = 1024;
 
-// Shared memory of the rank table: uint16 [warps][E].
-static size_t rank_table_bytes(int warps, int E) { return (size_t)warps * E * sizeof(uint16_t); }
+// The rank kernels run 32 warps (kPermChunk threads).  Rank table: uint16
+// [E][32], expert-major, so a warp scans one expert's 32 per-warp counts with
+// lane = warp index.
+constexpr int kRankWarps = kPermChunk / 32;
+static size_t rank_table_bytes(int E) { return (size_t)E * kRankWarps * sizeof(uint16_t); }
 
-// Every thread of the block calls this with its pair (valid == false for
-// padding).  `base[e]` is the first sorted row of expert e available to this
-// block.  `tab` is zeroed by the caller (and a __syncthreads follows).
-__device__ __forceinline__ int block_stable_position(int e, bool valid, const int32_t* base, uint16_t* tab, int E) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
+// Phase 1 of the stable rank (every thread of the block, pair e / valid):
+// returns the pair's rank among the lower lanes of its warp with the same
+// expert and records the warp's count of e in tab[e][warp].  `tab` is zero
+// on entry; a __syncthreads must follow before block_rank_scan.
+__device__ __forceinline__ int warp_rank_and_count(int e, bool valid, uint16_t* tab) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int key = valid ? e : -1 - lane;  // padding pairs: unique keys
   const uint32_t peers = __match_any_sync(0xFFFFFFFFu, key);
-  const int rank = __popc(peers & ((1u << lane) - 1u));
-  if (valid && lane == __ffs(peers) - 1) tab[warp * E + e] = (uint16_t)__popc(peers);
-  __syncthreads();
-  for (int ex = threadIdx.x; ex < E; ex += blockDim.x) {  // exclusive prefix over warps, per expert
-    uint16_t run = 0;
-    for (int w = 0; w < nwarps; ++w) {
-      const uint16_t c = tab[w * E + ex];
-      tab[w * E + ex] = run;
-      run = (uint16_t)(run + c);
+  if (valid && lane == __ffs(peers) - 1) tab[e * kRankWarps + warp] = (uint16_t)__popc(peers);
+  return __popc(peers & ((1u << lane) - 1u));
+}
+
+// Phase 2: per expert, the exclusive prefix over warps replaces tab[e][w];
+// cnt[e] (if cnt != nullptr) receives the block's count of e.  Warp w scans
+// experts w, w+32, ...  A __syncthreads must follow.
+__device__ __forceinline__ void block_rank_scan(uint16_t* tab, int32_t* cnt, int E) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  for (int e = warp; e < E; e += kRankWarps) {
+    const uint32_t c = tab[e * kRankWarps + lane];
+    uint32_t incl = c;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, incl, off);
+      if (lane >= off) incl += y;
     }
+    tab[e * kRankWarps + lane] = (uint16_t)(incl - c);
+    if (cnt != nullptr && lane == 31) cnt[e] = (int32_t)incl;
   }
-  __syncthreads();
-  return valid ? base[e] + tab[warp * E + e] + rank : 0;
 }
 
 __global__ void __launch_bounds__(256) perm_hist_kernel(const int32_t* __restrict__ ids, int n, int E,
                                                         int32_t* __restrict__ chunk_counts) {
   extern __shared__ int32_t hist[];
   for (int e = threadIdx.x; e < E; e += blockDim.x) hist[e] = 0;
+  pdl_wait();
+  pdl_trigger();
   __syncthreads();
   const int base = blockIdx.x * kPermChunk;
   for (int i = threadIdx.x; i < kPermChunk; i += blockDim.x) {
     const int g = base + i;
-    if (g < n) atomicAdd(&hist[__ldg(ids + g)], 1);
+    if (g < n) atomicAdd(&hist[ids[g]], 1);
   }
   __syncthreads();
   for (int e = threadIdx.x; e < E; e += blockDim.x) chunk_counts[(size_t)blockIdx.x * E + e] = hist[e];
@@ -200,6 +223,8 @@ __global__ void __launch_bounds__(1024) perm_scan_kernel(int32_t* __restrict__ c
                                                          int32_t* __restrict__ counts, int32_t* __restrict__ offsets) {
   __shared__ int32_t warp_tot[32];
   const int e = threadIdx.x;
+  pdl_wait();
+  pdl_trigger();
   int32_t run = 0;
   if (e < E) {
     for (int b = 0; b < nchunks; ++b) {
@@ -218,8 +243,8 @@ __global__ void __launch_bounds__(1024) perm_scan_kernel(int32_t* __restrict__ c
   }
 }
 
-// Shared memory of the scatter kernels: base[E] int32, then the rank table.
-static size_t scatter_smem_bytes(int warps, int E) { return (size_t)E * sizeof(int32_t) + rank_table_bytes(warps, E); }
+// Shared memory of the scatter kernel: base[E] int32, then the rank table.
+static size_t scatter_smem_bytes(int E) { return (size_t)E * sizeof(int32_t) + rank_table_bytes(E); }
 
 // One block of kPermChunk threads per chunk; thread i owns pair base + i.
 __global__ void __launch_bounds__(kPermChunk) perm_scatter_kernel(const int32_t* __restrict__ ids, int n, int E, int k,
@@ -230,13 +255,20 @@ __global__ void __launch_bounds__(kPermChunk) perm_scatter_kernel(const int32_t*
   int32_t* base = smem_i;
   uint16_t* tab = reinterpret_cast<uint16_t*>(smem_i + E);
   const int g = blockIdx.x * kPermChunk + threadIdx.x;
+  const int warp = threadIdx.x >> 5;
+  for (int x = threadIdx.x; x < E * kRankWarps; x += blockDim.x) tab[x] = 0;
+  pdl_wait();
+  pdl_trigger();
   for (int e = threadIdx.x; e < E; e += blockDim.x) base[e] = chunk_base[(size_t)blockIdx.x * E + e];
-  for (int x = threadIdx.x; x < (int)(blockDim.x >> 5) * E; x += blockDim.x) tab[x] = 0;
   const bool valid = g < n;
-  const int e = valid ? __ldg(ids + g) : 0;
+  const int e = valid ? ids[g] : 0;
   __syncthreads();
-  const int pos = block_stable_position(e, valid, base, tab, E);
+  const int rank = warp_rank_and_count(e, valid, tab);
+  __syncthreads();
+  block_rank_scan(tab, nullptr, E);
+  __syncthreads();
   if (valid) {
+    const int pos = base[e] + tab[e * kRankWarps + warp] + rank;
     sorted_token[pos] = g / k;
     inv_perm[g] = pos;
   }
@@ -244,8 +276,8 @@ __global__ void __launch_bounds__(kPermChunk) perm_scatter_kernel(const int32_t*
 
 // All pairs in one block (T*k <= kPermChunk), routing optionally included:
 // with logits != nullptr the block first routes its T tokens (one warp per
-// token, warps striding), writing ids / weights; then histogram, scan and
-// stable scatter, all in one launch.
+// token, warps striding), writing ids / weights; then per-warp counts, the
+// scans over warps and over experts, and the stable scatter, in one launch.
 template <int NV>
 __global__ void __launch_bounds__(kPermChunk) route_permute_small_kernel(
     const float* __restrict__ logits, int T, int E, int k, int32_t* __restrict__ ids, float* __restrict__ wts,
@@ -256,12 +288,13 @@ __global__ void __launch_bounds__(kPermChunk) route_permute_small_kernel(
   int32_t* s_ids = smem_i + E;                             // [kPermChunk]
   uint16_t* tab = reinterpret_cast<uint16_t*>(smem_i + E + kPermChunk);
   __shared__ int32_t warp_tot[32];
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwarps = blockDim.x >> 5;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int n = T * k;
-  for (int e = tid; e < E; e += blockDim.x) base[e] = 0;
-  for (int x = tid; x < nwarps * E; x += blockDim.x) tab[x] = 0;
+  for (int x = tid; x < E * kRankWarps; x += blockDim.x) tab[x] = 0;
+  pdl_wait();
+  pdl_trigger();
   if (logits != nullptr) {
-    for (int t = warp; t < T; t += nwarps) {
+    for (int t = warp; t < T; t += kRankWarps) {
       int id;
       float w;
       route_token<NV>(logits + (size_t)t * E, E, k, id, w);
@@ -272,12 +305,14 @@ __global__ void __launch_bounds__(kPermChunk) route_permute_small_kernel(
       }
     }
   } else {
-    for (int i = tid; i < n; i += blockDim.x) s_ids[i] = __ldg(ids + i);
+    for (int i = tid; i < n; i += blockDim.x) s_ids[i] = ids[i];
   }
   __syncthreads();
   const bool valid = tid < n;
   const int e = valid ? s_ids[tid] : 0;
-  if (valid) atomicAdd(&base[e], 1);
+  const int rank = warp_rank_and_count(e, valid, tab);
+  __syncthreads();
+  block_rank_scan(tab, base, E);  // base[e] = count of e
   __syncthreads();
   const int32_t c = tid < E ? base[tid] : 0;
   int32_t total;
@@ -289,26 +324,26 @@ __global__ void __launch_bounds__(kPermChunk) route_permute_small_kernel(
     if (tid == E - 1) offsets[E] = excl + c;
   }
   __syncthreads();
-  const int pos = block_stable_position(e, valid, base, tab, E);
   if (valid) {
+    const int pos = base[e] + tab[e * kRankWarps + warp] + rank;
     sorted_token[pos] = tid / k;
     inv_perm[tid] = pos;
   }
 }
 
-static size_t small_smem_bytes(int E) {
-  return (size_t)(E + kPermChunk) * sizeof(int32_t) + rank_table_bytes(kPermChunk / 32, E);
-}
+static size_t small_smem_bytes(int E) { return (size_t)(E + kPermChunk) * sizeof(int32_t) + rank_table_bytes(E); }
 
 // x_perm[p] = x[sorted_token[p]]: one thread per 16-byte vector (H % 8 == 0).
 __global__ void __launch_bounds__(256) perm_gather_kernel(const uint16_t* __restrict__ x,
                                                           const int32_t* __restrict__ sorted_token, long long nvec,
                                                           int vec_per_row, uint16_t* __restrict__ x_perm) {
+  pdl_wait();
+  pdl_trigger();
   for (long long v = (long long)blockIdx.x * blockDim.x + threadIdx.x; v < nvec; v += (long long)gridDim.x * blockDim.x) {
     const long long p = v / vec_per_row;
     const int c = (int)(v - p * vec_per_row);
-    const int t = __ldg(sorted_token + p);
-    reinterpret_cast<uint4*>(x_perm)[v] = __ldg(reinterpret_cast<const uint4*>(x + (size_t)t * vec_per_row * 8) + c);
+    const int t = sorted_token[p];
+    reinterpret_cast<uint4*>(x_perm)[v] = reinterpret_cast<const uint4*>(x + (size_t)t * vec_per_row * 8)[c];
   }
 }
 
@@ -325,8 +360,7 @@ cudaError_t launch_gather(const uint16_t* x, const int32_t* sorted_token, int n,
   const long long nvec = (long long)n * vpr;
   long long blocks = (nvec + 255) / 256;
   if (blocks > 4096) blocks = 4096;
-  perm_gather_kernel<<<(unsigned)blocks, 256, 0, s>>>(x, sorted_token, nvec, vpr, x_perm);
-  return cudaGetLastError();
+  return launch_pdl(perm_gather_kernel, dim3((unsigned)blocks), dim3(256), 0, s, x, sorted_token, nvec, vpr, x_perm);
 }
 
 template <int NV>
@@ -336,24 +370,22 @@ static cudaError_t launch_small(const float* logits, int T, int E, int k, int32_
   auto kern = route_permute_small_kernel<NV>;
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (err != cudaSuccess) return err;
-  kern<<<1, kPermChunk, smem, s>>>(logits, T, E, k, ids, w, counts, offsets, sorted_token, inv_perm);
-  return cudaGetLastError();
+  return launch_pdl(kern, dim3(1), dim3(kPermChunk), smem, s, logits, T, E, k, ids, w, counts, offsets, sorted_token,
+                    inv_perm);
 }
 
 static cudaError_t launch_chunked(const int32_t* ids, int n, int E, int k, int32_t* counts, int32_t* offsets,
                                   int32_t* sorted_token, int32_t* inv_perm, int32_t* scratch, cudaStream_t s) {
   const int nchunks = (n + kPermChunk - 1) / kPermChunk;
-  perm_hist_kernel<<<nchunks, 256, E * sizeof(int32_t), s>>>(ids, n, E, scratch);
-  cudaError_t err = cudaGetLastError();
+  cudaError_t err = launch_pdl(perm_hist_kernel, dim3(nchunks), dim3(256), E * sizeof(int32_t), s, ids, n, E, scratch);
   if (err != cudaSuccess) return err;
-  perm_scan_kernel<<<1, 1024, 0, s>>>(scratch, nchunks, E, counts, offsets);
-  err = cudaGetLastError();
+  err = launch_pdl(perm_scan_kernel, dim3(1), dim3(1024), 0, s, scratch, nchunks, E, counts, offsets);
   if (err != cudaSuccess) return err;
-  const size_t smem = scatter_smem_bytes(kPermChunk / 32, E);
+  const size_t smem = scatter_smem_bytes(E);
   err = cudaFuncSetAttribute(perm_scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (err != cudaSuccess) return err;
-  perm_scatter_kernel<<<nchunks, kPermChunk, smem, s>>>(ids, n, E, k, scratch, sorted_token, inv_perm);
-  return cudaGetLastError();
+  return launch_pdl(perm_scatter_kernel, dim3(nchunks), dim3(kPermChunk), smem, s, ids, n, E, k,
+                    (const int32_t*)scratch, sorted_token, inv_perm);
 }
 
 cudaError_t launch_permute(const int32_t* ids, const uint16_t* x, int T, int H, int E, int k, int32_t* counts,
@@ -368,35 +400,61 @@ cudaError_t launch_permute(const int32_t* ids, const uint16_t* x, int T, int H, 
   return launch_gather(x, sorted_token, n, H, x_perm, s);
 }
 
+// Routing runs inside the single grouping block only while the logits are
+// small enough for one SM to read quickly (T*E floats, 128 KiB).
+constexpr long long kFusedRouteLogits = 32768;
+
+int route_group_launches(int T, int E, int k) {
+  const int n = T * k;
+  if (n <= kPermChunk && (long long)T * E <= kFusedRouteLogits) return 1;
+  return n <= kPermChunk ? 2 : 4;
+}
+
 cudaError_t launch_route_group(const float* logits, int T, int E, int k, int32_t* ids, float* w, int32_t* counts,
                                int32_t* offsets, int32_t* sorted_token, int32_t* inv_perm, int32_t* scratch,
                                cudaStream_t s) {
   const int n = T * k;
-  if (n <= kPermChunk) {
-    cudaError_t err;
+  cudaError_t err;
+  if (n <= kPermChunk && (long long)T * E <= kFusedRouteLogits) {
     MOE_DISPATCH_NV(route_nv(E), err = (launch_small<NV>(logits, T, E, k, ids, w, counts, offsets, sorted_token,
                                                          inv_perm, s)));
     return err;
   }
-  const cudaError_t err = launch_route_topk(logits, T, E, k, ids, w, s);
+  err = launch_route_topk(logits, T, E, k, ids, w, s);
   if (err != cudaSuccess) return err;
+  if (n <= kPermChunk)
+    return launch_small<1>(nullptr, T, E, k, ids, nullptr, counts, offsets, sorted_token, inv_perm, s);
   return launch_chunked(ids, n, E, k, counts, offsets, sorted_token, inv_perm, scratch, s);
 }
 
 // ------------------------------------------------------------------ combine
 // out[t, c] = bf16_rne(sum_j w[t,j] * y[inv[t*k+j], c]) with the fp32 sum in
-// ascending j.  One thread per 4 consecutive columns.
-__global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ y, const int32_t* __restrict__ inv,
-                                                      const float* __restrict__ w, int T, int H, int k,
-                                                      uint16_t* __restrict__ out) {
+// ascending j.  A block of kCombineThreads takes 4 * kCombineThreads columns
+// of one token; the token's k rows and weights are staged in shared memory
+// first so the k row loads of a thread are independent of each other.
+constexpr int kCombineThreads = 128;
+
+__global__ void __launch_bounds__(kCombineThreads) combine_kernel(const float* __restrict__ y,
+                                                                  const int32_t* __restrict__ inv,
+                                                                  const float* __restrict__ w, int T, int H, int k,
+                                                                  uint16_t* __restrict__ out) {
+  __shared__ int32_t s_row[32];
+  __shared__ float s_w[32];
   const int t = blockIdx.y;
   const int c4 = blockIdx.x * blockDim.x + threadIdx.x;
+  pdl_wait();
+  pdl_trigger();
+  if (threadIdx.x < k) {
+    s_row[threadIdx.x] = inv[(size_t)t * k + threadIdx.x];
+    s_w[threadIdx.x] = w[(size_t)t * k + threadIdx.x];
+  }
+  __syncthreads();
   if (c4 * 4 >= H) return;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 8
   for (int j = 0; j < k; ++j) {
-    const int p = __ldg(inv + (size_t)t * k + j);
-    const float wj = __ldg(w + (size_t)t * k + j);
-    const float4 v = __ldg(reinterpret_cast<const float4*>(y + (size_t)p * H) + c4);
+    const float wj = s_w[j];
+    const float4 v = reinterpret_cast<const float4*>(y + (size_t)s_row[j] * H)[c4];
     acc.x = fmaf(wj, v.x, acc.x);
     acc.y = fmaf(wj, v.y, acc.y);
     acc.z = fmaf(wj, v.z, acc.z);
@@ -413,9 +471,8 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
 cudaError_t launch_combine(const float* y, const int32_t* inv, const float* w, int T, int H, int k, uint16_t* out,
                            cudaStream_t s) {
   if (T == 0) return cudaSuccess;
-  dim3 grid((H / 4 + 255) / 256, T);
-  combine_kernel<<<grid, 256, 0, s>>>(y, inv, w, T, H, k, out);
-  return cudaGetLastError();
+  dim3 grid((H / 4 + kCombineThreads - 1) / kCombineThreads, T);
+  return launch_pdl(combine_kernel, grid, dim3(kCombineThreads), 0, s, y, inv, w, T, H, k, out);
 }
 
 }  // namespace moe

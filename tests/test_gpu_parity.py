@@ -82,10 +82,13 @@ def test_route_parity(name):
 
 
 def test_route_edge_cases():
-    logits = torch.zeros(4, 8)
+    logits = torch.zeros(6, 8)
     logits[1, [2, 5, 6]] = 1.0
     logits[2, 0] = float("nan")
     logits[3, :] = float("nan")
+    logits[4, [0, 3, 4]] = -0.0            # -0 and +0 tie: the lower index goes first
+    logits[5, :] = -float("inf")           # one finite logit among -inf
+    logits[5, 6] = 1.0
     for k in (1, 3, 8):
         ids, w = _route_gpu(logits, k)
         rids, rw = orc.route(logits.numpy(), k)
@@ -255,6 +258,8 @@ def test_layer_host_entry_matches_device_entry():
     (24, 128, 64, 1, 1),     # one expert: dense FFN
     (300, 256, 192, 16, 2),  # several token tiles for hot experts, I not a multiple of 128
     (5, 128, 64, 1024, 32),  # maximum E and k
+    (40, 256, 256, 64, 4),   # 16-row tiles in both projections, rows gathered by the GEMM
+    (96, 512, 256, 64, 8),   # 32-row tiles
 ])
 def test_layer_edge_shapes(T, H, I, E, k):
     d = wk.generate_dims(T, H, I, E, k, seed=T * 7 + E)
@@ -268,6 +273,7 @@ def test_layer_edge_shapes(T, H, I, E, k):
 
 @pytest.mark.parametrize("T,E,k", [
     (1, 4, 1), (33, 1024, 31), (128, 8, 8),   # one fused routing + grouping block (T*k <= 1024)
+    (64, 1024, 4),                            # T*E too large to route inside the grouping block
     (129, 8, 8), (300, 96, 5),                # routing, then histogram / scan / scatter
 ])
 def test_layer_routing_and_grouping_outputs(T, E, k):
@@ -291,6 +297,18 @@ def test_layer_routing_and_grouping_outputs(T, E, k):
     rows = np.arange(min(T, 16), dtype=np.int32)
     ref = orc.layer_rows(bits(d["x"]), rids, rw, gu, dn, rows)
     check_layer(bits(out)[rows], ref, f"T{T} E{E} k{k}")
+
+
+@pytest.mark.parametrize("T,H,I,E,k", [(64, 256, 256, 32, 4), (48, 512, 512, 32, 8)])
+def test_layer_skewed_narrow_tiles(T, H, I, E, k):
+    # zipf-biased routing: hot experts span several narrow token tiles, cold ones none
+    d = wk.generate_dims(T, H, I, E, k, seed=5 * T + E, router="zipf")
+    gu, dn = numpy_weights(d)
+    layer = MoELayer(d["gu"], d["dn"], H, I, E, k, T, DEV)
+    out = layer.forward(d["x"].to(DEV), d["logits"].to(DEV))
+    assert layer.device_status() == _lib.MOE_OK
+    ref, _, _ = orc.layer(bits(d["x"]), d["logits"].numpy(), gu, dn, k)
+    check_layer(bits(out), ref, f"zipf T{T} H{H} I{I} E{E} k{k}")
 
 
 def test_layer_zero_tokens():
