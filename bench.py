@@ -453,9 +453,9 @@ def run_ours(args, wl, dist, rank, world, local_rank):
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": wl.T * wl.H * 2 + wl.T * wl.E * 4,
                 "d2h_bytes_per_step": wl.T * wl.H * 2},
         "cpu_baseline": cpu,
-        # routing + grouping (one fused block when T*k <= 1024, else route / histogram /
-        # scan / scatter) + row gather + gate_up + down + combine
-        "gpu_launches": ((1 if n <= 1024 else 4) + 1 + 1 + 1 + 1) * args.steps,
+        # the library's own kernels per step (routing + grouping, row gather unless the
+        # GEMM gathers, gate_up, down, combine) times the timed steps
+        "gpu_launches": _lib.moe_layer_kernel_launches(dims) * args.steps,
         "clocks": clk,
     }
     print(json.dumps(line), flush=True)
