@@ -264,16 +264,16 @@ def run_reference(args, wl, dist, rank, world):
 # ------------------------------------------------------------------ ours
 def _kernel_hash() -> str:
     h = hashlib.sha256()
-    for f in ("gemm_w4a16.cu", "device_common.cuh"):
+    for f in ("gemm_w4a16.cu", "gemm_common.cuh", "device_common.cuh"):
         with open(os.path.join(ROOT, "moe_layer_bit_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
 
 
 def _traffic_from_profile(wl):
-    """Per-launch DRAM bytes of the gate_up kernel from the committed ncu summary, or None if the
-    summary is missing or was taken on a different kernel source."""
-    p = os.path.join(ROOT, "profiles", f"gate_up_{wl.name}.txt")
+    """Per-launch DRAM bytes of the dominant GEMM launch from the committed ncu summary, or None
+    if the summary is missing or was taken on a different kernel source."""
+    p = os.path.join(ROOT, "profiles", f"gemm_{wl.name}.txt")
     if not os.path.exists(p):
         return None
     kv = {}
@@ -383,11 +383,16 @@ def run_ours(args, wl, dist, rank, world, local_rank):
     counts = np.bincount(ids.cpu().numpy().reshape(-1), minlength=wl.E)
     touched = int(np.count_nonzero(counts))
     n = wl.T * wl.k
+    # the dominant kernel: gate_up + SwiGLU, or both projections when the layer runs
+    # them as one launch (then stage 2 spans that launch and stage 3 is empty)
+    fused = _lib.moe_layer_projections_fused(dims)
     gu_bytes = touched * (2 * wl.I * wl.H * 9 // 16 + 4) + n * wl.H * 2 + n * wl.I * 2
+    if fused:
+        gu_bytes += touched * (wl.H * wl.I * 9 // 16 + 4) + n * wl.I * 2 + n * wl.H * 4
     gu_ms = float(stage_ms[:, 2].mean())
     hbm_peak, tf_peak, tf_sus, peak_kind = _peaks()
     achieved = gu_bytes / (gu_ms * 1e-3) / 1e9
-    gu_flops = 2 * n * (2 * wl.I) * wl.H
+    gu_flops = 2 * n * (3 if fused else 2) * wl.I * wl.H
     achieved_tf = gu_flops / (gu_ms * 1e-3) / 1e12
     # the bound is whichever roof the kernel is closer to: HBM for decode-sized
     # batches, the bf16 tensor pipe for prefill-sized ones
@@ -399,7 +404,8 @@ def run_ours(args, wl, dist, rank, world, local_rank):
         roofline = {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
                     "frac": achieved / hbm_peak, "peak_kind": f"{peak_kind} burst copy bandwidth",
                     "algorithmic_bytes_per_launch": gu_bytes}
-    roofline.update({"kernel": "w4a16_gemm_kernel (gate_up + SwiGLU)", "traffic": _traffic_from_profile(wl),
+    roofline.update({"kernel": "w4a16_gemm_kernel (gate_up + SwiGLU" + (", then down, one launch)" if fused else ")"),
+                     "traffic": _traffic_from_profile(wl),
                      "launch_ms": gu_ms,
                      "other_roof_frac": (achieved / hbm_peak) if roofline["bound"] == "tensor"
                      else (achieved_tf / tf_peak)})

@@ -119,6 +119,11 @@ size_t moe_workspace_bytes(moe_dims d);
  * its stream (0 for T == 0); minus a moe_status code if d is invalid.  Host
  * only: touches no device. */
 int moe_layer_kernel_launches(moe_dims d);
+
+/* 1 if moe_layer_forward runs gate_up + SwiGLU and down as ONE kernel launch
+ * for these dims (narrow token tiles: decode-sized batches), 0 if as two;
+ * minus a moe_status code if d is invalid.  Host only. */
+int moe_layer_projections_fused(moe_dims d);
 size_t moe_stage_workspace_bytes(moe_dims d);
 
 /* [Atlas] "KV Cache量化…" (gate logits -> expert IDs), [ATOM] 8.1 (top-k).
@@ -196,7 +201,9 @@ int moe_layer_forward(const uint16_t *x, const float *logits, moe_w4 w_gate_up, 
  * cudaEvent_t handles (created by the caller; any entry may be NULL).
  * stage_events[i] is recorded on `stream` just before stage i (0 routing and
  * grouping: top-k ids and weights, counts, offsets, sorted_token, inv_perm;
- * 1 the row gather into x_perm; 2 gate_up+SwiGLU, 3 down, 4 combine) and
+ * 1 the row gather into x_perm, empty when the GEMM gathers rows itself;
+ * 2 gate_up+SwiGLU, 3 down, 4 combine; when moe_layer_projections_fused(d),
+ * stage 2 spans the one launch of both projections and stage 3 is empty) and
  * stage_events[5] after
  * the last, so cudaEventElapsedTime(ev[2], ev[3]) is the gate_up launch.
  * Same results and launches as moe_layer_forward. */

@@ -53,6 +53,7 @@ _SIGS = {
     "moe_prepack_w4": (INT, [P, P, I32, I32, I32, I32, P, P]),
     "moe_workspace_bytes": (SZ, [Dims]),
     "moe_layer_kernel_launches": (ctypes.c_int, [Dims]),
+    "moe_layer_projections_fused": (ctypes.c_int, [Dims]),
     "moe_stage_workspace_bytes": (SZ, [Dims]),
     "moe_route_topk": (INT, [P, Dims, P, P, P]),
     "moe_permute": (INT, [P, P, Dims, P, P, P, P, P, P, SZ, P]),
@@ -139,6 +140,13 @@ def moe_workspace_bytes(d: Dims) -> int:
 
 def moe_layer_kernel_launches(d: Dims) -> int:
     return int(load().moe_layer_kernel_launches(d))
+
+
+def moe_layer_projections_fused(d: Dims) -> bool:
+    r = int(load().moe_layer_projections_fused(d))
+    if r < 0:
+        raise MoeError(-r, "moe_layer_projections_fused")
+    return r == 1
 
 
 def moe_stage_workspace_bytes(d: Dims) -> int:

@@ -114,6 +114,41 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
   }
 }
 
+// One acquire load: has the GPU-scope counter reached `target`?
+__device__ __forceinline__ bool counter_reached(const int* ctr, int target) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(ctr) : "memory");
+  return v >= target;
+}
+// Bounded wait until the GPU-scope counter *ctr reaches `target`, polled with
+// acquire loads (so this thread's later reads see what the writers published
+// before their release increments) and a short sleep between polls.  Same
+// abort / timeout behaviour as mbar_wait.
+__device__ __forceinline__ bool wait_counter(const int* ctr, int target, volatile int* abort_flag, int* status,
+                                             unsigned long long limit_ns = kWaitTimeoutNs) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(ctr) : "memory");
+  if (v >= target) return true;
+  const unsigned long long t0 = globaltimer_ns();
+#pragma unroll 1
+  for (uint32_t n = 1;; ++n) {
+    __nanosleep(128);
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(ctr) : "memory");
+    if (v >= target) return true;
+    if ((n & 15u) != 0) continue;
+    if (abort_flag != nullptr && *abort_flag) return false;
+    if (globaltimer_ns() - t0 > limit_ns) {
+      if (abort_flag != nullptr) *abort_flag = 1;
+      if (status != nullptr) atomicExch(status, kStatusDeviceTimeout);
+      return false;
+    }
+  }
+}
+// Adds v to a GPU-scope counter with release semantics.
+__device__ __forceinline__ void counter_add_release(int* ctr, int v) {
+  asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(ctr), "r"(v) : "memory");
+}
+
 // ----------------------------------------------------------- bulk / TMA copy
 __device__ __forceinline__ void bulk_copy_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
   asm volatile(

@@ -13,17 +13,20 @@ struct TileCoord {
   int e, mt, nt;
 };
 
-// Largest e with prefix[e] <= t (experts with no tiles have prefix[e] == prefix[e+1]).
-__device__ __forceinline__ TileCoord decode_tile(int t, const int32_t* prefix, const int32_t* offs, int E, int BN) {
+// Tile t of a projection with MT weight tiles per expert: expert e owns tiles
+// tprefix[e] * MT .. tprefix[e+1] * MT - 1, where tprefix is the prefix sum of
+// the experts' token-tile counts (experts without tokens own none); inside
+// them the token tile varies fastest, so the token tiles of one weight tile
+// are adjacent.
+__device__ __forceinline__ TileCoord decode_tile(int t, const int32_t* tprefix, int E, int MT) {
   int lo = 0, hi = E;
   while (hi - lo > 1) {
     const int mid = (lo + hi) >> 1;
-    if (prefix[mid] <= t) lo = mid;
+    if (tprefix[mid] * MT <= t) lo = mid;
     else hi = mid;
   }
-  const int cnt = offs[lo + 1] - offs[lo];
-  const int nt_count = (cnt + BN - 1) / BN;
-  const int local = t - prefix[lo];
+  const int nt_count = tprefix[lo + 1] - tprefix[lo];
+  const int local = t - tprefix[lo] * MT;
   TileCoord c;
   c.e = lo;
   c.mt = local / nt_count;
@@ -61,13 +64,12 @@ __device__ __forceinline__ void dequant_block(const BlockCodes& b, uint32_t (&v)
   dequant_word(b.c1.w, s3, v + 28);
 }
 
-// Tile list of a grouped GEMM, built in shared memory by the whole CTA:
-// s_off[0..E] = the expert offsets, s_prefix[e] = the first tile of expert e
-// (expert e has ceil(count_e / BN) token tiles times MT weight tiles) and
-// s_prefix[E] = *total = the number of tiles.  Every thread calls it; it ends
-// with the table visible to all.
-__device__ __forceinline__ void build_tile_table(const int32_t* offsets, int E, int BN, int MT, int32_t* s_off,
-                                                 int32_t* s_prefix, volatile uint32_t* total) {
+// Token-tile table of a grouped GEMM, built in shared memory by the whole
+// CTA: s_off[0..E] = the expert offsets, s_tprefix[e] = the token tiles
+// (ceil(count / BN)) of experts before e, s_tprefix[E] = *ntok = all token
+// tiles.  Every thread calls it; it ends with the table visible to all.
+__device__ __forceinline__ void build_tile_table(const int32_t* offsets, int E, int BN, int32_t* s_off,
+                                                 int32_t* s_tprefix, volatile uint32_t* ntok) {
   for (int i = threadIdx.x; i <= E; i += blockDim.x) s_off[i] = offsets[i];
   __syncthreads();
   if (threadIdx.x < 32) {
@@ -75,7 +77,7 @@ __device__ __forceinline__ void build_tile_table(const int32_t* offsets, int E, 
     const int per = (E + 31) / 32;
     const int e0 = lane * per;
     int sum = 0;
-    for (int e = e0; e < e0 + per && e < E; ++e) sum += ((s_off[e + 1] - s_off[e] + BN - 1) / BN) * MT;
+    for (int e = e0; e < e0 + per && e < E; ++e) sum += (s_off[e + 1] - s_off[e] + BN - 1) / BN;
     int incl = sum;
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {
@@ -84,12 +86,12 @@ __device__ __forceinline__ void build_tile_table(const int32_t* offsets, int E, 
     }
     int run = incl - sum;
     for (int e = e0; e < e0 + per && e < E; ++e) {
-      s_prefix[e] = run;
-      run += ((s_off[e + 1] - s_off[e] + BN - 1) / BN) * MT;
+      s_tprefix[e] = run;
+      run += (s_off[e + 1] - s_off[e] + BN - 1) / BN;
     }
     if (lane == 31) {
-      s_prefix[E] = incl;
-      *total = (uint32_t)incl;
+      s_tprefix[E] = incl;
+      *ntok = (uint32_t)incl;
     }
   }
   __syncthreads();

@@ -30,9 +30,15 @@
 //    MMA's A operand (tcgen05.st), so no dequantised weight touches shared
 //    memory; one MMA warp (operands warp-uniform, one elected lane issuing)
 //    runs tcgen05.mma with A from TMEM, B from shared memory and an fp32
-//    accumulator in TMEM, double-buffered across tiles; four epilogue warps
+//    accumulator in TMEM, a ring of 2 (wide tiles) or 4 (narrow) across tiles; four epilogue warps
 //    read the accumulator (tcgen05.ld), apply global_scale * 2^7 and write
 //    SwiGLU(bf16) or fp32 rows;
+//  * one launch can run both projections of the layer (narrow token tiles):
+//    the schedule is the gate_up tiles, then the down tiles, the weight
+//    stream runs on without a break, and a down tile's activation loads wait
+//    (per expert, on a GPU-scope counter the gate_up epilogues publish with
+//    release semantics) until that expert's h rows are written; the launch is
+//    cooperative, so all CTAs are resident and the waits cannot deadlock;
 //  * every barrier wait is bounded (about 1 s); on expiry the CTA records a
 //    timeout in the status word, drains its copies and MMAs and exits.
 #include <cstdint>
@@ -62,13 +68,17 @@ constexpr int kBInFlight = 2;  // activation stages a gathering producer lane ke
 // Token-tile width BN and SB K blocks per stage: shared-memory rings of NSW
 // weight stages (SB packed blocks) and NSB activation stages (SB sub-tiles),
 // and a TMEM ring of NA A-operand slots of 32*SB columns (128 rows x 64*SB
-// bf16) placed after the two BN-column accumulators.
+// bf16) placed after the ND accumulators of BN columns.
 template <int BN, int SB>
 struct Cfg {
   static constexpr int kBSub = BN * 128;  // BN rows x 64 bf16, 128-byte swizzled
   static constexpr int kBTile = SB * kBSub;
   static constexpr int kWBytes = SB * kWBlockBytes;
-  static constexpr int A0 = (2 * BN < 32) ? 32 : 2 * BN;
+  // ND fp32 accumulators of BN columns (tiles round-robin), so the MMA warp
+  // runs ND - 1 tiles ahead of the epilogue: 4 for narrow tiles, whose tiles
+  // are short (a down tile of a decode step is 3 stages), where TMEM has room.
+  static constexpr int ND = BN <= 32 ? 4 : 2;
+  static constexpr int A0 = (ND * BN < 32) ? 32 : ND * BN;
   static constexpr int kSlotCols = 32 * SB;
   static constexpr int NA = (int)(kTmemCols - A0) / kSlotCols;
   // A stage's SB blocks are split over kSplit warps per TMEM lane quadrant,
@@ -105,8 +115,8 @@ struct Cfg {
   static constexpr int kOffW = NSB * kBTile;
   static constexpr int kOffBar = kOffW + NSW * kWBytes;
   // fullw[NSW], emptyw[NSW], fullb[NSB], emptyb[NSB], afull[NA], aempty[NA],
-  // dfull[2], dempty[2], drain
-  static constexpr int kNumBars = 2 * NSW + 2 * NSB + 2 * NA + 5;
+  // dfull[ND], dempty[ND], drain
+  static constexpr int kNumBars = 2 * NSW + 2 * NSB + 2 * NA + 2 * ND + 1;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;  // [0] tmem base, [1] abort, [2] total tiles
   static constexpr int kOffTables = kOffMisc + 16;         // offsets[E+1], prefix[E+1]
   static_assert(NA >= 1, "TMEM ring needs a slot");
@@ -117,12 +127,9 @@ struct Cfg {
   }
 };
 
-template <int BN, int SB, int MODE>
+template <int BN, int SB>
 __global__ void __launch_bounds__(kThreads, 1)
-    w4a16_gemm_kernel(const __grid_constant__ CUtensorMap tmap_act, const uint16_t* __restrict__ act,
-                      const int32_t* __restrict__ gather_rows, const uint8_t* __restrict__ packed,
-                      const float* __restrict__ gscale, const int32_t* __restrict__ offsets, void* __restrict__ out,
-                      int* __restrict__ status, int E, int N, int K, int out_ld) {
+    w4a16_gemm_kernel(const __grid_constant__ CUtensorMap tmap_act, const __grid_constant__ GemmLaunch L) {
   using C = Cfg<BN, SB>;
   constexpr int NSW = C::NSW, NSB = C::NSB, NA = C::NA;
   extern __shared__ uint8_t smem_raw[];
@@ -137,21 +144,21 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto emptyb_bar = [&](int s) { return bar0 + 8u * (2 * NSW + NSB + s); };
   auto afull_bar = [&](int a) { return bar0 + 8u * (2 * NSW + 2 * NSB + a); };
   auto aempty_bar = [&](int a) { return bar0 + 8u * (2 * NSW + 2 * NSB + NA + a); };
+  constexpr int ND = C::ND;
   auto dfull_bar = [&](int d) { return bar0 + 8u * (2 * NSW + 2 * NSB + 2 * NA + d); };
-  auto dempty_bar = [&](int d) { return bar0 + 8u * (2 * NSW + 2 * NSB + 2 * NA + 2 + d); };
-  const uint32_t drain_bar = bar0 + 8u * (2 * NSW + 2 * NSB + 2 * NA + 4);
+  auto dempty_bar = [&](int d) { return bar0 + 8u * (2 * NSW + 2 * NSB + 2 * NA + ND + d); };
+  const uint32_t drain_bar = bar0 + 8u * (2 * NSW + 2 * NSB + 2 * NA + 2 * ND);
   volatile uint32_t* misc = reinterpret_cast<volatile uint32_t*>(smem + C::kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 4);
+  const int E = L.E;
   int32_t* s_off = reinterpret_cast<int32_t*>(smem + C::kOffTables);
-  int32_t* s_prefix = s_off + (E + 1);
+  int32_t* s_tprefix = s_off + (E + 1);
+  int* status = L.status;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int MT = N / kTileM;
-  const int KB = K / kBlockK;
-  const int KS = KB / SB;  // stages per tile
 
-  // ---- set-up: barriers, TMEM, tile table
+  // ---- set-up: barriers and TMEM (on-chip only), then the tile table
   if (threadIdx.x == 0) {
     for (int s = 0; s < NSW; ++s) {
       mbar_init(fullw_bar(s), 1);
@@ -165,7 +172,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(afull_bar(a), C::kGroupWarps);
       mbar_init(aempty_bar(a), 1);
     }
-    for (int d = 0; d < 2; ++d) {
+    for (int d = 0; d < ND; ++d) {
       mbar_init(dfull_bar(d), 1);
       mbar_init(dempty_bar(d), 4);
     }
@@ -178,31 +185,52 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_alloc(sbase + C::kOffMisc, kTmemCols);
     tmem_relinquish();
   }
-  // everything above is on-chip; the expert offsets come from the kernel before
+  // everything above is on-chip; the offsets and activations come from the
+  // kernels before
   pdl_wait();
   pdl_trigger();
-  build_tile_table(offsets, E, BN, MT, s_off, s_prefix, misc + 2);
+  build_tile_table(L.offsets, E, BN, s_off, s_tprefix, misc + 2);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = misc[0];
-  const int total = (int)misc[2];
-  const int my_tiles = total > (int)blockIdx.x ? (total - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x : 0;
-  const int my_stages = my_tiles * KS;
+
+  // The CTA's schedule: tiles u = blockIdx.x, + gridDim.x, ... of the
+  // concatenated tile lists of the phases (phase 0, then phase 1).
+  const int ntok = (int)misc[2];
+  const int MT0 = L.ph[0].N / kTileM;
+  const int MT1 = L.nph > 1 ? L.ph[1].N / kTileM : 0;
+  const int T0 = ntok * MT0;
+  const int total = T0 + ntok * MT1;
+  const int KS0 = L.ph[0].K / (kBlockK * SB);
+  const int KS1 = L.nph > 1 ? L.ph[1].K / (kBlockK * SB) : 0;
+  struct TileRef {
+    int ph;  // phase
+    TileCoord c;
+  };
+  auto tile_of = [&](int u) {
+    TileRef r;
+    r.ph = u < T0 ? 0 : 1;
+    r.c = decode_tile(r.ph == 0 ? u : u - T0, s_tprefix, E, r.ph == 0 ? MT0 : MT1);
+    return r;
+  };
 
   if (warp == kWarpProducer || (warp == kWarpProducerB && !C::kGatherB)) {
     // ----------------------------------------------------------- producers
-    // One warp streams the packed weight blocks, the other (wide token
-    // tiles) the permuted activation tiles by TMA; each walks the schedule with
-    // uniform values and one elected lane issues the copies.
+    // One warp streams the packed weight blocks (phase after phase, with no
+    // break in between), the other (wide token tiles, one phase) the permuted
+    // activation tiles by TMA; each walks the schedule with uniform values and
+    // one elected lane issues the copies.
     const bool is_w = warp == kWarpProducer;
     const int ring = is_w ? NSW : NSB;
     int i = 0;
     bool ok = true;
-    for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-      const TileCoord c = decode_tile(t, s_prefix, s_off, E, BN);
-      const uint8_t* wsrc = packed + (size_t)(c.e * MT + c.mt) * KB * kWBlockBytes;
-      const int row0 = s_off[c.e] + c.nt * BN;
+    for (int u = blockIdx.x; u < total && ok; u += gridDim.x) {
+      const TileRef tr = tile_of(u);
+      const GemmPhase& P = L.ph[tr.ph];
+      const int MT = tr.ph == 0 ? MT0 : MT1, KS = tr.ph == 0 ? KS0 : KS1;
+      const uint8_t* wsrc = P.packed + (size_t)(tr.c.e * MT + tr.c.mt) * KS * SB * kWBlockBytes;
+      const int row0 = s_off[tr.c.e] + tr.c.nt * BN;
       for (int ks = 0; ks < KS; ++ks, ++i) {
         const int s = i % ring;
         const uint32_t ph = (uint32_t)(i / ring) & 1u;
@@ -234,25 +262,51 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Lane -> (row r, 16-byte chunks c0 .. c0 + kChunks - 1 of every 64-column
     // block); chunk c of row r lands at r * 128 + ((c ^ (r & 7)) * 16), the
     // 128-byte swizzle the MMA's shared-memory descriptor expects.  Rows past
-    // the expert's last token are zero-filled, not read.
+    // the expert's last token are zero-filled, not read.  A phase-1 tile of
+    // expert e first waits until every phase-0 tile of e has written its rows.
     constexpr int kChunks = BN == 16 ? 4 : 8;
     const int r = BN == 16 ? (lane & 15) : lane;
     const int c0 = BN == 16 ? (lane >> 4) * 4 : 0;
     uint32_t dst_off[kChunks];
 #pragma unroll
     for (int j = 0; j < kChunks; ++j) dst_off[j] = (uint32_t)(r * 128 + (((c0 + j) ^ (r & 7)) * 16));
-    int i = 0;
+    // Stages [released, issued) are copied or in flight but not yet handed to
+    // the MMA warp; a stage is handed over once at most kBInFlight newer ones
+    // are pending, or all at once before a wait on another CTA (so this CTA's
+    // own phase-0 tiles never wait behind that wait).
+    int issued = 0, released = 0;
+    auto release_all = [&]() {
+      cp_async_wait_group<0>();
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0)
+        for (int j = released; j < issued; ++j) mbar_arrive(fullb_bar(j % NSB));
+      released = issued;
+    };
     bool ok = true;
-    for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-      const TileCoord c = decode_tile(t, s_prefix, s_off, E, BN);
-      const int p0 = s_off[c.e] + c.nt * BN;
-      const bool valid = r < s_off[c.e + 1] - p0;
-      const size_t src_row = valid ? (size_t)(gather_rows != nullptr ? gather_rows[p0 + r] : p0 + r) : 0;
-      const uint16_t* rowp = act + src_row * (size_t)K + c0 * 8;
+    for (int u = blockIdx.x; u < total && ok; u += gridDim.x) {
+      const TileRef tr = tile_of(u);
+      const GemmPhase& P = L.ph[tr.ph];
+      const int KS = tr.ph == 0 ? KS0 : KS1;
+      const int p0 = s_off[tr.c.e] + tr.c.nt * BN;
+      if (tr.ph == 1) {
+        // this expert's h rows: every phase-0 tile of it, 4 epilogue warps each
+        const int* ctr = L.ready + tr.c.e;
+        const int target = 4 * MT0 * (s_tprefix[tr.c.e + 1] - s_tprefix[tr.c.e]);
+        if (!__all_sync(0xFFFFFFFFu, counter_reached(ctr, target))) {
+          release_all();
+          ok = __all_sync(0xFFFFFFFFu, wait_counter(ctr, target, abort_flag, status));
+          if (!ok) break;
+        }
+      }
+      const bool valid = r < s_off[tr.c.e + 1] - p0;
+      const size_t src_row = valid ? (size_t)(P.gather_rows != nullptr ? P.gather_rows[p0 + r] : p0 + r) : 0;
+      const uint16_t* rowp = P.act + src_row * (size_t)P.K + c0 * 8;
       const uint32_t nbytes = valid ? 16u : 0u;
-      for (int ks = 0; ks < KS; ++ks, ++i) {
-        const int s = i % NSB;
-        if (!__all_sync(0xFFFFFFFFu, mbar_wait(emptyb_bar(s), ((uint32_t)(i / NSB) & 1u) ^ 1u, abort_flag, status))) {
+      for (int ks = 0; ks < KS; ++ks) {
+        const int s = issued % NSB;
+        if (!__all_sync(0xFFFFFFFFu,
+                        mbar_wait(emptyb_bar(s), ((uint32_t)(issued / NSB) & 1u) ^ 1u, abort_flag, status))) {
           ok = false;
           break;
         }
@@ -264,21 +318,23 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int j = 0; j < kChunks; ++j) cp_async16(dst + b * C::kBSub + dst_off[j], src + j * 8, nbytes);
         }
         cp_async_commit();
-        if (i >= kBInFlight) {
-          // stage i - kBInFlight has landed for this lane; after the proxy
+        ++issued;
+        if (issued - released > kBInFlight) {
+          // the oldest pending stage has landed for this lane; after the proxy
           // fence and the warp sync it is complete for the MMA to read
           cp_async_wait_group<kBInFlight>();
           fence_proxy_async_smem();
           __syncwarp();
-          if (lane == 0) mbar_arrive(fullb_bar((i - kBInFlight) % NSB));
+          if (lane == 0) mbar_arrive(fullb_bar(released % NSB));
+          ++released;
         }
       }
     }
-    cp_async_wait_group<0>();
-    fence_proxy_async_smem();
-    __syncwarp();
-    if (ok && lane == 0)
-      for (int j = (i > kBInFlight ? i - kBInFlight : 0); j < i; ++j) mbar_arrive(fullb_bar(j % NSB));
+    if (ok) {
+      release_all();
+    } else {
+      cp_async_wait_group<0>();  // nothing may land after the CTA exits
+    }
   } else if (warp == kWarpMma) {
     // ---------------------------------------------------------- MMA issue
     // The whole warp waits and computes the (uniform) operands; one elected
@@ -286,9 +342,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr uint32_t idesc = idesc_bf16_f32(kTileM, BN);
     int i = 0, it = 0;
     bool ok = true;
-    for (int t = blockIdx.x; t < total && ok; t += gridDim.x, ++it) {
-      const int d = it & 1;
-      if (!__all_sync(0xFFFFFFFFu, mbar_wait(dempty_bar(d), ((uint32_t)(it >> 1) & 1u) ^ 1u, abort_flag, status)))
+    for (int u = blockIdx.x; u < total && ok; u += gridDim.x, ++it) {
+      const int KS = u < T0 ? KS0 : KS1;
+      const int d = it % ND;
+      if (!__all_sync(0xFFFFFFFFu, mbar_wait(dempty_bar(d), ((uint32_t)(it / ND) & 1u) ^ 1u, abort_flag, status)))
         break;
       tc_fence_after();
       const uint32_t d_tmem = tmem_base + (uint32_t)(d * BN);
@@ -333,6 +390,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int part = (dw % C::kGroupWarps) >> 2;
     const int r = 32 * q + lane;
     const uint32_t t_row = tmem_base + ((uint32_t)(32 * q) << 16) + (uint32_t)C::A0;
+    // stages of this CTA: its tiles of phase 0 times KS0, then of phase 1
+    const int n_all = total > (int)blockIdx.x ? (total - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x : 0;
+    const int n0 = T0 > (int)blockIdx.x ? (T0 - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x : 0;
+    const int my_stages = n0 * KS0 + (n_all - n0) * KS1;
 #pragma unroll 1
     for (int i = group; group < G && i < my_stages; i += G) {
       const int s = i % NSW, a = i % NA;
@@ -367,15 +428,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ epilogue
     const int q = warp - kWarpEpi0;
     int it = 0;
-    for (int t = blockIdx.x; t < total; t += gridDim.x, ++it) {
-      const TileCoord c = decode_tile(t, s_prefix, s_off, E, BN);
-      const int d = it & 1;
-      const uint32_t dph = (uint32_t)(it >> 1) & 1u;
+    for (int u = blockIdx.x; u < total; u += gridDim.x, ++it) {
+      const TileRef tr = tile_of(u);
+      const GemmPhase& P = L.ph[tr.ph];
+      const TileCoord c = tr.c;
+      const int d = it % ND;
+      const uint32_t dph = (uint32_t)(it / ND) & 1u;
       if (!__all_sync(0xFFFFFFFFu, mbar_wait(dfull_bar(d), dph, abort_flag, status))) break;
       tc_fence_after();
       const int p0 = s_off[c.e] + c.nt * BN;
       const int nvalid = min(BN, s_off[c.e + 1] - p0);
-      const float gsc = __ldg(gscale + c.e) * 128.0f;
+      const float gsc = __ldg(P.gscale + c.e) * 128.0f;
       const uint32_t t_acc = tmem_base + ((uint32_t)(32 * q) << 16) + (uint32_t)(d * BN);
 #pragma unroll 1
       for (int cc = 0; cc < BN / 16; ++cc) {
@@ -383,11 +446,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld16(t_acc + (uint32_t)(cc * 16), v);
         tc_wait_ld();
         if (cc * 16 >= nvalid) continue;
-        if (MODE == 0) {
+        if (P.mode == 0) {
           // rows 32q..32q+15 hold gate features f, rows 32q+16.. the matching up rows
           const int f = c.mt * 64 + 16 * q + (lane & 15);
           const bool is_gate = lane < 16;
-          uint16_t* h = reinterpret_cast<uint16_t*>(out);
+          uint16_t* h = reinterpret_cast<uint16_t*>(P.out);
 #pragma unroll
           for (int j = 0; j < 8; ++j) {
             const float a = __uint_as_float(v[j]);
@@ -396,26 +459,32 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float recv = __shfl_xor_sync(0xFFFFFFFFu, send, 16);
             const float own = is_gate ? a : b;
             const float g = (is_gate ? own : recv) * gsc;
-            const float u = (is_gate ? recv : own) * gsc;
+            const float up = (is_gate ? recv : own) * gsc;
             const int col = cc * 16 + j + (is_gate ? 0 : 8);
             if (col < nvalid) {
-              const float hv = g / (1.0f + __expf(-g)) * u;
-              h[(size_t)(p0 + col) * out_ld + f] = __bfloat16_as_ushort(__float2bfloat16_rn(hv));
+              const float hv = g / (1.0f + __expf(-g)) * up;
+              h[(size_t)(p0 + col) * P.out_ld + f] = __bfloat16_as_ushort(__float2bfloat16_rn(hv));
             }
           }
         } else {
           const int n = c.mt * kTileM + 32 * q + lane;
-          float* y = reinterpret_cast<float*>(out);
+          float* y = reinterpret_cast<float*>(P.out);
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
             const int col = cc * 16 + j;
-            if (col < nvalid) y[(size_t)(p0 + col) * out_ld + n] = __uint_as_float(v[j]) * gsc;
+            if (col < nvalid) y[(size_t)(p0 + col) * P.out_ld + n] = __uint_as_float(v[j]) * gsc;
           }
         }
       }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(dempty_bar(d));
+      if (tr.ph == 0 && L.nph > 1) {
+        // this warp's rows of h are written: publish them to phase-1 tiles
+        __threadfence();
+        __syncwarp();
+        if (lane == 0) counter_add_release(L.ready + c.e, 1);
+      }
     }
   }
 
@@ -444,40 +513,64 @@ static PFN_encodeTiled get_encode_fn() {
   return fn;
 }
 
-template <int BN, int SB, int MODE>
-static cudaError_t launch_gemm_cfg(const GemmArgs& a, cudaStream_t s) {
+static GemmPhase phase_of(int mode, const GemmArgs& a) {
+  GemmPhase p;
+  p.packed = a.packed;
+  p.gscale = a.gscale;
+  p.out = a.out;
+  p.act = a.act;
+  p.gather_rows = a.gather_rows;
+  p.N = a.N;
+  p.K = a.K;
+  p.out_ld = a.out_ld;
+  p.mode = mode;
+  return p;
+}
+
+// `rows` activation rows (T*k); the phases of L share them and the offsets.
+template <int BN, int SB>
+static cudaError_t launch_gemm_cfg(const GemmLaunch& L, int rows, cudaStream_t s) {
+  using C = Cfg<BN, SB>;
   CUtensorMap tmap;
   memset(&tmap, 0, sizeof(tmap));
-  if (!Cfg<BN, SB>::kGatherB) {
-    if (a.gather_rows != nullptr) return cudaErrorInvalidValue;  // TMA tiles read permuted rows only
+  if (!C::kGatherB) {
+    // TMA tiles read a permuted copy, one phase per launch
+    if (L.nph != 1 || L.ph[0].gather_rows != nullptr) return cudaErrorInvalidValue;
     PFN_encodeTiled enc = get_encode_fn();
     if (enc == nullptr) return cudaErrorNotSupported;
-    const cuuint64_t gdim[2] = {(cuuint64_t)a.K, (cuuint64_t)a.rows};
-    const cuuint64_t gstride[1] = {(cuuint64_t)a.K * 2};
+    const cuuint64_t gdim[2] = {(cuuint64_t)L.ph[0].K, (cuuint64_t)rows};
+    const cuuint64_t gstride[1] = {(cuuint64_t)L.ph[0].K * 2};
     const cuuint32_t box[2] = {(cuuint32_t)kBlockK, (cuuint32_t)BN};
     const cuuint32_t estride[2] = {1, 1};
-    CUresult r = enc(&tmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(a.act), gdim, gstride, box,
+    CUresult r = enc(&tmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(L.ph[0].act), gdim, gstride, box,
                      estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
   }
-
   int dev = 0, sms = 0;
   cudaError_t err = cudaGetDevice(&dev);
   if (err != cudaSuccess) return err;
   err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (err != cudaSuccess) return err;
-  const int MT = a.N / kTileM;
-  const long long n = a.rows;
-  const long long max_tiles = (long long)MT * (n / BN + (n < a.E ? n : a.E));
-  int grid = (int)(max_tiles < sms ? max_tiles : sms);
+  const long long n = rows;
+  long long max_tiles = 0;
+  for (int p = 0; p < L.nph; ++p) max_tiles += (long long)(L.ph[p].N / kTileM) * (n / BN + (n < L.E ? n : L.E));
+  const int grid = (int)(max_tiles < sms ? max_tiles : sms);
   if (grid <= 0) return cudaSuccess;
-  const int smem = Cfg<BN, SB>::bytes(a.E);
-  auto kern = w4a16_gemm_kernel<BN, SB, MODE>;
+  const int smem = C::bytes(L.E);
+  auto kern = w4a16_gemm_kernel<BN, SB>;
   err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (err != cudaSuccess) return err;
-  return launch_pdl(kern, dim3(grid), dim3(kThreads), smem, s, tmap, a.act, a.gather_rows, a.packed, a.gscale,
-                    a.offsets, a.out, a.status, a.E, a.N, a.K, a.out_ld);
+  // Two phases: phase-1 CTAs wait on phase-0 tiles of other CTAs, so all CTAs
+  // must be resident together (one per SM, grid <= SMs): a cooperative launch.
+  const bool coop = L.nph > 1;
+  err = launch_ex(kern, dim3(grid), dim3(kThreads), smem, s, true, coop, tmap, L);
+  if (err != cudaSuccess && coop) {
+    // without the programmatic overlap if the driver does not combine the two
+    (void)cudaGetLastError();
+    err = launch_ex(kern, dim3(grid), dim3(kThreads), smem, s, false, true, tmap, L);
+  }
+  return err;
 }
 
 // Token tile width: the smallest of 16/32/64/128 that covers about twice the
@@ -493,35 +586,67 @@ static int pick_bn(int rows, int E) {
 
 // K blocks per stage: 4 for the narrowest token tile (decode: amortise the MMA
 // warp's per-stage cost), 2 otherwise (keeps enough TMEM A slots next to the
-// 2 x BN accumulator columns and a deep enough shared-memory ring), 1 when K/64
-// is not a multiple.
-template <int BN, int MODE>
-static cudaError_t launch_gemm_bn(const GemmArgs& a, cudaStream_t s) {
-  constexpr int kWide = (BN <= 16) ? 4 : 2;
-  const int KB = a.K / kBlockK;
-  if (KB % kWide == 0) return launch_gemm_cfg<BN, kWide, MODE>(a, s);
-  return launch_gemm_cfg<BN, 1, MODE>(a, s);
+// 2 x BN accumulator columns and a deep enough shared-memory ring), fewer when
+// a phase's K/64 is not a multiple.
+static int pick_sb(int bn, const int* kb, int nph) {
+  int sb = bn <= 16 ? 4 : 2;
+  for (;;) {
+    bool ok = true;
+    for (int p = 0; p < nph; ++p) ok = ok && kb[p] % sb == 0;
+    if (ok || sb == 1) return sb;
+    sb >>= 1;
+  }
+}
+
+template <int BN>
+static cudaError_t launch_gemm_bn(const GemmLaunch& L, int rows, cudaStream_t s) {
+  int kb[2];
+  for (int p = 0; p < L.nph; ++p) kb[p] = L.ph[p].K / kBlockK;
+  switch (pick_sb(BN, kb, L.nph)) {
+    case 4: return launch_gemm_cfg<BN, (BN <= 16 ? 4 : 2)>(L, rows, s);
+    case 2: return launch_gemm_cfg<BN, 2>(L, rows, s);
+    default: return launch_gemm_cfg<BN, 1>(L, rows, s);
+  }
+}
+
+static cudaError_t launch_gemm_any(const GemmLaunch& L, int rows, cudaStream_t s) {
+  switch (pick_bn(rows, L.E)) {
+    case 16: return launch_gemm_bn<16>(L, rows, s);
+    case 32: return launch_gemm_bn<32>(L, rows, s);
+    case 64: return launch_gemm_bn<64>(L, rows, s);
+    default: return launch_gemm_bn<128>(L, rows, s);
+  }
 }
 
 bool gemm_gathers_rows(int rows, int E, int /*K*/) { return pick_bn(rows, E) <= 32; }
 
+bool gemm_fuses_layer(int rows, int E, int /*H*/, int /*I*/) { return rows > 0 && pick_bn(rows, E) <= 32; }
+
 cudaError_t launch_gemm(int mode, const GemmArgs& a, cudaStream_t s) {
   if (a.rows == 0) return cudaSuccess;
-  const int bn = pick_bn(a.rows, a.E);
-  if (mode == 0) {
-    switch (bn) {
-      case 16: return launch_gemm_bn<16, 0>(a, s);
-      case 32: return launch_gemm_bn<32, 0>(a, s);
-      case 64: return launch_gemm_bn<64, 0>(a, s);
-      default: return launch_gemm_bn<128, 0>(a, s);
-    }
-  }
-  switch (bn) {
-    case 16: return launch_gemm_bn<16, 1>(a, s);
-    case 32: return launch_gemm_bn<32, 1>(a, s);
-    case 64: return launch_gemm_bn<64, 1>(a, s);
-    default: return launch_gemm_bn<128, 1>(a, s);
-  }
+  GemmLaunch L;
+  memset(&L, 0, sizeof(L));
+  L.ph[0] = phase_of(mode, a);
+  L.nph = 1;
+  L.offsets = a.offsets;
+  L.status = a.status;
+  L.E = a.E;
+  return launch_gemm_any(L, a.rows, s);
+}
+
+cudaError_t launch_gemm_layer(const GemmArgs& gate_up, const GemmArgs& down, int32_t* ready, cudaStream_t s) {
+  if (gate_up.rows == 0) return cudaSuccess;
+  if (!gemm_fuses_layer(gate_up.rows, gate_up.E, gate_up.K, down.K) || ready == nullptr) return cudaErrorInvalidValue;
+  GemmLaunch L;
+  memset(&L, 0, sizeof(L));
+  L.ph[0] = phase_of(0, gate_up);
+  L.ph[1] = phase_of(1, down);
+  L.nph = 2;
+  L.offsets = gate_up.offsets;
+  L.ready = ready;
+  L.status = gate_up.status;
+  L.E = gate_up.E;
+  return launch_gemm_any(L, gate_up.rows, s);
 }
 
 // ------------------------------------------------------------------ prepack

@@ -10,21 +10,36 @@ namespace moe {
 
 // Launches `kern` with programmatic stream serialization: it may start its
 // on-chip set-up while the previous kernel in `s` finishes (the kernels call
-// pdl_wait() before touching global memory).
+// pdl_wait() before touching global memory).  `cooperative` also asks for all
+// CTAs to be resident at once (kernels whose CTAs wait on one another).
 template <typename... KArgs, typename... Args>
-inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
-                              Args&&... args) {
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
+inline cudaError_t launch_ex(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s, bool pdl,
+                             bool cooperative, Args&&... args) {
+  cudaLaunchAttribute attr[2];
+  int n = 0;
+  if (pdl) {
+    attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[n].val.programmaticStreamSerializationAllowed = 1;
+    ++n;
+  }
+  if (cooperative) {
+    attr[n].id = cudaLaunchAttributeCooperative;
+    attr[n].val.cooperative = 1;
+    ++n;
+  }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = block;
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = n;
   return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                              Args&&... args) {
+  return launch_ex(kern, grid, block, smem, s, true, false, std::forward<Args>(args)...);
 }
 
 // Packed NVFP4 layout: tiles of 128 weight rows x 64 K elements, 4608 bytes each.
@@ -40,12 +55,13 @@ cudaError_t launch_permute(const int32_t* ids, const uint16_t* x, int T, int H, 
                            int32_t* scratch, cudaStream_t s);
 
 // Routing and grouping of the layer: top-k routing, then counts, offsets,
-// sorted_token and inv_perm.  T*k <= 1024 with T*E <= 32768 runs as one
-// single-block launch; otherwise routing, then one grouping block
-// (T*k <= 1024) or histogram + scan + scatter.
+// sorted_token and inv_perm; zero_e (E int32, may be null) is zeroed.
+// T*k <= 1024 with T*E <= 32768 runs as one single-block launch; otherwise
+// routing, then one grouping block (T*k <= 1024) or histogram + scan +
+// scatter.
 cudaError_t launch_route_group(const float* logits, int T, int E, int k, int32_t* ids, float* w, int32_t* counts,
                                int32_t* offsets, int32_t* sorted_token, int32_t* inv_perm, int32_t* scratch,
-                               cudaStream_t s);
+                               int32_t* zero_e, cudaStream_t s);
 // x_perm[p] = x[sorted_token[p]] for p < n.
 cudaError_t launch_gather(const uint16_t* x, const int32_t* sorted_token, int n, int H, uint16_t* x_perm,
                           cudaStream_t s);
@@ -81,6 +97,31 @@ cudaError_t launch_gemm(int mode, const GemmArgs& a, cudaStream_t s);
 // True when launch_gemm picks narrow token tiles (16 or 32 rows) for these
 // sizes; those gather activation rows themselves (GemmArgs::gather_rows).
 bool gemm_gathers_rows(int rows, int E, int K);
+
+// Both projections of the layer in one persistent launch (narrow token tiles
+// only): gate_up + SwiGLU tiles first, then down tiles, whose activation
+// loads wait per expert until that expert's h rows are written.  `ready`:
+// E int32 zeroed before the launch.
+bool gemm_fuses_layer(int rows, int E, int H, int I);
+cudaError_t launch_gemm_layer(const GemmArgs& gate_up, const GemmArgs& down, int32_t* ready, cudaStream_t s);
+
+// Kernel-side view of one projection (a phase) of a launch.
+struct GemmPhase {
+  const uint8_t* packed;
+  const float* gscale;
+  void* out;
+  const uint16_t* act;
+  const int32_t* gather_rows;
+  int N, K, out_ld, mode;
+};
+struct GemmLaunch {
+  GemmPhase ph[2];
+  int nph;
+  const int32_t* offsets;
+  int32_t* ready;  // per expert: epilogue warps done with phase-0 tiles (nph == 2)
+  int* status;
+  int E;
+};
 
 // Kernel launches made by launch_route_group for these sizes.
 int route_group_launches(int T, int E, int k);

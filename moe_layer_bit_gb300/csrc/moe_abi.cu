@@ -18,8 +18,8 @@ inline cudaStream_t as_stream(void* s) { return reinterpret_cast<cudaStream_t>(s
 
 // Workspace layout: the status word always sits at offset 0.
 struct Layout {
-  size_t status, perm, ids, w, counts, offsets, sorted_token, inv_perm, x_perm, h, y, hx, hlogits, hout, stage_total,
-      total;
+  size_t status, perm, ids, w, counts, offsets, ready, sorted_token, inv_perm, x_perm, h, y, hx, hlogits, hout,
+      stage_total, total;
 };
 
 Layout layout_of(const moe_dims& d) {
@@ -39,6 +39,8 @@ Layout layout_of(const moe_dims& d) {
   o = align_up(o + (size_t)d.E * sizeof(int32_t));
   L.offsets = o;
   o = align_up(o + (size_t)(d.E + 1) * sizeof(int32_t));
+  L.ready = o;
+  o = align_up(o + (size_t)d.E * sizeof(int32_t));
   L.sorted_token = o;
   o = align_up(o + n * sizeof(int32_t));
   L.inv_perm = o;
@@ -124,7 +126,13 @@ int moe_layer_kernel_launches(moe_dims d) {
   MOE_TRY_NEG(check_dims(d));
   if (d.T == 0) return 0;
   const bool gemm_gathers = moe::gemm_gathers_rows(d.T * d.k, d.E, d.H);
-  return moe::route_group_launches(d.T, d.E, d.k) + (gemm_gathers ? 0 : 1) + 3;
+  const bool fused = moe::gemm_fuses_layer(d.T * d.k, d.E, d.H, d.I);
+  return moe::route_group_launches(d.T, d.E, d.k) + (gemm_gathers ? 0 : 1) + (fused ? 1 : 2) + 1;
+}
+
+int moe_layer_projections_fused(moe_dims d) {
+  MOE_TRY_NEG(check_dims(d));
+  return d.T > 0 && moe::gemm_fuses_layer(d.T * d.k, d.E, d.H, d.I) ? 1 : 0;
 }
 
 size_t moe_stage_workspace_bytes(moe_dims d) {
@@ -241,8 +249,10 @@ int layer_forward_impl(const uint16_t* x, const float* logits, moe_w4 w_gate_up,
   uint16_t* h = reinterpret_cast<uint16_t*>(w + L.h);
   float* y = reinterpret_cast<float*>(w + L.y);
   MOE_TRY(mark(0));
+  int32_t* ready = reinterpret_cast<int32_t*>(w + L.ready);
+  const bool fused = moe::gemm_fuses_layer(d.T * d.k, d.E, d.H, d.I);
   MOE_TRY(cuda_status(moe::launch_route_group(logits, d.T, d.E, d.k, ids, wts, counts, offs, sorted, inv,
-                                              reinterpret_cast<int32_t*>(w + L.perm), s)));
+                                              reinterpret_cast<int32_t*>(w + L.perm), fused ? ready : nullptr, s)));
   MOE_TRY(mark(1));
   // the narrow-tile GEMM gathers the rows of x itself; the wide one reads x_perm
   const bool gemm_gathers = moe::gemm_gathers_rows(d.T * d.k, d.E, d.H);
@@ -263,17 +273,24 @@ int layer_forward_impl(const uint16_t* x, const float* logits, moe_w4 w_gate_up,
   a.N = 2 * d.I;
   a.K = d.H;
   a.out_ld = d.I;
-  MOE_TRY(cuda_status(run_gemm(0, a, s)));
-  MOE_TRY(mark(3));
-  a.act = h;
-  a.gather_rows = nullptr;
-  a.packed = static_cast<const uint8_t*>(w_down.packed);
-  a.gscale = w_down.global_scale;
-  a.out = y;
-  a.N = d.H;
-  a.K = d.I;
-  a.out_ld = d.H;
-  MOE_TRY(cuda_status(run_gemm(1, a, s)));
+  moe::GemmArgs b = a;
+  b.act = h;
+  b.gather_rows = nullptr;
+  b.packed = static_cast<const uint8_t*>(w_down.packed);
+  b.gscale = w_down.global_scale;
+  b.out = y;
+  b.N = d.H;
+  b.K = d.I;
+  b.out_ld = d.H;
+  if (fused) {
+    // one launch for both projections: stage 2 spans it, stage 3 is empty
+    MOE_TRY(cuda_status(moe::launch_gemm_layer(a, b, ready, s)));
+    MOE_TRY(mark(3));
+  } else {
+    MOE_TRY(cuda_status(run_gemm(0, a, s)));
+    MOE_TRY(mark(3));
+    MOE_TRY(cuda_status(run_gemm(1, b, s)));
+  }
   MOE_TRY(mark(4));
   MOE_TRY(cuda_status(moe::launch_combine(y, inv, wts, d.T, d.H, d.k, out, s)));
   return mark(5);

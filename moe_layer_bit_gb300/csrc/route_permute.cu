@@ -220,7 +220,8 @@ __device__ __forceinline__ int32_t block_exclusive_scan(int32_t x, int32_t* warp
 
 // One block of 1024 threads; thread e owns expert e.
 __global__ void __launch_bounds__(1024) perm_scan_kernel(int32_t* __restrict__ chunk_counts, int nchunks, int E,
-                                                         int32_t* __restrict__ counts, int32_t* __restrict__ offsets) {
+                                                         int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
+                                                         int32_t* __restrict__ zero_e) {
   __shared__ int32_t warp_tot[32];
   const int e = threadIdx.x;
   pdl_wait();
@@ -233,6 +234,7 @@ __global__ void __launch_bounds__(1024) perm_scan_kernel(int32_t* __restrict__ c
       run += c;
     }
     counts[e] = run;
+    if (zero_e != nullptr) zero_e[e] = 0;
   }
   int32_t total;
   const int32_t excl = block_exclusive_scan(run, warp_tot, &total);
@@ -282,7 +284,7 @@ template <int NV>
 __global__ void __launch_bounds__(kPermChunk) route_permute_small_kernel(
     const float* __restrict__ logits, int T, int E, int k, int32_t* __restrict__ ids, float* __restrict__ wts,
     int32_t* __restrict__ counts, int32_t* __restrict__ offsets, int32_t* __restrict__ sorted_token,
-    int32_t* __restrict__ inv_perm) {
+    int32_t* __restrict__ inv_perm, int32_t* __restrict__ zero_e) {
   extern __shared__ int32_t smem_i[];
   int32_t* base = smem_i;                                  // [E] counts, then offsets
   int32_t* s_ids = smem_i + E;                             // [kPermChunk]
@@ -322,6 +324,7 @@ __global__ void __launch_bounds__(kPermChunk) route_permute_small_kernel(
     offsets[tid] = excl;
     base[tid] = excl;
     if (tid == E - 1) offsets[E] = excl + c;
+    if (zero_e != nullptr) zero_e[tid] = 0;
   }
   __syncthreads();
   if (valid) {
@@ -365,21 +368,23 @@ cudaError_t launch_gather(const uint16_t* x, const int32_t* sorted_token, int n,
 
 template <int NV>
 static cudaError_t launch_small(const float* logits, int T, int E, int k, int32_t* ids, float* w, int32_t* counts,
-                                int32_t* offsets, int32_t* sorted_token, int32_t* inv_perm, cudaStream_t s) {
+                                int32_t* offsets, int32_t* sorted_token, int32_t* inv_perm, int32_t* zero_e,
+                                cudaStream_t s) {
   const size_t smem = small_smem_bytes(E);
   auto kern = route_permute_small_kernel<NV>;
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (err != cudaSuccess) return err;
   return launch_pdl(kern, dim3(1), dim3(kPermChunk), smem, s, logits, T, E, k, ids, w, counts, offsets, sorted_token,
-                    inv_perm);
+                    inv_perm, zero_e);
 }
 
 static cudaError_t launch_chunked(const int32_t* ids, int n, int E, int k, int32_t* counts, int32_t* offsets,
-                                  int32_t* sorted_token, int32_t* inv_perm, int32_t* scratch, cudaStream_t s) {
+                                  int32_t* sorted_token, int32_t* inv_perm, int32_t* scratch, int32_t* zero_e,
+                                  cudaStream_t s) {
   const int nchunks = (n + kPermChunk - 1) / kPermChunk;
   cudaError_t err = launch_pdl(perm_hist_kernel, dim3(nchunks), dim3(256), E * sizeof(int32_t), s, ids, n, E, scratch);
   if (err != cudaSuccess) return err;
-  err = launch_pdl(perm_scan_kernel, dim3(1), dim3(1024), 0, s, scratch, nchunks, E, counts, offsets);
+  err = launch_pdl(perm_scan_kernel, dim3(1), dim3(1024), 0, s, scratch, nchunks, E, counts, offsets, zero_e);
   if (err != cudaSuccess) return err;
   const size_t smem = scatter_smem_bytes(E);
   err = cudaFuncSetAttribute(perm_scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -394,8 +399,8 @@ cudaError_t launch_permute(const int32_t* ids, const uint16_t* x, int T, int H, 
   const int n = T * k;
   cudaError_t err = (n <= kPermChunk)
                         ? launch_small<1>(nullptr, T, E, k, const_cast<int32_t*>(ids), nullptr, counts, offsets,
-                                          sorted_token, inv_perm, s)
-                        : launch_chunked(ids, n, E, k, counts, offsets, sorted_token, inv_perm, scratch, s);
+                                          sorted_token, inv_perm, nullptr, s)
+                        : launch_chunked(ids, n, E, k, counts, offsets, sorted_token, inv_perm, scratch, nullptr, s);
   if (err != cudaSuccess) return err;
   return launch_gather(x, sorted_token, n, H, x_perm, s);
 }
@@ -412,19 +417,19 @@ int route_group_launches(int T, int E, int k) {
 
 cudaError_t launch_route_group(const float* logits, int T, int E, int k, int32_t* ids, float* w, int32_t* counts,
                                int32_t* offsets, int32_t* sorted_token, int32_t* inv_perm, int32_t* scratch,
-                               cudaStream_t s) {
+                               int32_t* zero_e, cudaStream_t s) {
   const int n = T * k;
   cudaError_t err;
   if (n <= kPermChunk && (long long)T * E <= kFusedRouteLogits) {
     MOE_DISPATCH_NV(route_nv(E), err = (launch_small<NV>(logits, T, E, k, ids, w, counts, offsets, sorted_token,
-                                                         inv_perm, s)));
+                                                         inv_perm, zero_e, s)));
     return err;
   }
   err = launch_route_topk(logits, T, E, k, ids, w, s);
   if (err != cudaSuccess) return err;
   if (n <= kPermChunk)
-    return launch_small<1>(nullptr, T, E, k, ids, nullptr, counts, offsets, sorted_token, inv_perm, s);
-  return launch_chunked(ids, n, E, k, counts, offsets, sorted_token, inv_perm, scratch, s);
+    return launch_small<1>(nullptr, T, E, k, ids, nullptr, counts, offsets, sorted_token, inv_perm, zero_e, s);
+  return launch_chunked(ids, n, E, k, counts, offsets, sorted_token, inv_perm, scratch, zero_e, s);
 }
 
 // ------------------------------------------------------------------ combine

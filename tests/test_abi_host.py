@@ -73,17 +73,19 @@ def test_bad_dims_are_rejected_before_launch(lib, dims, code):
     assert _lib.moe_layer_kernel_launches(d) == -code
 
 
-@pytest.mark.parametrize("dims,launches", [
-    ((0, 2048, 768, 128, 8), 0),          # nothing to do
-    ((32, 2048, 768, 128, 8), 4),         # fused routing + grouping; the narrow GEMM gathers x itself
-    ((64, 256, 128, 1024, 4), 5),         # T*E too large for the fused block: routing + grouping
-    ((800, 2048, 512, 256, 8), 8),        # chunked grouping, row gather, wide GEMM tiles
-    ((16, 128, 64, 8, 2), 4),             # narrow tiles at any K
-    ((2048, 256, 128, 64, 2), 8),         # 64-row tiles read a permuted copy: row gather kernel
+@pytest.mark.parametrize("dims,launches,fused", [
+    ((0, 2048, 768, 128, 8), 0, False),     # nothing to do
+    ((32, 2048, 768, 128, 8), 3, True),     # routing + grouping block; both projections in one GEMM launch
+    ((64, 256, 128, 1024, 4), 4, True),     # T*E too large for the fused block: routing, then grouping
+    ((800, 2048, 512, 256, 8), 8, False),   # chunked grouping, row gather, two wide-tile GEMMs
+    ((16, 128, 64, 8, 2), 3, True),         # narrow tiles at any K
+    ((2048, 256, 128, 64, 2), 8, False),    # 128-row tiles read a permuted copy: row gather kernel
 ])
-def test_layer_kernel_launch_count(lib, dims, launches):
-    # host-only query; the bench reports it as the launches it timed
-    assert _lib.moe_layer_kernel_launches(_lib.dims(*dims)) == launches
+def test_layer_kernel_launch_count(lib, dims, launches, fused):
+    # host-only queries; the bench reports the launches it timed
+    d = _lib.dims(*dims)
+    assert _lib.moe_layer_kernel_launches(d) == launches
+    assert _lib.moe_layer_projections_fused(d) == fused
 
 
 def test_null_misaligned_and_small_workspace(lib):
