@@ -241,6 +241,15 @@ int moe_debug_dequant_table(uint16_t *out, void *stream);
  * moe_get_device_status.  Nothing faults and the context stays usable. */
 int moe_debug_timeout_probe(void *ws, uint64_t limit_ns, void *stream);
 
+/* Test hook for failure detection of the cross-CTA wait: when
+ * moe_layer_projections_fused(d), a down tile waits on a per-expert counter
+ * that the gate_up tiles of other CTAs increment.  This launches a kernel
+ * that waits, with limit `limit_ns`, on a counter nothing increments (the int
+ * at byte 128 of `ws`, zeroed first; ws must hold >= 132 bytes).  The wait
+ * gives up and records MOE_ERR_DEVICE_TIMEOUT in the status word; nothing
+ * faults and the context stays usable. */
+int moe_debug_counter_timeout_probe(void *ws, uint64_t limit_ns, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

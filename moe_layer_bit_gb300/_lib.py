@@ -68,6 +68,7 @@ _SIGS = {
     "moe_status_string": (ctypes.c_char_p, [INT]),
     "moe_debug_dequant_table": (INT, [P, P]),
     "moe_debug_timeout_probe": (INT, [P, ctypes.c_uint64, P]),
+    "moe_debug_counter_timeout_probe": (INT, [P, ctypes.c_uint64, P]),
 }
 
 
@@ -211,3 +212,8 @@ def moe_debug_dequant_table(out, stream=None):
 
 def moe_debug_timeout_probe(ws, limit_ns: int, stream=None):
     _check(load().moe_debug_timeout_probe(_p(ws), int(limit_ns), _s(stream)), "moe_debug_timeout_probe")
+
+
+def moe_debug_counter_timeout_probe(ws, limit_ns: int, stream=None):
+    _check(load().moe_debug_counter_timeout_probe(_p(ws), int(limit_ns), _s(stream)),
+           "moe_debug_counter_timeout_probe")

@@ -114,11 +114,11 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
   }
 }
 
-// One acquire load: has the GPU-scope counter reached `target`?
-__device__ __forceinline__ bool counter_reached(const int* ctr, int target) {
+// Acquire load of a GPU-scope counter.
+__device__ __forceinline__ int counter_load_acquire(const int* ctr) {
   int v;
   asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(ctr) : "memory");
-  return v >= target;
+  return v;
 }
 // Bounded wait until the GPU-scope counter *ctr reaches `target`, polled with
 // acquire loads (so this thread's later reads see what the writers published

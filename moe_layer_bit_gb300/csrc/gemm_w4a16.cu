@@ -95,7 +95,7 @@ struct Cfg {
   // activation stage is then released kBInFlight stages after it was issued,
   // so that ring is deeper.  Wider tiles read permuted rows with TMA.
   static constexpr bool kGatherB = BN <= 32;
-  static constexpr int NSB = kGatherB ? 4 + kBInFlight : 4;
+  static constexpr int NSB = kGatherB ? 8 + kBInFlight : 4;
   static_assert(!kGatherB || NSB > kBInFlight, "the gathering producer must not wait on a stage it has not released");
   static constexpr int NSW0 = (kSmemBudget - NSB * kBTile) / kWBytes;
   static constexpr int NSW1 = NSW0 > 12 ? 12 : NSW0;
@@ -293,7 +293,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // this expert's h rows: every phase-0 tile of it, 4 epilogue warps each
         const int* ctr = L.ready + tr.c.e;
         const int target = 4 * MT0 * (s_tprefix[tr.c.e + 1] - s_tprefix[tr.c.e]);
-        if (!__all_sync(0xFFFFFFFFu, counter_reached(ctr, target))) {
+        if (!__all_sync(0xFFFFFFFFu, counter_load_acquire(ctr) >= target)) {
           release_all();
           ok = __all_sync(0xFFFFFFFFu, wait_counter(ctr, target, abort_flag, status));
           if (!ok) break;
@@ -761,6 +761,18 @@ __global__ void timeout_probe_kernel(int* status, unsigned long long limit_ns) {
 
 cudaError_t launch_timeout_probe(int* status, unsigned long long limit_ns, cudaStream_t s) {
   timeout_probe_kernel<<<1, 32, 0, s>>>(status, limit_ns);
+  return cudaGetLastError();
+}
+
+// Waits, like a down tile of the one-launch projections, on a GPU-scope
+// readiness counter that nothing increments (`ctr`, zero, target 1); the
+// bounded wait must give up and record a timeout.
+__global__ void counter_timeout_probe_kernel(int* status, const int* ctr, unsigned long long limit_ns) {
+  wait_counter(ctr, 1, nullptr, status, limit_ns);
+}
+
+cudaError_t launch_counter_timeout_probe(int* status, const int* ctr, unsigned long long limit_ns, cudaStream_t s) {
+  counter_timeout_probe_kernel<<<1, 32, 0, s>>>(status, ctr, limit_ns);
   return cudaGetLastError();
 }
 

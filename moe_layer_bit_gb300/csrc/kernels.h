@@ -129,5 +129,7 @@ int route_group_launches(int T, int E, int k);
 // Bounded-wait self test: a kernel waits on a barrier nobody arrives at and
 // must give up after `limit_ns`, recording a timeout in `status`.
 cudaError_t launch_timeout_probe(int* status, unsigned long long limit_ns, cudaStream_t s);
+// The same for the cross-CTA counter wait: `ctr` is a zero int nothing increments.
+cudaError_t launch_counter_timeout_probe(int* status, const int* ctr, unsigned long long limit_ns, cudaStream_t s);
 
 }  // namespace moe

@@ -369,4 +369,13 @@ int moe_debug_timeout_probe(void* ws, uint64_t limit_ns, void* stream) {
                                                as_stream(stream)));
 }
 
+int moe_debug_counter_timeout_probe(void* ws, uint64_t limit_ns, void* stream) {
+  MOE_TRY(check_ptrs({ws}));
+  int* base = static_cast<int*>(ws);
+  cudaStream_t s = as_stream(stream);
+  // the counter: the int at byte 128 of ws, zeroed here
+  MOE_TRY(cuda_status(cudaMemsetAsync(base + 32, 0, sizeof(int), s)));
+  return cuda_status(moe::launch_counter_timeout_probe(base, base + 32, (unsigned long long)limit_ns, s));
+}
+
 }  // extern "C"

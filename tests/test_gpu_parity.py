@@ -349,6 +349,18 @@ def test_output_guard_bands_untouched():
     assert bool((b[:guard] == 0x5A5A).all()) and bool((b[guard + wl.T * wl.H:] == 0x5A5A).all())
 
 
+def test_cross_cta_counter_wait_reports_timeout_and_context_survives():
+    ws = torch.zeros(256, dtype=torch.uint8, device=DEV)
+    _lib.moe_debug_counter_timeout_probe(ws, 20_000_000)    # 20 ms limit
+    assert _lib.moe_get_device_status(ws) == _lib.MOE_ERR_DEVICE_TIMEOUT
+    assert _lib.moe_get_device_status(ws) == _lib.MOE_OK
+    wl, d = workload_inputs("decode")
+    layer = _layer(wl, d)
+    out = layer.forward(d["x"].to(DEV), d["logits"].to(DEV))
+    assert layer.device_status() == _lib.MOE_OK
+    assert torch.isfinite(out.float()).all()
+
+
 def test_bounded_wait_reports_timeout_and_context_survives():
     ws = torch.zeros(256, dtype=torch.uint8, device=DEV)
     _lib.moe_debug_timeout_probe(ws, 20_000_000)            # 20 ms limit
