@@ -127,7 +127,9 @@ struct Cfg {
   }
 };
 
-template <int BN, int SB>
+// MODE 0 / 1: one phase, gate_up + SwiGLU / down, fixed at compile time;
+// MODE 2: the phases' own modes (the one-launch layer).
+template <int BN, int SB, int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
     w4a16_gemm_kernel(const __grid_constant__ CUtensorMap tmap_act, const __grid_constant__ GemmLaunch L) {
   using C = Cfg<BN, SB>;
@@ -446,7 +448,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld16(t_acc + (uint32_t)(cc * 16), v);
         tc_wait_ld();
         if (cc * 16 >= nvalid) continue;
-        if (P.mode == 0) {
+        if ((MODE == 2 ? P.mode : MODE) == 0) {
           // rows 32q..32q+15 hold gate features f, rows 32q+16.. the matching up rows
           const int f = c.mt * 64 + 16 * q + (lane & 15);
           const bool is_gate = lane < 16;
@@ -528,7 +530,7 @@ static GemmPhase phase_of(int mode, const GemmArgs& a) {
 }
 
 // `rows` activation rows (T*k); the phases of L share them and the offsets.
-template <int BN, int SB>
+template <int BN, int SB, int MODE>
 static cudaError_t launch_gemm_cfg(const GemmLaunch& L, int rows, cudaStream_t s) {
   using C = Cfg<BN, SB>;
   CUtensorMap tmap;
@@ -558,7 +560,7 @@ static cudaError_t launch_gemm_cfg(const GemmLaunch& L, int rows, cudaStream_t s
   const int grid = (int)(max_tiles < sms ? max_tiles : sms);
   if (grid <= 0) return cudaSuccess;
   const int smem = C::bytes(L.E);
-  auto kern = w4a16_gemm_kernel<BN, SB>;
+  auto kern = w4a16_gemm_kernel<BN, SB, MODE>;
   err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (err != cudaSuccess) return err;
   // Two phases: phase-1 CTAs wait on phase-0 tiles of other CTAs, so all CTAs
@@ -598,15 +600,24 @@ static int pick_sb(int bn, const int* kb, int nph) {
   }
 }
 
-template <int BN>
-static cudaError_t launch_gemm_bn(const GemmLaunch& L, int rows, cudaStream_t s) {
+template <int BN, int MODE>
+static cudaError_t launch_gemm_mode(const GemmLaunch& L, int rows, cudaStream_t s) {
   int kb[2];
   for (int p = 0; p < L.nph; ++p) kb[p] = L.ph[p].K / kBlockK;
   switch (pick_sb(BN, kb, L.nph)) {
-    case 4: return launch_gemm_cfg<BN, (BN <= 16 ? 4 : 2)>(L, rows, s);
-    case 2: return launch_gemm_cfg<BN, 2>(L, rows, s);
-    default: return launch_gemm_cfg<BN, 1>(L, rows, s);
+    case 4: return launch_gemm_cfg<BN, (BN <= 16 ? 4 : 2), MODE>(L, rows, s);
+    case 2: return launch_gemm_cfg<BN, 2, MODE>(L, rows, s);
+    default: return launch_gemm_cfg<BN, 1, MODE>(L, rows, s);
   }
+}
+
+template <int BN>
+static cudaError_t launch_gemm_bn(const GemmLaunch& L, int rows, cudaStream_t s) {
+  if (L.nph > 1) {
+    if constexpr (BN <= 32) return launch_gemm_mode<BN, 2>(L, rows, s);
+    return cudaErrorInvalidValue;  // one-launch layers use narrow token tiles only
+  }
+  return L.ph[0].mode == 0 ? launch_gemm_mode<BN, 0>(L, rows, s) : launch_gemm_mode<BN, 1>(L, rows, s);
 }
 
 static cudaError_t launch_gemm_any(const GemmLaunch& L, int rows, cudaStream_t s) {
