@@ -126,6 +126,19 @@ int moe_layer_kernel_launches(moe_dims d);
 int moe_layer_projections_fused(moe_dims d);
 size_t moe_stage_workspace_bytes(moe_dims d);
 
+/* Gate logits of the layer (Atlas: gate input -> gate logits -> expert IDs,
+ * section «KV Cache量化、MTP推测解码和调试工具链»):
+ *   logits[t][e] = sum_h x[t][h] * router_weight[e][h]  (+ router_bias[e])
+ * x bf16 [T][H], router_weight bf16 [E][H], router_bias f32 [E] or NULL,
+ * logits f32 [T][E] out.  Computed in one fixed fp32 order, independent of
+ * the launch shape, so routing on the result is reproducible bit for bit: the
+ * hidden dimension is cut into 8-element chunks, part l (0..31) sums x*w over
+ * chunks l, l+32, ... in ascending h with fused multiply-adds from 0, the 32
+ * parts are combined pairwise (part l + part l^s for s = 16, 8, 4, 2, 1) and
+ * the bias is added last.  x, router_weight, logits 16-byte aligned. */
+int moe_router_logits(const uint16_t *x, const uint16_t *router_weight, const float *router_bias,
+                      moe_dims d, float *logits, void *stream);
+
 /* [Atlas] "KV Cache量化…" (gate logits -> expert IDs), [ATOM] 8.1 (top-k).
  * logits  float [T][E]   router logits (NaN is treated as -infinity)
  * topk_ids int32 [T][k]  out: selected experts, slot order = descending logit,
@@ -210,6 +223,34 @@ int moe_layer_forward(const uint16_t *x, const float *logits, moe_w4 w_gate_up, 
 int moe_layer_forward_profiled(const uint16_t *x, const float *logits, moe_w4 w_gate_up, moe_w4 w_down,
                                moe_dims d, uint16_t *out, int32_t *topk_ids, float *topk_w, void *ws,
                                size_t ws_bytes, void *stream, void *const *stage_events);
+
+/* moe_layer_forward with the gate logits computed in the layer from the
+ * router weights (moe_router_logits) instead of passed in.  logits_out:
+ * f32 [T][E] that receives them, or NULL (then they live in ws).  Same
+ * workspace as moe_layer_forward. */
+int moe_layer_forward_router(const uint16_t *x, const uint16_t *router_weight, const float *router_bias,
+                             moe_w4 w_gate_up, moe_w4 w_down, moe_dims d, uint16_t *out, float *logits_out,
+                             int32_t *topk_ids, float *topk_w, void *ws, size_t ws_bytes, void *stream);
+
+/* The layer with a shared expert.  The Atlas article's MoE layer produces a
+ * routed output and a shared-expert output (section «KV Cache量化、MTP推测解码
+ * 和调试工具链», which dumps both per layer); here
+ *   out[t] = bf16( sum_j topk_w[t][j] * y_{ids[t][j]}(x[t])  +  y_shared(x[t]) )
+ * with the routed sum in ascending j (fp32), then the shared term added with
+ * weight 1.  y_shared is a SwiGLU FFN like a routed expert's, with
+ * shared_gate_up / shared_down: one-expert NVFP4 matrices (moe_prepack_w4
+ * with E = 1) of the routed experts' H and I.  It runs in the same grouped
+ * launches as the routed experts, as an extra expert that every token uses.
+ * Gate logits: `logits` (f32 [T][E]), or, with logits == NULL,
+ * computed from router_weight (bf16 [E][H]) and router_bias (f32 [E] or
+ * NULL) as moe_router_logits does, into logits_out (f32 [T][E], or ws when
+ * NULL).  Exactly one of logits / router_weight is non-NULL.  Needs E < 1024
+ * and k < 32 (else MOE_ERR_UNSUPPORTED_SHAPE).  Same workspace as
+ * moe_layer_forward. */
+int moe_layer_forward_shared(const uint16_t *x, const float *logits, const uint16_t *router_weight,
+                             const float *router_bias, moe_w4 w_gate_up, moe_w4 w_down, moe_w4 shared_gate_up,
+                             moe_w4 shared_down, moe_dims d, uint16_t *out, float *logits_out, int32_t *topk_ids,
+                             float *topk_w, void *ws, size_t ws_bytes, void *stream);
 
 /* The whole layer from HOST buffers: copies host_x (bf16 [T][H]) and
  * host_logits (float [T][E]) into ws, runs moe_layer_forward, copies the

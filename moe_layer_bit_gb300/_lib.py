@@ -55,6 +55,7 @@ _SIGS = {
     "moe_layer_kernel_launches": (ctypes.c_int, [Dims]),
     "moe_layer_projections_fused": (ctypes.c_int, [Dims]),
     "moe_stage_workspace_bytes": (SZ, [Dims]),
+    "moe_router_logits": (INT, [P, P, P, Dims, P, P]),
     "moe_route_topk": (INT, [P, Dims, P, P, P]),
     "moe_permute": (INT, [P, P, Dims, P, P, P, P, P, P, SZ, P]),
     "moe_permute_noalloc": (INT, [P, P, Dims, P, P, P, P, P, P]),
@@ -64,6 +65,8 @@ _SIGS = {
     "moe_layer_forward": (INT, [P, P, W4, W4, Dims, P, P, P, P, SZ, P]),
     "moe_layer_forward_profiled": (INT, [P, P, W4, W4, Dims, P, P, P, P, SZ, P, P]),
     "moe_layer_forward_host": (INT, [P, P, W4, W4, Dims, P, P, SZ, P]),
+    "moe_layer_forward_router": (INT, [P, P, P, W4, W4, Dims, P, P, P, P, P, SZ, P]),
+    "moe_layer_forward_shared": (INT, [P, P, P, P, W4, W4, W4, W4, Dims, P, P, P, P, P, SZ, P]),
     "moe_get_device_status": (INT, [P, P]),
     "moe_status_string": (ctypes.c_char_p, [INT]),
     "moe_debug_dequant_table": (INT, [P, P]),
@@ -152,6 +155,25 @@ def moe_layer_projections_fused(d: Dims) -> bool:
 
 def moe_stage_workspace_bytes(d: Dims) -> int:
     return int(load().moe_stage_workspace_bytes(d))
+
+
+def moe_router_logits(x, router_weight, router_bias, d, logits, stream=None):
+    _check(load().moe_router_logits(_p(x), _p(router_weight), _p(router_bias), d, _p(logits), _s(stream)),
+           "moe_router_logits")
+
+
+def moe_layer_forward_router(x, router_weight, router_bias, w_gate_up: W4, w_down: W4, d, out, logits_out,
+                             topk_ids, topk_w, ws, ws_bytes, stream=None):
+    _check(load().moe_layer_forward_router(_p(x), _p(router_weight), _p(router_bias), w_gate_up, w_down, d, _p(out),
+                                           _p(logits_out), _p(topk_ids), _p(topk_w), _p(ws), ws_bytes, _s(stream)),
+           "moe_layer_forward_router")
+
+
+def moe_layer_forward_shared(x, logits, router_weight, router_bias, w_gate_up: W4, w_down: W4, shared_gate_up: W4,
+                             shared_down: W4, d, out, logits_out, topk_ids, topk_w, ws, ws_bytes, stream=None):
+    _check(load().moe_layer_forward_shared(_p(x), _p(logits), _p(router_weight), _p(router_bias), w_gate_up, w_down,
+                                           shared_gate_up, shared_down, d, _p(out), _p(logits_out), _p(topk_ids),
+                                           _p(topk_w), _p(ws), ws_bytes, _s(stream)), "moe_layer_forward_shared")
 
 
 def moe_route_topk(logits, d, topk_ids, topk_w, stream=None):

@@ -231,7 +231,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       const TileRef tr = tile_of(u);
       const GemmPhase& P = L.ph[tr.ph];
       const int MT = tr.ph == 0 ? MT0 : MT1, KS = tr.ph == 0 ? KS0 : KS1;
-      const uint8_t* wsrc = P.packed + (size_t)(tr.c.e * MT + tr.c.mt) * KS * SB * kWBlockBytes;
+      // experts 0 .. E_routed-1 are the routed ones; the next (if any) is the
+      // shared expert, whose weights are a separate one-expert matrix
+      const uint8_t* wsrc = tr.c.e < P.E_routed
+                                ? P.packed + (size_t)(tr.c.e * MT + tr.c.mt) * KS * SB * kWBlockBytes
+                                : P.shared_packed + (size_t)tr.c.mt * KS * SB * kWBlockBytes;
       const int row0 = s_off[tr.c.e] + tr.c.nt * BN;
       for (int ks = 0; ks < KS; ++ks, ++i) {
         const int s = i % ring;
@@ -440,7 +444,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const int p0 = s_off[c.e] + c.nt * BN;
       const int nvalid = min(BN, s_off[c.e + 1] - p0);
-      const float gsc = __ldg(P.gscale + c.e) * 128.0f;
+      const float gsc = __ldg(c.e < P.E_routed ? P.gscale + c.e : P.shared_gscale) * 128.0f;
       const uint32_t t_acc = tmem_base + ((uint32_t)(32 * q) << 16) + (uint32_t)(d * BN);
 #pragma unroll 1
       for (int cc = 0; cc < BN / 16; ++cc) {
@@ -519,6 +523,9 @@ static GemmPhase phase_of(int mode, const GemmArgs& a) {
   GemmPhase p;
   p.packed = a.packed;
   p.gscale = a.gscale;
+  p.shared_packed = a.shared_packed;
+  p.shared_gscale = a.shared_gscale;
+  p.E_routed = a.shared_packed != nullptr ? a.E - 1 : a.E;
   p.out = a.out;
   p.act = a.act;
   p.gather_rows = a.gather_rows;

@@ -47,6 +47,11 @@ constexpr int kTileM = 128;
 constexpr int kBlockK = 64;
 constexpr int kWBlockBytes = 4608;
 
+// Gate logits [T][E] = x [T][H] * Wr^T (Wr bf16 [E][H]) (+ bias [E]) in the
+// library's fixed fp32 order (router.cu).
+cudaError_t launch_router_logits(const uint16_t* x, const uint16_t* wr, const float* bias, int T, int H, int E,
+                                 float* logits, cudaStream_t s);
+
 cudaError_t launch_route_topk(const float* logits, int T, int E, int k, int32_t* ids, float* w, cudaStream_t s);
 
 size_t perm_scratch_bytes(int T, int E, int k);
@@ -54,20 +59,23 @@ cudaError_t launch_permute(const int32_t* ids, const uint16_t* x, int T, int H, 
                            int32_t* offsets, int32_t* sorted_token, int32_t* inv_perm, uint16_t* x_perm,
                            int32_t* scratch, cudaStream_t s);
 
-// Routing and grouping of the layer: top-k routing, then counts, offsets,
-// sorted_token and inv_perm; zero_e (E int32, may be null) is zeroed.
-// T*k <= 1024 with T*E <= 32768 runs as one single-block launch; otherwise
-// routing, then one grouping block (T*k <= 1024) or histogram + scan +
-// scatter.
-cudaError_t launch_route_group(const float* logits, int T, int E, int k, int32_t* ids, float* w, int32_t* counts,
-                               int32_t* offsets, int32_t* sorted_token, int32_t* inv_perm, int32_t* scratch,
-                               int32_t* zero_e, cudaStream_t s);
+// Routing and grouping of the layer: top-k routing (ids / w [T][k]), then
+// counts, offsets, sorted_token and inv_perm of the grouped view: with
+// `shared`, every token has a (k+1)-th slot for the shared expert, grouped as
+// expert E (so E+1 groups, T*(k+1) rows).  zero_e (one int32 per group, may
+// be null) is zeroed.  T*(k+shared) <= 1024 with T*E <= 32768 runs as one
+// single-block launch; otherwise routing, then one grouping block or
+// histogram + scan + scatter.
+cudaError_t launch_route_group(const float* logits, int T, int E, int k, bool shared, int32_t* ids, float* w,
+                               int32_t* counts, int32_t* offsets, int32_t* sorted_token, int32_t* inv_perm,
+                               int32_t* scratch, int32_t* zero_e, cudaStream_t s);
 // x_perm[p] = x[sorted_token[p]] for p < n.
 cudaError_t launch_gather(const uint16_t* x, const int32_t* sorted_token, int n, int H, uint16_t* x_perm,
                           cudaStream_t s);
 
-cudaError_t launch_combine(const float* y, const int32_t* inv, const float* w, int T, int H, int k, uint16_t* out,
-                           cudaStream_t s);
+// out = sum over the k routed slots of w * y (+ the shared expert's row).
+cudaError_t launch_combine(const float* y, const int32_t* inv, const float* w, int T, int H, int k, bool shared,
+                           uint16_t* out, cudaStream_t s);
 
 cudaError_t launch_prepack(const uint8_t* codes, const uint8_t* scales, int E, int N, int K, int proj,
                            uint8_t* packed, cudaStream_t s);
@@ -84,10 +92,14 @@ struct GemmArgs {
   const int32_t* gather_rows;
   const uint8_t* packed;
   const float* gscale;
+  // with a shared expert: its one-expert packed matrix and global scale; it is
+  // the last of the E experts the offsets describe (E - 1 routed ones)
+  const uint8_t* shared_packed;
+  const float* shared_gscale;
   const int32_t* offsets;
   void* out;
   int* status;
-  int rows;  // T*k
+  int rows;  // T*k (T*(k+1) with a shared expert)
   int E, N, K;
   int out_ld;  // I (mode 0) or H (mode 1)
   int T, k;
@@ -109,6 +121,9 @@ cudaError_t launch_gemm_layer(const GemmArgs& gate_up, const GemmArgs& down, int
 struct GemmPhase {
   const uint8_t* packed;
   const float* gscale;
+  const uint8_t* shared_packed;
+  const float* shared_gscale;
+  int E_routed;  // experts >= E_routed take the shared weights
   void* out;
   const uint16_t* act;
   const int32_t* gather_rows;
@@ -124,7 +139,7 @@ struct GemmLaunch {
 };
 
 // Kernel launches made by launch_route_group for these sizes.
-int route_group_launches(int T, int E, int k);
+int route_group_launches(int T, int E, int k, bool shared);
 
 // Bounded-wait self test: a kernel waits on a barrier nobody arrives at and
 // must give up after `limit_ns`, recording a timeout in `status`.

@@ -22,25 +22,30 @@ struct Layout {
       stage_total, total;
 };
 
-Layout layout_of(const moe_dims& d) {
+// A shared expert adds one slot per token and one expert group (needs E < 1024).
+bool shared_possible(const moe_dims& d) { return d.E < 1024; }
+
+Layout layout_of(const moe_dims& d, bool shared) {
   Layout L{};
-  const size_t n = (size_t)d.T * d.k;
+  const int ks = d.k + (shared ? 1 : 0), EG = d.E + (shared ? 1 : 0);
+  const size_t nr = (size_t)d.T * d.k;  // routed (token, slot) pairs
+  const size_t n = (size_t)d.T * ks;    // grouped rows
   size_t o = 0;
   L.status = o;
   o = align_up(o + sizeof(int));
   L.perm = o;
-  o = align_up(o + moe::perm_scratch_bytes(d.T, d.E, d.k));
+  o = align_up(o + moe::perm_scratch_bytes(d.T, EG, ks));
   L.stage_total = o;
   L.ids = o;
-  o = align_up(o + n * sizeof(int32_t));
+  o = align_up(o + nr * sizeof(int32_t));
   L.w = o;
-  o = align_up(o + n * sizeof(float));
+  o = align_up(o + nr * sizeof(float));
   L.counts = o;
-  o = align_up(o + (size_t)d.E * sizeof(int32_t));
+  o = align_up(o + (size_t)EG * sizeof(int32_t));
   L.offsets = o;
-  o = align_up(o + (size_t)(d.E + 1) * sizeof(int32_t));
+  o = align_up(o + (size_t)(EG + 1) * sizeof(int32_t));
   L.ready = o;
-  o = align_up(o + (size_t)d.E * sizeof(int32_t));
+  o = align_up(o + (size_t)EG * sizeof(int32_t));
   L.sorted_token = o;
   o = align_up(o + n * sizeof(int32_t));
   L.inv_perm = o;
@@ -60,6 +65,10 @@ Layout layout_of(const moe_dims& d) {
   L.total = o;
   return L;
 }
+
+// The workspace the layer entry points ask for covers the shared-expert
+// layout (a superset) whenever a shared expert is possible.
+Layout layout_of(const moe_dims& d) { return layout_of(d, shared_possible(d)); }
 
 int check_dims(const moe_dims& d) {
   if (d.T < 0 || d.H <= 0 || d.I <= 0 || d.E < 1 || d.k < 1) return MOE_ERR_INVALID_ARG;
@@ -127,7 +136,7 @@ int moe_layer_kernel_launches(moe_dims d) {
   if (d.T == 0) return 0;
   const bool gemm_gathers = moe::gemm_gathers_rows(d.T * d.k, d.E, d.H);
   const bool fused = moe::gemm_fuses_layer(d.T * d.k, d.E, d.H, d.I);
-  return moe::route_group_launches(d.T, d.E, d.k) + (gemm_gathers ? 0 : 1) + (fused ? 1 : 2) + 1;
+  return moe::route_group_launches(d.T, d.E, d.k, false) + (gemm_gathers ? 0 : 1) + (fused ? 1 : 2) + 1;
 }
 
 int moe_layer_projections_fused(moe_dims d) {
@@ -138,6 +147,16 @@ int moe_layer_projections_fused(moe_dims d) {
 size_t moe_stage_workspace_bytes(moe_dims d) {
   if (check_dims(d) != MOE_OK) return 0;
   return layout_of(d).stage_total;
+}
+
+int moe_router_logits(const uint16_t* x, const uint16_t* router_weight, const float* router_bias, moe_dims d,
+                      float* logits, void* stream) {
+  MOE_TRY(check_dims(d));
+  if (d.T == 0) return MOE_OK;
+  MOE_TRY(check_ptrs({x, router_weight, logits}));
+  if (router_bias != nullptr && (reinterpret_cast<uintptr_t>(router_bias) & 3u) != 0) return MOE_ERR_MISALIGNED;
+  return cuda_status(
+      moe::launch_router_logits(x, router_weight, router_bias, d.T, d.H, d.E, logits, as_stream(stream)));
 }
 
 int moe_route_topk(const float* logits, moe_dims d, int32_t* topk_ids, float* topk_w, void* stream) {
@@ -213,7 +232,7 @@ int moe_unpermute_combine(const float* y_perm, const int32_t* inv_perm, const fl
   MOE_TRY(check_dims(d));
   if (d.T == 0) return MOE_OK;
   MOE_TRY(check_ptrs({y_perm, inv_perm, topk_w, out}));
-  return cuda_status(moe::launch_combine(y_perm, inv_perm, topk_w, d.T, d.H, d.k, out, as_stream(stream)));
+  return cuda_status(moe::launch_combine(y_perm, inv_perm, topk_w, d.T, d.H, d.k, false, out, as_stream(stream)));
 }
 
 }  // extern "C"
@@ -221,16 +240,24 @@ int moe_unpermute_combine(const float* y_perm, const int32_t* inv_perm, const fl
 namespace {
 
 // The layer, optionally recording ev[0..5] around the five stages
-// (ev[i] before stage i, ev[5] after the last).
-int layer_forward_impl(const uint16_t* x, const float* logits, moe_w4 w_gate_up, moe_w4 w_down, moe_dims d,
-                       uint16_t* out, int32_t* topk_ids, float* topk_w, void* ws, size_t ws_bytes, void* stream,
-                       void* const* ev) {
+// (ev[i] before stage i, ev[5] after the last).  shared_gu / shared_dn: the
+// shared expert's projections (both or neither), packed as one-expert
+// matrices of the routed experts' shapes.
+int layer_forward_impl(const uint16_t* x, const float* logits, moe_w4 w_gate_up, moe_w4 w_down,
+                       const moe_w4* shared_gu, const moe_w4* shared_dn, moe_dims d, uint16_t* out,
+                       int32_t* topk_ids, float* topk_w, void* ws, size_t ws_bytes, void* stream, void* const* ev) {
   MOE_TRY(check_dims(d));
   if (d.T == 0) return MOE_OK;
   MOE_TRY(check_ptrs({x, logits, w_gate_up.packed, w_gate_up.global_scale, w_down.packed, w_down.global_scale, out,
                       ws}));
   if ((topk_ids != nullptr && !aligned16(topk_ids)) || (topk_w != nullptr && !aligned16(topk_w)))
     return MOE_ERR_MISALIGNED;
+  const bool shared = shared_gu != nullptr;
+  if (shared) {
+    if (shared_dn == nullptr) return MOE_ERR_INVALID_ARG;
+    if (!shared_possible(d) || d.k >= 32) return MOE_ERR_UNSUPPORTED_SHAPE;  // E + 1 groups, k + 1 slots
+    MOE_TRY(check_ptrs({shared_gu->packed, shared_gu->global_scale, shared_dn->packed, shared_dn->global_scale}));
+  }
   const Layout L = layout_of(d);
   if (ws_bytes < L.total) return MOE_ERR_WORKSPACE_TOO_SMALL;
   uint8_t* w = static_cast<uint8_t*>(ws);
@@ -248,27 +275,33 @@ int layer_forward_impl(const uint16_t* x, const float* logits, moe_w4 w_gate_up,
   uint16_t* xp = reinterpret_cast<uint16_t*>(w + L.x_perm);
   uint16_t* h = reinterpret_cast<uint16_t*>(w + L.h);
   float* y = reinterpret_cast<float*>(w + L.y);
+  // grouped view: with a shared expert every token has k + 1 rows and the
+  // shared expert is group E
+  const int rows = d.T * (d.k + (shared ? 1 : 0));
+  const int EG = d.E + (shared ? 1 : 0);
   MOE_TRY(mark(0));
   int32_t* ready = reinterpret_cast<int32_t*>(w + L.ready);
-  const bool fused = moe::gemm_fuses_layer(d.T * d.k, d.E, d.H, d.I);
-  MOE_TRY(cuda_status(moe::launch_route_group(logits, d.T, d.E, d.k, ids, wts, counts, offs, sorted, inv,
+  const bool fused = moe::gemm_fuses_layer(rows, EG, d.H, d.I);
+  MOE_TRY(cuda_status(moe::launch_route_group(logits, d.T, d.E, d.k, shared, ids, wts, counts, offs, sorted, inv,
                                               reinterpret_cast<int32_t*>(w + L.perm), fused ? ready : nullptr, s)));
   MOE_TRY(mark(1));
   // the narrow-tile GEMM gathers the rows of x itself; the wide one reads x_perm
-  const bool gemm_gathers = moe::gemm_gathers_rows(d.T * d.k, d.E, d.H);
-  if (!gemm_gathers) MOE_TRY(cuda_status(moe::launch_gather(x, sorted, d.T * d.k, d.H, xp, s)));
+  const bool gemm_gathers = moe::gemm_gathers_rows(rows, EG, d.H);
+  if (!gemm_gathers) MOE_TRY(cuda_status(moe::launch_gather(x, sorted, rows, d.H, xp, s)));
   MOE_TRY(mark(2));
   moe::GemmArgs a{};
   a.offsets = offs;
   a.status = reinterpret_cast<int*>(w + L.status);
-  a.rows = d.T * d.k;
-  a.E = d.E;
+  a.rows = rows;
+  a.E = EG;
   a.T = d.T;
   a.k = d.k;
   a.act = gemm_gathers ? x : xp;
   a.gather_rows = gemm_gathers ? sorted : nullptr;
   a.packed = static_cast<const uint8_t*>(w_gate_up.packed);
   a.gscale = w_gate_up.global_scale;
+  a.shared_packed = shared ? static_cast<const uint8_t*>(shared_gu->packed) : nullptr;
+  a.shared_gscale = shared ? shared_gu->global_scale : nullptr;
   a.out = h;
   a.N = 2 * d.I;
   a.K = d.H;
@@ -278,6 +311,8 @@ int layer_forward_impl(const uint16_t* x, const float* logits, moe_w4 w_gate_up,
   b.gather_rows = nullptr;
   b.packed = static_cast<const uint8_t*>(w_down.packed);
   b.gscale = w_down.global_scale;
+  b.shared_packed = shared ? static_cast<const uint8_t*>(shared_dn->packed) : nullptr;
+  b.shared_gscale = shared ? shared_dn->global_scale : nullptr;
   b.out = y;
   b.N = d.H;
   b.K = d.I;
@@ -292,7 +327,7 @@ int layer_forward_impl(const uint16_t* x, const float* logits, moe_w4 w_gate_up,
     MOE_TRY(cuda_status(run_gemm(1, b, s)));
   }
   MOE_TRY(mark(4));
-  MOE_TRY(cuda_status(moe::launch_combine(y, inv, wts, d.T, d.H, d.k, out, s)));
+  MOE_TRY(cuda_status(moe::launch_combine(y, inv, wts, d.T, d.H, d.k, shared, out, s)));
   return mark(5);
 }
 
@@ -302,14 +337,56 @@ extern "C" {
 
 int moe_layer_forward(const uint16_t* x, const float* logits, moe_w4 w_gate_up, moe_w4 w_down, moe_dims d,
                       uint16_t* out, int32_t* topk_ids, float* topk_w, void* ws, size_t ws_bytes, void* stream) {
-  return layer_forward_impl(x, logits, w_gate_up, w_down, d, out, topk_ids, topk_w, ws, ws_bytes, stream, nullptr);
+  return layer_forward_impl(x, logits, w_gate_up, w_down, nullptr, nullptr, d, out, topk_ids, topk_w, ws, ws_bytes,
+                            stream, nullptr);
 }
 
 int moe_layer_forward_profiled(const uint16_t* x, const float* logits, moe_w4 w_gate_up, moe_w4 w_down, moe_dims d,
                                uint16_t* out, int32_t* topk_ids, float* topk_w, void* ws, size_t ws_bytes,
                                void* stream, void* const* stage_events) {
-  return layer_forward_impl(x, logits, w_gate_up, w_down, d, out, topk_ids, topk_w, ws, ws_bytes, stream,
-                            stage_events);
+  return layer_forward_impl(x, logits, w_gate_up, w_down, nullptr, nullptr, d, out, topk_ids, topk_w, ws, ws_bytes,
+                            stream, stage_events);
+}
+
+int moe_layer_forward_router(const uint16_t* x, const uint16_t* router_weight, const float* router_bias,
+                             moe_w4 w_gate_up, moe_w4 w_down, moe_dims d, uint16_t* out, float* logits_out,
+                             int32_t* topk_ids, float* topk_w, void* ws, size_t ws_bytes, void* stream) {
+  MOE_TRY(check_dims(d));
+  if (d.T == 0) return MOE_OK;
+  MOE_TRY(check_ptrs({x, router_weight, ws}));
+  if (router_bias != nullptr && (reinterpret_cast<uintptr_t>(router_bias) & 3u) != 0) return MOE_ERR_MISALIGNED;
+  if (logits_out != nullptr && !aligned16(logits_out)) return MOE_ERR_MISALIGNED;
+  const Layout L = layout_of(d);
+  if (ws_bytes < L.total) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  float* logits = logits_out != nullptr ? logits_out : reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + L.hlogits);
+  MOE_TRY(cuda_status(
+      moe::launch_router_logits(x, router_weight, router_bias, d.T, d.H, d.E, logits, as_stream(stream))));
+  return layer_forward_impl(x, logits, w_gate_up, w_down, nullptr, nullptr, d, out, topk_ids, topk_w, ws, ws_bytes,
+                            stream, nullptr);
+}
+
+int moe_layer_forward_shared(const uint16_t* x, const float* logits, const uint16_t* router_weight,
+                             const float* router_bias, moe_w4 w_gate_up, moe_w4 w_down, moe_w4 shared_gate_up,
+                             moe_w4 shared_down, moe_dims d, uint16_t* out, float* logits_out, int32_t* topk_ids,
+                             float* topk_w, void* ws, size_t ws_bytes, void* stream) {
+  MOE_TRY(check_dims(d));
+  if (d.T == 0) return MOE_OK;
+  if ((logits == nullptr) == (router_weight == nullptr)) return MOE_ERR_INVALID_ARG;  // exactly one source
+  MOE_TRY(check_ptrs({x, ws}));
+  const Layout L = layout_of(d);
+  if (ws_bytes < L.total) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  if (router_weight != nullptr) {
+    if (!aligned16(router_weight)) return MOE_ERR_MISALIGNED;
+    if (router_bias != nullptr && (reinterpret_cast<uintptr_t>(router_bias) & 3u) != 0) return MOE_ERR_MISALIGNED;
+    if (logits_out != nullptr && !aligned16(logits_out)) return MOE_ERR_MISALIGNED;
+    float* lg = logits_out != nullptr ? logits_out
+                                      : reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + L.hlogits);
+    MOE_TRY(cuda_status(
+        moe::launch_router_logits(x, router_weight, router_bias, d.T, d.H, d.E, lg, as_stream(stream))));
+    logits = lg;
+  }
+  return layer_forward_impl(x, logits, w_gate_up, w_down, &shared_gate_up, &shared_down, d, out, topk_ids, topk_w, ws,
+                            ws_bytes, stream, nullptr);
 }
 
 int moe_layer_forward_host(const uint16_t* host_x, const float* host_logits, moe_w4 w_gate_up, moe_w4 w_down,

@@ -140,6 +140,15 @@ cudaError_t launch_route_topk(const float* logits, int T, int E, int k, int32_t*
 // independent of scheduling.
 constexpr int kPermChunk = 1024;
 
+// The grouped view of the (token, slot) pairs: ks slots per token, the first
+// k routed (ids [T][k]) and, when ks == k + 1, a last slot for the shared
+// expert, which takes index E_r (after the E_r routed experts).
+__device__ __forceinline__ int pair_expert(const int32_t* ids, int g, int k, int ks, int E_r) {
+  if (ks == k) return ids[g];
+  const int t = g / ks, j = g - t * ks;
+  return j < k ? ids[t * k + j] : E_r;
+}
+
 // The rank kernels run 32 warps (kPermChunk threads).  Rank table: uint16
 // [E][32], expert-major, so a warp scans one expert's 32 per-warp counts with
 // lane = warp index.
@@ -176,7 +185,7 @@ __device__ __forceinline__ void block_rank_scan(uint16_t* tab, int32_t* cnt, int
   }
 }
 
-__global__ void __launch_bounds__(256) perm_hist_kernel(const int32_t* __restrict__ ids, int n, int E,
+__global__ void __launch_bounds__(256) perm_hist_kernel(const int32_t* __restrict__ ids, int n, int E, int k, int ks,
                                                         int32_t* __restrict__ chunk_counts) {
   extern __shared__ int32_t hist[];
   for (int e = threadIdx.x; e < E; e += blockDim.x) hist[e] = 0;
@@ -186,7 +195,7 @@ __global__ void __launch_bounds__(256) perm_hist_kernel(const int32_t* __restric
   const int base = blockIdx.x * kPermChunk;
   for (int i = threadIdx.x; i < kPermChunk; i += blockDim.x) {
     const int g = base + i;
-    if (g < n) atomicAdd(&hist[ids[g]], 1);
+    if (g < n) atomicAdd(&hist[pair_expert(ids, g, k, ks, E - (ks - k))], 1);
   }
   __syncthreads();
   for (int e = threadIdx.x; e < E; e += blockDim.x) chunk_counts[(size_t)blockIdx.x * E + e] = hist[e];
@@ -250,6 +259,7 @@ static size_t scatter_smem_bytes(int E) { return (size_t)E * sizeof(int32_t) + r
 
 // One block of kPermChunk threads per chunk; thread i owns pair base + i.
 __global__ void __launch_bounds__(kPermChunk) perm_scatter_kernel(const int32_t* __restrict__ ids, int n, int E, int k,
+                                                                  int ks,
                                                                   const int32_t* __restrict__ chunk_base,
                                                                   int32_t* __restrict__ sorted_token,
                                                                   int32_t* __restrict__ inv_perm) {
@@ -263,7 +273,7 @@ __global__ void __launch_bounds__(kPermChunk) perm_scatter_kernel(const int32_t*
   pdl_trigger();
   for (int e = threadIdx.x; e < E; e += blockDim.x) base[e] = chunk_base[(size_t)blockIdx.x * E + e];
   const bool valid = g < n;
-  const int e = valid ? ids[g] : 0;
+  const int e = valid ? pair_expert(ids, g, k, ks, E - (ks - k)) : 0;
   __syncthreads();
   const int rank = warp_rank_and_count(e, valid, tab);
   __syncthreads();
@@ -271,7 +281,7 @@ __global__ void __launch_bounds__(kPermChunk) perm_scatter_kernel(const int32_t*
   __syncthreads();
   if (valid) {
     const int pos = base[e] + tab[e * kRankWarps + warp] + rank;
-    sorted_token[pos] = g / k;
+    sorted_token[pos] = g / ks;
     inv_perm[g] = pos;
   }
 }
@@ -282,17 +292,19 @@ __global__ void __launch_bounds__(kPermChunk) perm_scatter_kernel(const int32_t*
 // scans over warps and over experts, and the stable scatter, in one launch.
 template <int NV>
 __global__ void __launch_bounds__(kPermChunk) route_permute_small_kernel(
-    const float* __restrict__ logits, int T, int E, int k, int32_t* __restrict__ ids, float* __restrict__ wts,
+    const float* __restrict__ logits, int T, int E, int k, int ks, int32_t* __restrict__ ids, float* __restrict__ wts,
     int32_t* __restrict__ counts, int32_t* __restrict__ offsets, int32_t* __restrict__ sorted_token,
     int32_t* __restrict__ inv_perm, int32_t* __restrict__ zero_e) {
+  // E routed experts; the grouping sees EG = E + (ks - k) (the shared expert last)
+  const int EG = E + (ks - k);
   extern __shared__ int32_t smem_i[];
-  int32_t* base = smem_i;                                  // [E] counts, then offsets
-  int32_t* s_ids = smem_i + E;                             // [kPermChunk]
-  uint16_t* tab = reinterpret_cast<uint16_t*>(smem_i + E + kPermChunk);
+  int32_t* base = smem_i;                                  // [EG] counts, then offsets
+  int32_t* s_ids = smem_i + EG;                            // [kPermChunk]
+  uint16_t* tab = reinterpret_cast<uint16_t*>(smem_i + EG + kPermChunk);
   __shared__ int32_t warp_tot[32];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int n = T * k;
-  for (int x = tid; x < E * kRankWarps; x += blockDim.x) tab[x] = 0;
+  const int n = T * ks;
+  for (int x = tid; x < EG * kRankWarps; x += blockDim.x) tab[x] = 0;
   pdl_wait();
   pdl_trigger();
   if (logits != nullptr) {
@@ -301,35 +313,36 @@ __global__ void __launch_bounds__(kPermChunk) route_permute_small_kernel(
       float w;
       route_token<NV>(logits + (size_t)t * E, E, k, id, w);
       if (lane < k) {
-        s_ids[t * k + lane] = id;
+        s_ids[t * ks + lane] = id;
         ids[(size_t)t * k + lane] = id;
         wts[(size_t)t * k + lane] = w;
       }
+      if (ks > k && lane == k) s_ids[t * ks + k] = E;
     }
   } else {
-    for (int i = tid; i < n; i += blockDim.x) s_ids[i] = ids[i];
+    for (int i = tid; i < n; i += blockDim.x) s_ids[i] = pair_expert(ids, i, k, ks, E);
   }
   __syncthreads();
   const bool valid = tid < n;
   const int e = valid ? s_ids[tid] : 0;
   const int rank = warp_rank_and_count(e, valid, tab);
   __syncthreads();
-  block_rank_scan(tab, base, E);  // base[e] = count of e
+  block_rank_scan(tab, base, EG);  // base[e] = count of e
   __syncthreads();
-  const int32_t c = tid < E ? base[tid] : 0;
+  const int32_t c = tid < EG ? base[tid] : 0;
   int32_t total;
   const int32_t excl = block_exclusive_scan(c, warp_tot, &total);
-  if (tid < E) {
+  if (tid < EG) {
     counts[tid] = c;
     offsets[tid] = excl;
     base[tid] = excl;
-    if (tid == E - 1) offsets[E] = excl + c;
+    if (tid == EG - 1) offsets[EG] = excl + c;
     if (zero_e != nullptr) zero_e[tid] = 0;
   }
   __syncthreads();
   if (valid) {
     const int pos = base[e] + tab[e * kRankWarps + warp] + rank;
-    sorted_token[pos] = tid / k;
+    sorted_token[pos] = tid / ks;
     inv_perm[tid] = pos;
   }
 }
@@ -366,30 +379,34 @@ cudaError_t launch_gather(const uint16_t* x, const int32_t* sorted_token, int n,
   return launch_pdl(perm_gather_kernel, dim3((unsigned)blocks), dim3(256), 0, s, x, sorted_token, nvec, vpr, x_perm);
 }
 
+// E routed experts, k routed slots, ks slots per token in the grouped view
+// (k + 1 with the shared expert, which groups as expert E).
 template <int NV>
-static cudaError_t launch_small(const float* logits, int T, int E, int k, int32_t* ids, float* w, int32_t* counts,
-                                int32_t* offsets, int32_t* sorted_token, int32_t* inv_perm, int32_t* zero_e,
-                                cudaStream_t s) {
-  const size_t smem = small_smem_bytes(E);
+static cudaError_t launch_small(const float* logits, int T, int E, int k, int ks, int32_t* ids, float* w,
+                                int32_t* counts, int32_t* offsets, int32_t* sorted_token, int32_t* inv_perm,
+                                int32_t* zero_e, cudaStream_t s) {
+  const size_t smem = small_smem_bytes(E + (ks - k));
   auto kern = route_permute_small_kernel<NV>;
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (err != cudaSuccess) return err;
-  return launch_pdl(kern, dim3(1), dim3(kPermChunk), smem, s, logits, T, E, k, ids, w, counts, offsets, sorted_token,
-                    inv_perm, zero_e);
+  return launch_pdl(kern, dim3(1), dim3(kPermChunk), smem, s, logits, T, E, k, ks, ids, w, counts, offsets,
+                    sorted_token, inv_perm, zero_e);
 }
 
-static cudaError_t launch_chunked(const int32_t* ids, int n, int E, int k, int32_t* counts, int32_t* offsets,
+static cudaError_t launch_chunked(const int32_t* ids, int T, int E, int k, int ks, int32_t* counts, int32_t* offsets,
                                   int32_t* sorted_token, int32_t* inv_perm, int32_t* scratch, int32_t* zero_e,
                                   cudaStream_t s) {
+  const int n = T * ks, EG = E + (ks - k);
   const int nchunks = (n + kPermChunk - 1) / kPermChunk;
-  cudaError_t err = launch_pdl(perm_hist_kernel, dim3(nchunks), dim3(256), E * sizeof(int32_t), s, ids, n, E, scratch);
+  cudaError_t err =
+      launch_pdl(perm_hist_kernel, dim3(nchunks), dim3(256), EG * sizeof(int32_t), s, ids, n, EG, k, ks, scratch);
   if (err != cudaSuccess) return err;
-  err = launch_pdl(perm_scan_kernel, dim3(1), dim3(1024), 0, s, scratch, nchunks, E, counts, offsets, zero_e);
+  err = launch_pdl(perm_scan_kernel, dim3(1), dim3(1024), 0, s, scratch, nchunks, EG, counts, offsets, zero_e);
   if (err != cudaSuccess) return err;
-  const size_t smem = scatter_smem_bytes(E);
+  const size_t smem = scatter_smem_bytes(EG);
   err = cudaFuncSetAttribute(perm_scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (err != cudaSuccess) return err;
-  return launch_pdl(perm_scatter_kernel, dim3(nchunks), dim3(kPermChunk), smem, s, ids, n, E, k,
+  return launch_pdl(perm_scatter_kernel, dim3(nchunks), dim3(kPermChunk), smem, s, ids, n, EG, k, ks,
                     (const int32_t*)scratch, sorted_token, inv_perm);
 }
 
@@ -398,9 +415,9 @@ cudaError_t launch_permute(const int32_t* ids, const uint16_t* x, int T, int H, 
                            int32_t* scratch, cudaStream_t s) {
   const int n = T * k;
   cudaError_t err = (n <= kPermChunk)
-                        ? launch_small<1>(nullptr, T, E, k, const_cast<int32_t*>(ids), nullptr, counts, offsets,
+                        ? launch_small<1>(nullptr, T, E, k, k, const_cast<int32_t*>(ids), nullptr, counts, offsets,
                                           sorted_token, inv_perm, nullptr, s)
-                        : launch_chunked(ids, n, E, k, counts, offsets, sorted_token, inv_perm, scratch, nullptr, s);
+                        : launch_chunked(ids, T, E, k, k, counts, offsets, sorted_token, inv_perm, scratch, nullptr, s);
   if (err != cudaSuccess) return err;
   return launch_gather(x, sorted_token, n, H, x_perm, s);
 }
@@ -409,49 +426,51 @@ cudaError_t launch_permute(const int32_t* ids, const uint16_t* x, int T, int H, 
 // small enough for one SM to read quickly (T*E floats, 128 KiB).
 constexpr long long kFusedRouteLogits = 32768;
 
-int route_group_launches(int T, int E, int k) {
-  const int n = T * k;
+int route_group_launches(int T, int E, int k, bool shared) {
+  const int n = T * (k + (shared ? 1 : 0));
   if (n <= kPermChunk && (long long)T * E <= kFusedRouteLogits) return 1;
   return n <= kPermChunk ? 2 : 4;
 }
 
-cudaError_t launch_route_group(const float* logits, int T, int E, int k, int32_t* ids, float* w, int32_t* counts,
-                               int32_t* offsets, int32_t* sorted_token, int32_t* inv_perm, int32_t* scratch,
-                               int32_t* zero_e, cudaStream_t s) {
-  const int n = T * k;
+cudaError_t launch_route_group(const float* logits, int T, int E, int k, bool shared, int32_t* ids, float* w,
+                               int32_t* counts, int32_t* offsets, int32_t* sorted_token, int32_t* inv_perm,
+                               int32_t* scratch, int32_t* zero_e, cudaStream_t s) {
+  const int ks = k + (shared ? 1 : 0);
+  const int n = T * ks;
   cudaError_t err;
   if (n <= kPermChunk && (long long)T * E <= kFusedRouteLogits) {
-    MOE_DISPATCH_NV(route_nv(E), err = (launch_small<NV>(logits, T, E, k, ids, w, counts, offsets, sorted_token,
+    MOE_DISPATCH_NV(route_nv(E), err = (launch_small<NV>(logits, T, E, k, ks, ids, w, counts, offsets, sorted_token,
                                                          inv_perm, zero_e, s)));
     return err;
   }
   err = launch_route_topk(logits, T, E, k, ids, w, s);
   if (err != cudaSuccess) return err;
   if (n <= kPermChunk)
-    return launch_small<1>(nullptr, T, E, k, ids, nullptr, counts, offsets, sorted_token, inv_perm, zero_e, s);
-  return launch_chunked(ids, n, E, k, counts, offsets, sorted_token, inv_perm, scratch, zero_e, s);
+    return launch_small<1>(nullptr, T, E, k, ks, ids, nullptr, counts, offsets, sorted_token, inv_perm, zero_e, s);
+  return launch_chunked(ids, T, E, k, ks, counts, offsets, sorted_token, inv_perm, scratch, zero_e, s);
 }
 
 // ------------------------------------------------------------------ combine
-// out[t, c] = bf16_rne(sum_j w[t,j] * y[inv[t*k+j], c]) with the fp32 sum in
-// ascending j.  A block of kCombineThreads takes 4 * kCombineThreads columns
-// of one token; the token's k rows and weights are staged in shared memory
-// first so the k row loads of a thread are independent of each other.
+// out[t, c] = bf16_rne(sum_j w[t,j] * y[inv[t*ks+j], c]) with the fp32 sum in
+// ascending j over the k routed slots, then, with a shared expert (ks == k +
+// 1), plus y[inv[t*ks+k], c] (weight 1).  A block of kCombineThreads takes
+// 4 * kCombineThreads columns of one token; the token's rows and weights are
+// staged in shared memory first so the row loads of a thread are independent.
 constexpr int kCombineThreads = 128;
 
 __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const float* __restrict__ y,
                                                                   const int32_t* __restrict__ inv,
                                                                   const float* __restrict__ w, int T, int H, int k,
-                                                                  uint16_t* __restrict__ out) {
-  __shared__ int32_t s_row[32];
-  __shared__ float s_w[32];
+                                                                  int ks, uint16_t* __restrict__ out) {
+  __shared__ int32_t s_row[33];
+  __shared__ float s_w[33];
   const int t = blockIdx.y;
   const int c4 = blockIdx.x * blockDim.x + threadIdx.x;
   pdl_wait();
   pdl_trigger();
-  if (threadIdx.x < k) {
-    s_row[threadIdx.x] = inv[(size_t)t * k + threadIdx.x];
-    s_w[threadIdx.x] = w[(size_t)t * k + threadIdx.x];
+  if (threadIdx.x < ks) {
+    s_row[threadIdx.x] = inv[(size_t)t * ks + threadIdx.x];
+    s_w[threadIdx.x] = threadIdx.x < k ? w[(size_t)t * k + threadIdx.x] : 1.0f;
   }
   __syncthreads();
   if (c4 * 4 >= H) return;
@@ -465,6 +484,13 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const float* _
     acc.z = fmaf(wj, v.z, acc.z);
     acc.w = fmaf(wj, v.w, acc.w);
   }
+  if (ks > k) {
+    const float4 v = reinterpret_cast<const float4*>(y + (size_t)s_row[k] * H)[c4];
+    acc.x += v.x;
+    acc.y += v.y;
+    acc.z += v.z;
+    acc.w += v.w;
+  }
   __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y);
   __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z, acc.w);
   uint2 pk;
@@ -473,11 +499,11 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const float* _
   reinterpret_cast<uint2*>(out + (size_t)t * H)[c4] = pk;
 }
 
-cudaError_t launch_combine(const float* y, const int32_t* inv, const float* w, int T, int H, int k, uint16_t* out,
-                           cudaStream_t s) {
+cudaError_t launch_combine(const float* y, const int32_t* inv, const float* w, int T, int H, int k, bool shared,
+                           uint16_t* out, cudaStream_t s) {
   if (T == 0) return cudaSuccess;
   dim3 grid((H / 4 + kCombineThreads - 1) / kCombineThreads, T);
-  return launch_pdl(combine_kernel, grid, dim3(kCombineThreads), 0, s, y, inv, w, T, H, k, out);
+  return launch_pdl(combine_kernel, grid, dim3(kCombineThreads), 0, s, y, inv, w, T, H, k, k + (shared ? 1 : 0), out);
 }
 
 }  // namespace moe

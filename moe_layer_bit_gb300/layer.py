@@ -45,11 +45,17 @@ def pack_projection(codes: torch.Tensor, scales: torch.Tensor, global_scale: tor
 class MoELayer:
     """W4A16 NVFP4 MoE FFN layer for up to T_max tokens per call."""
 
-    def __init__(self, gu, dn, H: int, I: int, E: int, k: int, T_max: int, device="cuda"):
+    def __init__(self, gu, dn, H: int, I: int, E: int, k: int, T_max: int, device="cuda", shared=None):
+        """shared: optional (gate_up, down) natural-layout weights of a shared expert
+        (one expert, the routed experts' H and I), used by forward_shared."""
         self.H, self.I, self.E, self.k, self.T_max = H, I, E, k, T_max
         self.device = torch.device(device)
         self.w_gate_up = pack_projection(*gu, _lib.MOE_PROJ_GATE_UP, device)
         self.w_down = pack_projection(*dn, _lib.MOE_PROJ_DOWN, device)
+        self.shared = None
+        if shared is not None:
+            self.shared = (pack_projection(*shared[0], _lib.MOE_PROJ_GATE_UP, device),
+                           pack_projection(*shared[1], _lib.MOE_PROJ_DOWN, device))
         d = _lib.dims(T_max, H, I, E, k)
         self.ws_bytes = _lib.moe_workspace_bytes(d)
         if self.ws_bytes == 0:
@@ -68,6 +74,32 @@ class MoELayer:
             out = torch.empty(T, self.H, dtype=torch.bfloat16, device=self.device)
         _lib.moe_layer_forward(x, logits, self.w_gate_up.abi, self.w_down.abi, self.dims(T), out, topk_ids, topk_w,
                                self.ws, self.ws_bytes, stream)
+        return out
+
+    def forward_router(self, x: torch.Tensor, router_weight: torch.Tensor, router_bias: torch.Tensor | None = None,
+                       out: torch.Tensor | None = None, logits_out: torch.Tensor | None = None,
+                       topk_ids: torch.Tensor | None = None, topk_w: torch.Tensor | None = None, stream=None):
+        """The layer with its gate logits computed from bf16 router weights [E][H] (+ fp32 bias [E])."""
+        T = x.shape[0]
+        if out is None:
+            out = torch.empty(T, self.H, dtype=torch.bfloat16, device=self.device)
+        _lib.moe_layer_forward_router(x, router_weight, router_bias, self.w_gate_up.abi, self.w_down.abi, self.dims(T),
+                                      out, logits_out, topk_ids, topk_w, self.ws, self.ws_bytes, stream)
+        return out
+
+    def forward_shared(self, x: torch.Tensor, logits: torch.Tensor | None = None,
+                       router_weight: torch.Tensor | None = None, router_bias: torch.Tensor | None = None,
+                       out: torch.Tensor | None = None, logits_out: torch.Tensor | None = None,
+                       topk_ids: torch.Tensor | None = None, topk_w: torch.Tensor | None = None, stream=None):
+        """The layer plus the shared expert; gate logits given, or computed from router weights."""
+        if self.shared is None:
+            raise ValueError("MoELayer was built without shared expert weights")
+        T = x.shape[0]
+        if out is None:
+            out = torch.empty(T, self.H, dtype=torch.bfloat16, device=self.device)
+        _lib.moe_layer_forward_shared(x, logits, router_weight, router_bias, self.w_gate_up.abi, self.w_down.abi,
+                                      self.shared[0].abi, self.shared[1].abi, self.dims(T), out, logits_out,
+                                      topk_ids, topk_w, self.ws, self.ws_bytes, stream)
         return out
 
     def forward_host(self, x_host: torch.Tensor, logits_host: torch.Tensor, out_host: torch.Tensor, stream=None):

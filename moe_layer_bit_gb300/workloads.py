@@ -156,6 +156,26 @@ def generate(wl: Workload, seed: int | None = None, with_weights: bool = True):
     return out
 
 
+def router_weights(wl: Workload, seed: int | None = None, bias: bool = True):
+    """bf16 router weights Wr [E,H] ~ N(0, 1/H) (variance 1/H) and an fp32 bias
+    [E] ~ N(0, 0.1^2) (or None), from a generator of their own (seed + 7777),
+    for the layer that computes its own gate logits."""
+    seed = (wl.seed if seed is None else seed) + 7777
+    gen = torch.Generator().manual_seed(seed)
+    Wr = (torch.randn(wl.E, wl.H, generator=gen, dtype=torch.float32) * (1.0 / math.sqrt(wl.H))).to(torch.bfloat16)
+    b = (torch.randn(wl.E, generator=gen, dtype=torch.float32) * 0.1) if bias else None
+    return Wr.contiguous(), b
+
+
+def shared_expert(wl: Workload, seed: int | None = None):
+    """NVFP4 weights of one shared expert with the routed experts' H and I, from a
+    generator of their own (seed + 4242): (gu, dn) in the layout of generate()'s,
+    with E = 1."""
+    seed = (wl.seed if seed is None else seed) + 4242
+    gen = torch.Generator().manual_seed(seed)
+    return _quantize_experts(gen, 1, 2 * wl.I, wl.H), _quantize_experts(gen, 1, wl.H, wl.I)
+
+
 def generate_dims(T, H, I, E, k, seed, router="normal"):
     """Same recipe for an arbitrary shape (used by edge-case tests)."""
     return generate(Workload(f"custom_T{T}_H{H}_I{I}_E{E}_k{k}", T, H, I, E, k, router, seed))

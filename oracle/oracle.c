@@ -151,6 +151,68 @@ void oracle_decode_row(const uint8_t *codes, const uint8_t *scales, const float 
     }
 }
 
+/* ------------------------------------------------------------ router logits */
+
+static float bf16_to_float(uint16_t b)
+{
+    uint32_t u = (uint32_t)b << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return f;
+}
+
+/* The gate logits of the Atlas article's MoE layer (section "KV Cache量化、MTP
+ * 推测解码和调试工具链": gate input -> gate logits -> expert IDs), exactly:
+ * logits[t][e] = sum_h x[t][h] * Wr[e][h] (+ bias[e]) in fp64, rounded once to
+ * fp32.  x bf16 [T][H], Wr bf16 [E][H], bias fp32 [E] or NULL. */
+void oracle_router_logits_exact(const uint16_t *x, const uint16_t *wr, const float *bias, int T, int H, int E,
+                                double *logits)
+{
+    for (int t = 0; t < T; ++t)
+        for (int e = 0; e < E; ++e) {
+            double acc = 0.0;
+            for (int h = 0; h < H; ++h)
+                acc += (double)bf16_to_float(x[(size_t)t * H + h]) * (double)bf16_to_float(wr[(size_t)e * H + h]);
+            if (bias != NULL) acc += (double)bias[e];
+            logits[(size_t)t * E + e] = acc;
+        }
+}
+
+/* The same logits in fp32 with the library's fixed reduction order, so that
+ * routing on them is reproducible bit for bit:
+ *  - the hidden dimension is cut into 8-element chunks; part l (l = 0..31)
+ *    takes chunks l, l+32, l+64, ... and accumulates x*w over its elements in
+ *    ascending h with a fused multiply-add, starting from 0;
+ *  - the 32 parts are combined in five rounds; in round r (strides 16, 8, 4,
+ *    2, 1) every part l becomes part l + part (l XOR stride); the result is
+ *    part 0 (an fp32 add is commutative, so every part ends equal);
+ *  - the bias, if any, is added last. */
+void oracle_router_logits(const uint16_t *x, const uint16_t *wr, const float *bias, int T, int H, int E,
+                          float *logits)
+{
+    float part[32], next[32];
+    for (int t = 0; t < T; ++t)
+        for (int e = 0; e < E; ++e) {
+            const uint16_t *xr = x + (size_t)t * H, *wrow = wr + (size_t)e * H;
+            for (int l = 0; l < 32; ++l) {
+                float acc = 0.0f;
+                for (int chunk = l; chunk * 8 < H; chunk += 32)
+                    for (int c = 0; c < 8; ++c) {
+                        int h = chunk * 8 + c;
+                        acc = fmaf(bf16_to_float(xr[h]), bf16_to_float(wrow[h]), acc);
+                    }
+                part[l] = acc;
+            }
+            for (int stride = 16; stride >= 1; stride /= 2) {
+                for (int l = 0; l < 32; ++l) next[l] = part[l] + part[l ^ stride];
+                memcpy(part, next, sizeof part);
+            }
+            float v = part[0];
+            if (bias != NULL) v = v + bias[e];
+            logits[(size_t)t * E + e] = v;
+        }
+}
+
 /* ------------------------------------------------------------------ routing */
 
 static double route_key(float v)

@@ -55,6 +55,10 @@ def _load():
             lib.oracle_weight.argtypes = [P, P, P, i, i, i, i, i]
             lib.oracle_decode_row.restype = None
             lib.oracle_decode_row.argtypes = [P, P, P, i, i, i, i, P]
+            lib.oracle_router_logits.restype = None
+            lib.oracle_router_logits.argtypes = [P, P, P, i, i, i, P]
+            lib.oracle_router_logits_exact.restype = None
+            lib.oracle_router_logits_exact.argtypes = [P, P, P, i, i, i, P]
             lib.oracle_route.restype = None
             lib.oracle_route.argtypes = [P, i, i, i, P, P]
             lib.oracle_permute.restype = None
@@ -108,6 +112,29 @@ def decode_row(codes, scales, gs, N, K, e, n) -> np.ndarray:
     codes, scales, gs = _c(codes, np.uint8), _c(scales, np.uint8), _c(gs, np.float32)
     out = np.empty(K, np.float64)
     _load().oracle_decode_row(_ptr(codes), _ptr(scales), _ptr(gs), N, K, e, n, _ptr(out))
+    return out
+
+
+# ------------------------------------------------------------- router logits
+def router_logits(x_bf16, wr_bf16, bias=None) -> np.ndarray:
+    """fp32 [T,E] gate logits in the library's fixed reduction order (bit-exact target)."""
+    x, wr = _c(x_bf16, np.uint16), _c(wr_bf16, np.uint16)
+    T, H = x.shape
+    E = wr.shape[0]
+    b = None if bias is None else _c(bias, np.float32)
+    out = np.empty((T, E), np.float32)
+    _load().oracle_router_logits(_ptr(x), _ptr(wr), None if b is None else _ptr(b), T, H, E, _ptr(out))
+    return out
+
+
+def router_logits_exact(x_bf16, wr_bf16, bias=None) -> np.ndarray:
+    """fp64 [T,E] gate logits, the exact sum (the definition)."""
+    x, wr = _c(x_bf16, np.uint16), _c(wr_bf16, np.uint16)
+    T, H = x.shape
+    E = wr.shape[0]
+    b = None if bias is None else _c(bias, np.float32)
+    out = np.empty((T, E), np.float64)
+    _load().oracle_router_logits_exact(_ptr(x), _ptr(wr), None if b is None else _ptr(b), T, H, E, _ptr(out))
     return out
 
 
@@ -208,3 +235,12 @@ def layer_rows(x_bf16, ids, w, gu, dn, rows):
     _load().oracle_layer_rows(_ptr(x), _ptr(ids), _ptr(w), *[_ptr(v) for v in a], H, I, k,
                               _ptr(rows), len(rows), _ptr(out))
     return out
+
+
+def shared_rows(x_bf16, sgu, sdn, rows):
+    """Shared-expert output y_shared for a subset of tokens (f64 [len(rows), H]):
+    the same SwiGLU FFN as a routed expert's (h rounded to bf16), on a one-expert
+    matrix, with weight 1 -- i.e. layer_rows with every token routed to expert 0."""
+    x = _c(x_bf16, np.uint16)
+    T = x.shape[0]
+    return layer_rows(x, np.zeros((T, 1), np.int32), np.ones((T, 1), np.float64), sgu, sdn, rows)

@@ -105,3 +105,11 @@ def test_null_misaligned_and_small_workspace(lib):
     assert lib.moe_prepack_w4(ok, ok, 2, 128, 64, 7, ok, None) == _lib.MOE_ERR_INVALID_ARG
     assert lib.moe_get_device_status(None, None) == _lib.MOE_ERR_INVALID_ARG
     assert lib.moe_layer_forward_host(None, ok, w, w, d, ok, ok, 1 << 30, None) == _lib.MOE_ERR_INVALID_ARG
+    # router logits: weights required, bias optional but 4-byte aligned
+    assert lib.moe_router_logits(ok, None, None, d, ok, None) == _lib.MOE_ERR_INVALID_ARG
+    assert lib.moe_router_logits(ok, odd, None, d, ok, None) == _lib.MOE_ERR_MISALIGNED
+    assert lib.moe_router_logits(ok, ok, ctypes.c_void_p(0x10002), d, ok, None) == _lib.MOE_ERR_MISALIGNED
+    assert lib.moe_layer_forward_router(ok, ok, None, w, w, d, ok, None, None, None, ok, small, None) == \
+        _lib.MOE_ERR_WORKSPACE_TOO_SMALL
+    assert lib.moe_layer_forward_router(ok, ok, None, w, w, d, ok, odd, None, None, ok, 1 << 30, None) == \
+        _lib.MOE_ERR_MISALIGNED

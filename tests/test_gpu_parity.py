@@ -1,6 +1,7 @@
 """Parity of the CUDA path (called through the C ABI) with the fp64 oracle."""
 from __future__ import annotations
 
+import math
 import numpy as np
 import pytest
 import torch
@@ -100,6 +101,104 @@ def test_route_edge_cases():
     ids, w = _route_gpu(logits, 32)
     rids, rw = orc.route(logits.numpy(), 32)
     assert np.array_equal(ids, rids) and np.abs(w - rw).max() <= 2e-6
+
+
+# ------------------------------------------------------------ router logits
+@pytest.mark.parametrize("name", ALL)
+def test_router_logits_bit_exact(name):
+    wl = wk.by_name(name)
+    d = wk.generate(wl, with_weights=False)
+    Wr, b = wk.router_weights(wl)
+    x = d["x"]
+    logits = torch.empty(wl.T, wl.E, dtype=torch.float32, device=DEV)
+    _lib.moe_router_logits(x.to(DEV), Wr.to(DEV), b.to(DEV), _lib.dims(wl.T, wl.H, wl.I, wl.E, wl.k), logits)
+    got = logits.cpu().numpy()
+    rows = np.arange(wl.T) if wl.T <= 1024 else np.random.default_rng(5).choice(wl.T, 512, replace=False)
+    ref = orc.router_logits(bits(x)[rows], bits(Wr), b.numpy())
+    assert np.array_equal(got[rows].view(np.uint32), ref.view(np.uint32))
+
+
+def test_router_logits_without_bias_and_ragged_h():
+    g = torch.Generator().manual_seed(21)
+    for T, H, E in [(3, 128, 5), (17, 384, 70), (1, 65536, 2)]:
+        x = torch.randn(T, H, generator=g).to(torch.bfloat16)
+        Wr = (torch.randn(E, H, generator=g) / math.sqrt(H)).to(torch.bfloat16)
+        logits = torch.empty(T, E, dtype=torch.float32, device=DEV)
+        _lib.moe_router_logits(x.to(DEV), Wr.to(DEV), None, _lib.dims(T, H, 64, E, 1), logits)
+        ref = orc.router_logits(bits(x), bits(Wr))
+        assert np.array_equal(logits.cpu().numpy().view(np.uint32), ref.view(np.uint32)), (T, H, E)
+
+
+@pytest.mark.parametrize("name", ["tiny", "decode"])
+def test_layer_with_router_logits(name):
+    # the layer computing its own gate logits: logits bit-exact, routing
+    # exact, the output identical to the layer fed the same logits, and within
+    # tolerance of the oracle layer
+    wl, d = workload_inputs(name)
+    Wr, b = wk.router_weights(wl)
+    layer = _layer(wl, d)
+    x = d["x"].to(DEV)
+    logits = torch.empty(wl.T, wl.E, dtype=torch.float32, device=DEV)
+    ids = torch.empty(wl.T, wl.k, dtype=torch.int32, device=DEV)
+    w = torch.empty(wl.T, wl.k, dtype=torch.float32, device=DEV)
+    out = layer.forward_router(x, Wr.to(DEV), b.to(DEV), logits_out=logits, topk_ids=ids, topk_w=w)
+    assert layer.device_status() == _lib.MOE_OK
+    ref_logits = orc.router_logits(bits(d["x"]), bits(Wr), b.numpy())
+    assert np.array_equal(logits.cpu().numpy().view(np.uint32), ref_logits.view(np.uint32))
+    rids, rw = orc.route(ref_logits, wl.k)
+    assert np.array_equal(ids.cpu().numpy(), rids)
+    assert np.abs(w.cpu().numpy() - rw).max() <= 2e-6
+    out2 = layer.forward(x, torch.from_numpy(ref_logits).to(DEV))
+    assert np.array_equal(bits(out), bits(out2))
+    gu, dn = numpy_weights(d)
+    ref = orc.layer_rows(bits(d["x"]), rids, rw, gu, dn, np.arange(wl.T, dtype=np.int32))
+    check_layer(bits(out), ref, f"{name} with router")
+
+
+# ------------------------------------------------------------ shared expert
+@pytest.mark.parametrize("name", ["tiny", "decode", "grouped", "skewed"])
+def test_layer_with_shared_expert(name):
+    # routed output plus a shared expert every token uses (weight 1), in the
+    # same grouped launches; gate logits given
+    wl, d = workload_inputs(name)
+    sgu, sdn = wk.shared_expert(wl)
+    gu, dn = numpy_weights(d)
+    layer = MoELayer(d["gu"], d["dn"], wl.H, wl.I, wl.E, wl.k, wl.T, DEV, shared=(sgu, sdn))
+    ids = torch.empty(wl.T, wl.k, dtype=torch.int32, device=DEV)
+    w = torch.empty(wl.T, wl.k, dtype=torch.float32, device=DEV)
+    out = layer.forward_shared(d["x"].to(DEV), logits=d["logits"].to(DEV), topk_ids=ids, topk_w=w)
+    out2 = layer.forward_shared(d["x"].to(DEV), logits=d["logits"].to(DEV))
+    assert layer.device_status() == _lib.MOE_OK
+    assert np.array_equal(bits(out), bits(out2)), "not deterministic"
+    rids, rw = orc.route(d["logits"].numpy(), wl.k)
+    assert np.array_equal(ids.cpu().numpy(), rids)
+    if LAYER_SAMPLE[name] is None:
+        rows = np.arange(wl.T, dtype=np.int32)
+    else:
+        rows = sample_tokens(rids, wl.E, LAYER_SAMPLE[name], seed=9)
+    sgu_np = tuple(a.numpy() for a in sgu)
+    sdn_np = tuple(a.numpy() for a in sdn)
+    ref = orc.layer_rows(bits(d["x"]), rids, rw, gu, dn, rows) + orc.shared_rows(bits(d["x"]), sgu_np, sdn_np, rows)
+    check_layer(bits(out)[rows], ref, f"{name} + shared expert")
+
+
+def test_layer_with_shared_expert_and_router():
+    # logits from router weights and a shared expert, in one call
+    wl, d = workload_inputs("decode")
+    sgu, sdn = wk.shared_expert(wl)
+    Wr, b = wk.router_weights(wl)
+    gu, dn = numpy_weights(d)
+    layer = MoELayer(d["gu"], d["dn"], wl.H, wl.I, wl.E, wl.k, wl.T, DEV, shared=(sgu, sdn))
+    logits = torch.empty(wl.T, wl.E, dtype=torch.float32, device=DEV)
+    out = layer.forward_shared(d["x"].to(DEV), router_weight=Wr.to(DEV), router_bias=b.to(DEV), logits_out=logits)
+    assert layer.device_status() == _lib.MOE_OK
+    ref_logits = orc.router_logits(bits(d["x"]), bits(Wr), b.numpy())
+    assert np.array_equal(logits.cpu().numpy().view(np.uint32), ref_logits.view(np.uint32))
+    rids, rw = orc.route(ref_logits, wl.k)
+    rows = np.arange(wl.T, dtype=np.int32)
+    ref = orc.layer_rows(bits(d["x"]), rids, rw, gu, dn, rows) + orc.shared_rows(
+        bits(d["x"]), tuple(a.numpy() for a in sgu), tuple(a.numpy() for a in sdn), rows)
+    check_layer(bits(out), ref, "decode + router + shared expert")
 
 
 # ------------------------------------------------------------ permutation

@@ -275,3 +275,64 @@ def test_stage_functions_compose_to_layer():
             ref[t] += w[t, j] * y[inv_perm[t * 2 + j]]
     assert np.array_equal(ref, out)
     assert np.array_equal(orc.combine(y, inv_perm, w), out)
+
+
+# ------------------------------------------------------------ router logits
+def _bf16_bits(t: torch.Tensor) -> np.ndarray:
+    return t.to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+
+
+def test_router_logits_exact_matches_fp64_matmul():
+    g = torch.Generator().manual_seed(11)
+    x = torch.randn(7, 384, generator=g).to(torch.bfloat16)
+    w = torch.randn(9, 384, generator=g).to(torch.bfloat16)
+    b = torch.randn(9, generator=g)
+    got = orc.router_logits_exact(_bf16_bits(x), _bf16_bits(w), b.numpy())
+    ref = (x.double() @ w.double().T + b.double()[None, :]).numpy()
+    assert np.allclose(got, ref, rtol=0, atol=1e-12 * np.abs(ref).max())
+
+
+def test_router_logits_ordered_within_fp32_bound():
+    # each part sums at most 8*ceil(H/256) products with fma (one rounding
+    # each), then five pairwise rounds and the bias: first-order bound
+    # (n_fma + 6) * 2^-24 * sum |x w| + |bias| 2^-24
+    g = torch.Generator().manual_seed(12)
+    for H in (128, 256, 2048, 4096):
+        x = torch.randn(5, H, generator=g).to(torch.bfloat16)
+        w = (torch.randn(6, H, generator=g) / math.sqrt(H)).to(torch.bfloat16)
+        b = torch.randn(6, generator=g)
+        got = orc.router_logits(_bf16_bits(x), _bf16_bits(w), b.numpy()).astype(np.float64)
+        ref = orc.router_logits_exact(_bf16_bits(x), _bf16_bits(w), b.numpy())
+        absprod = (x.double().abs() @ w.double().abs().T).numpy()
+        n_fma = 8 * ((H + 255) // 256)
+        bound = (n_fma + 6) * 2.0 ** -24 * absprod + 2.0 ** -24 * np.abs(b.numpy())[None, :] + 1e-30
+        assert np.all(np.abs(got - ref) <= bound), f"H={H}"
+
+
+def test_router_logits_integer_inputs_are_exact():
+    # small integers: every product and partial sum is an exact fp32 integer,
+    # so any summation order gives the exact value (a dropped or doubled term
+    # would not)
+    g = torch.Generator().manual_seed(13)
+    x = torch.randint(-8, 9, (4, 512), generator=g).float()
+    w = torch.randint(-8, 9, (6, 512), generator=g).float()
+    b = torch.randint(-100, 101, (6,), generator=g).float()
+    got = orc.router_logits(_bf16_bits(x), _bf16_bits(w), b.numpy())
+    assert np.array_equal(got.astype(np.float64), (x.double() @ w.double().T + b.double()).numpy())
+
+
+def test_router_logits_order_fixture():
+    # H = 16: part 0 takes h = 0..7, part 1 takes h = 8..15, the others are 0.
+    # x = 1 everywhere; w[0] = 2^24, w[1..15] = 1.
+    # part 0: fma gives 2^24, then adding 1 seven times stays at 2^24 (2^24+1
+    #         is a tie that rounds to the even 2^24);
+    # part 1: 8;  pairwise rounds: part 0 = 2^24 + 8 = 16777224 (exact).
+    # (The exact sum 16777231 would round to 16777232; a sequential sum over
+    # h stays at 16777216.)  With bias -2^24 the result is exactly 8.
+    x = torch.ones(1, 16)
+    w = torch.ones(1, 16)
+    w[0, 0] = 2.0 ** 24
+    got = orc.router_logits(_bf16_bits(x), _bf16_bits(w))
+    assert got[0, 0] == np.float32(16777224.0)
+    got_b = orc.router_logits(_bf16_bits(x), _bf16_bits(w), np.array([-(2.0 ** 24)], np.float32))
+    assert got_b[0, 0] == np.float32(8.0)
