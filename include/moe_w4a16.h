@@ -256,7 +256,12 @@ int moe_layer_forward_shared(const uint16_t *x, const float *logits, const uint1
  * host_logits (float [T][E]) into ws, runs moe_layer_forward, copies the
  * result to host_out (bf16 [T][H]) and synchronises `stream` before returning.
  * Host buffers should be page-locked for full copy speed.  Weights stay on the
- * device.  Needs moe_workspace_bytes(d) of ws. */
+ * device.  Needs moe_workspace_bytes(d) of ws.
+ * On a non-default stream with page-locked host buffers the first call with a
+ * given set of arguments (pointers, dims, stream) records its copies and
+ * kernels as a CUDA graph, and later calls with the same arguments replay it
+ * (the host buffers are read and written when it runs); the library keeps the
+ * 8 most recent.  Other calls issue the copies and launches directly. */
 int moe_layer_forward_host(const uint16_t *host_x, const float *host_logits, moe_w4 w_gate_up,
                            moe_w4 w_down, moe_dims d, uint16_t *host_out, void *ws, size_t ws_bytes,
                            void *stream);

@@ -289,20 +289,38 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int j = released; j < issued; ++j) mbar_arrive(fullb_bar(j % NSB));
       released = issued;
     };
+    // A phase-1 tile of expert e needs every phase-0 tile of e finished (4
+    // epilogue warps each).  Readiness is checked for 32 tiles at once, lane
+    // l loading the counter of this CTA's tile j + l, so most tiles need no
+    // check of their own; each lane's acquire load, followed by the warp
+    // sync, orders the whole warp's later reads of those rows.
+    auto target_of = [&](int e) { return 4 * MT0 * (s_tprefix[e + 1] - s_tprefix[e]); };
+    int known_ready = -1;  // this CTA's tiles 0 .. known_ready are ready to read
     bool ok = true;
-    for (int u = blockIdx.x; u < total && ok; u += gridDim.x) {
+    int j = 0;
+    for (int u = blockIdx.x; u < total && ok; u += gridDim.x, ++j) {
       const TileRef tr = tile_of(u);
       const GemmPhase& P = L.ph[tr.ph];
       const int KS = tr.ph == 0 ? KS0 : KS1;
       const int p0 = s_off[tr.c.e] + tr.c.nt * BN;
-      if (tr.ph == 1) {
-        // this expert's h rows: every phase-0 tile of it, 4 epilogue warps each
-        const int* ctr = L.ready + tr.c.e;
-        const int target = 4 * MT0 * (s_tprefix[tr.c.e + 1] - s_tprefix[tr.c.e]);
-        if (!__all_sync(0xFFFFFFFFu, counter_load_acquire(ctr) >= target)) {
+      if (tr.ph == 1 && j > known_ready) {
+        const int ul = u + lane * (int)gridDim.x;
+        bool lane_ready = true;
+        if (ul < total) {
+          const TileRef tl = tile_of(ul);
+          if (tl.ph == 1) lane_ready = counter_load_acquire(L.ready + tl.c.e) >= target_of(tl.c.e);
+        }
+        const uint32_t not_ready = __ballot_sync(0xFFFFFFFFu, !lane_ready);
+        __syncwarp();
+        const int n_ready = not_ready != 0 ? __ffs(not_ready) - 1 : 32;
+        if (n_ready > 0) {
+          known_ready = j + n_ready - 1;
+        } else {
+          // hand every pending stage over before waiting on other CTAs
           release_all();
-          ok = __all_sync(0xFFFFFFFFu, wait_counter(ctr, target, abort_flag, status));
+          ok = __all_sync(0xFFFFFFFFu, wait_counter(L.ready + tr.c.e, target_of(tr.c.e), abort_flag, status));
           if (!ok) break;
+          known_ready = j;
         }
       }
       const bool valid = r < s_off[tr.c.e + 1] - p0;

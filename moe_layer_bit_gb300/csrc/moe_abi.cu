@@ -4,6 +4,7 @@
 #include <cstdlib>
 #include <cstring>
 #include <initializer_list>
+#include <mutex>
 #include <cuda_runtime.h>
 
 #include "moe_w4a16.h"
@@ -389,6 +390,66 @@ int moe_layer_forward_shared(const uint16_t* x, const float* logits, const uint1
                             ws_bytes, stream, nullptr);
 }
 
+}  // extern "C"
+
+namespace {
+
+// The copies and kernels of one host-buffer call, enqueued on `s`.
+int enqueue_host_call(const uint16_t* host_x, const float* host_logits, moe_w4 w_gate_up, moe_w4 w_down, moe_dims d,
+                      uint16_t* host_out, void* ws, size_t ws_bytes, cudaStream_t s) {
+  const Layout L = layout_of(d);
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  const size_t xb = (size_t)d.T * d.H * 2, lb = (size_t)d.T * d.E * sizeof(float);
+  uint16_t* dx = reinterpret_cast<uint16_t*>(w + L.hx);
+  float* dl = reinterpret_cast<float*>(w + L.hlogits);
+  uint16_t* dout = reinterpret_cast<uint16_t*>(w + L.hout);
+  MOE_TRY(cuda_status(cudaMemcpyAsync(dx, host_x, xb, cudaMemcpyHostToDevice, s)));
+  MOE_TRY(cuda_status(cudaMemcpyAsync(dl, host_logits, lb, cudaMemcpyHostToDevice, s)));
+  MOE_TRY(moe_layer_forward(dx, dl, w_gate_up, w_down, d, dout, nullptr, nullptr, ws, ws_bytes, s));
+  return cuda_status(cudaMemcpyAsync(host_out, dout, xb, cudaMemcpyDeviceToHost, s));
+}
+
+bool page_locked(const void* p) {
+  cudaPointerAttributes a{};
+  if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return false;
+  }
+  return a.type == cudaMemoryTypeHost;
+}
+
+// Replayed host-buffer calls: on a non-default stream with page-locked host
+// buffers, a call records its copies and kernels once as a CUDA graph and
+// later calls with the same arguments replay it (the host buffers are read
+// and written when the graph runs).  A small cache, most recent first.
+struct HostCall {
+  const void* hx;
+  const void* hl;
+  const void* ho;
+  moe_w4 gu, dn;
+  moe_dims d;
+  const void* ws;
+  size_t ws_bytes;
+  const void* stream;
+  int dev;
+  cudaGraphExec_t exec;  // nullptr: capturing failed, run directly
+  bool used;
+};
+bool same_call(const HostCall& a, const HostCall& b) {
+  return a.hx == b.hx && a.hl == b.hl && a.ho == b.ho && a.gu.packed == b.gu.packed &&
+         a.gu.global_scale == b.gu.global_scale && a.dn.packed == b.dn.packed &&
+         a.dn.global_scale == b.dn.global_scale && a.d.T == b.d.T && a.d.H == b.d.H && a.d.I == b.d.I &&
+         a.d.E == b.d.E && a.d.k == b.d.k && a.ws == b.ws && a.ws_bytes == b.ws_bytes && a.stream == b.stream &&
+         a.dev == b.dev;
+}
+constexpr int kHostCalls = 8;
+HostCall g_host_calls[kHostCalls];
+std::mutex g_host_calls_mutex;
+
+}  // namespace
+
+extern "C" {
+
 int moe_layer_forward_host(const uint16_t* host_x, const float* host_logits, moe_w4 w_gate_up, moe_w4 w_down,
                            moe_dims d, uint16_t* host_out, void* ws, size_t ws_bytes, void* stream) {
   MOE_TRY(check_dims(d));
@@ -397,16 +458,50 @@ int moe_layer_forward_host(const uint16_t* host_x, const float* host_logits, moe
   MOE_TRY(check_ptrs({w_gate_up.packed, w_gate_up.global_scale, w_down.packed, w_down.global_scale, ws}));
   const Layout L = layout_of(d);
   if (ws_bytes < L.total) return MOE_ERR_WORKSPACE_TOO_SMALL;
-  uint8_t* w = static_cast<uint8_t*>(ws);
   cudaStream_t s = as_stream(stream);
-  const size_t xb = (size_t)d.T * d.H * 2, lb = (size_t)d.T * d.E * sizeof(float);
-  uint16_t* dx = reinterpret_cast<uint16_t*>(w + L.hx);
-  float* dl = reinterpret_cast<float*>(w + L.hlogits);
-  uint16_t* dout = reinterpret_cast<uint16_t*>(w + L.hout);
-  if (xb) MOE_TRY(cuda_status(cudaMemcpyAsync(dx, host_x, xb, cudaMemcpyHostToDevice, s)));
-  if (lb) MOE_TRY(cuda_status(cudaMemcpyAsync(dl, host_logits, lb, cudaMemcpyHostToDevice, s)));
-  MOE_TRY(moe_layer_forward(dx, dl, w_gate_up, w_down, d, dout, nullptr, nullptr, ws, ws_bytes, stream));
-  if (xb) MOE_TRY(cuda_status(cudaMemcpyAsync(host_out, dout, xb, cudaMemcpyDeviceToHost, s)));
+  if (s != nullptr && page_locked(host_x) && page_locked(host_logits) && page_locked(host_out)) {
+    HostCall key{};
+    key.hx = host_x;
+    key.hl = host_logits;
+    key.ho = host_out;
+    key.gu = w_gate_up;
+    key.dn = w_down;
+    key.d = d;
+    key.ws = ws;
+    key.ws_bytes = ws_bytes;
+    key.stream = stream;
+    if (cudaGetDevice(&key.dev) != cudaSuccess) return cuda_status(cudaErrorUnknown);
+    std::lock_guard<std::mutex> lock(g_host_calls_mutex);
+    int hit = -1;
+    for (int i = 0; i < kHostCalls; ++i)
+      if (g_host_calls[i].used && same_call(g_host_calls[i], key)) hit = i;
+    if (hit < 0) {
+      // record the call once; a call that cannot be recorded runs directly
+      cudaGraph_t graph = nullptr;
+      cudaGraphExec_t exec = nullptr;
+      if (cudaStreamBeginCapture(s, cudaStreamCaptureModeThreadLocal) == cudaSuccess) {
+        const int rc = enqueue_host_call(host_x, host_logits, w_gate_up, w_down, d, host_out, ws, ws_bytes, s);
+        const cudaError_t e = cudaStreamEndCapture(s, &graph);
+        if (rc == MOE_OK && e == cudaSuccess && graph != nullptr &&
+            cudaGraphInstantiate(&exec, graph, 0) != cudaSuccess)
+          exec = nullptr;
+        if (graph != nullptr) cudaGraphDestroy(graph);
+      }
+      (void)cudaGetLastError();
+      HostCall& slot = g_host_calls[kHostCalls - 1];
+      if (slot.used && slot.exec != nullptr) cudaGraphExecDestroy(slot.exec);
+      for (int i = kHostCalls - 1; i > 0; --i) g_host_calls[i] = g_host_calls[i - 1];
+      key.exec = exec;
+      key.used = true;
+      g_host_calls[0] = key;
+      hit = 0;
+    }
+    if (g_host_calls[hit].exec != nullptr) {
+      MOE_TRY(cuda_status(cudaGraphLaunch(g_host_calls[hit].exec, s)));
+      return cuda_status(cudaStreamSynchronize(s));
+    }
+  }
+  MOE_TRY(enqueue_host_call(host_x, host_logits, w_gate_up, w_down, d, host_out, ws, ws_bytes, s));
   return cuda_status(cudaStreamSynchronize(s));
 }
 

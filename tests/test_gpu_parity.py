@@ -351,6 +351,26 @@ def test_layer_host_entry_matches_device_entry():
     assert np.array_equal(bits(out), bits(oh))
 
 
+def test_layer_host_entry_replays_its_graph():
+    # non-default stream + page-locked buffers: the first call records a graph,
+    # the second replays it and must read the new host inputs
+    wl, d = workload_inputs("decode")
+    layer = _layer(wl, d)
+    s = torch.cuda.Stream()
+    xh = d["x"].pin_memory()
+    lh = d["logits"].pin_memory()
+    oh = torch.empty(wl.T, wl.H, dtype=torch.bfloat16).pin_memory()
+    for rnd in range(3):
+        x = torch.roll(d["x"], shifts=rnd, dims=0)
+        lg = torch.roll(d["logits"], shifts=2 * rnd, dims=1)
+        xh.copy_(x)
+        lh.copy_(lg)
+        ref = layer.forward(x.to(DEV), lg.to(DEV))
+        layer.forward_host(xh, lh, oh, s)
+        assert np.array_equal(bits(oh), bits(ref)), f"round {rnd}"
+    assert layer.device_status() == _lib.MOE_OK
+
+
 @pytest.mark.parametrize("T,H,I,E,k", [
     (1, 128, 64, 4, 1),      # single token
     (37, 256, 128, 8, 8),    # k = E, ragged T
