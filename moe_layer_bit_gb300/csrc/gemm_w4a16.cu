@@ -58,8 +58,9 @@ constexpr int kWarpDq0 = 4;        // warps 4..19: dequant (groups of 4 x split 
 constexpr int kDqWarps = 16;
 constexpr int kWarpProducer = 20;  // warp 20: weight copies
 constexpr int kWarpMma = 21;       // warp 21: TMEM owner + MMA issue
-constexpr int kWarpProducerB = 22; // warp 22: activation-tile copies
-constexpr int kThreads = 23 * 32;
+constexpr int kWarpProducerB = 22; // warps 22, 23: activation rows (gathered; warp 22 alone for TMA tiles)
+constexpr int kBProducers = 2;
+constexpr int kThreads = 24 * 32;
 constexpr uint32_t kTmemCols = 512;
 constexpr int kMinSmem = 120 * 1024;  // keeps one CTA (one TMEM allocation) per SM
 constexpr int kSmemBudget = 216 * 1024;  // rings; the tile table (<= 8 KiB) and alignment slack on top
@@ -167,7 +168,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(emptyw_bar(s), C::kGroupWarps);  // the stage's dequant warps
     }
     for (int s = 0; s < NSB; ++s) {
-      mbar_init(fullb_bar(s), 1);
+      mbar_init(fullb_bar(s), C::kGatherB ? kBProducers : 1);  // each gathering warp, or the TMA bytes
       mbar_init(emptyb_bar(s), 1);  // the MMA commit
     }
     for (int a = 0; a < NA; ++a) {
@@ -263,16 +264,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int j = (i > ring ? i - ring : 0); j < i; ++j)
       mbar_wait(is_w ? fullw_bar(j % ring) : fullb_bar(j % ring), (uint32_t)(j / ring) & 1u, nullptr, status,
                 kDrainTimeoutNs);
-  } else if (warp == kWarpProducerB) {
+  } else if (C::kGatherB && warp >= kWarpProducerB && warp < kWarpProducerB + kBProducers) {
     // ------------------------------------- activation rows, gathered (BN <= 32)
-    // Lane -> (row r, 16-byte chunks c0 .. c0 + kChunks - 1 of every 64-column
-    // block); chunk c of row r lands at r * 128 + ((c ^ (r & 7)) * 16), the
-    // 128-byte swizzle the MMA's shared-memory descriptor expects.  Rows past
-    // the expert's last token are zero-filled, not read.  A phase-1 tile of
-    // expert e first waits until every phase-0 tile of e has written its rows.
-    constexpr int kChunks = BN == 16 ? 4 : 8;
+    // Two warps split every row's 16-byte chunks.  Lane -> (row r, chunks
+    // c0 .. c0 + kChunks - 1 of every 64-column block); chunk c of row r lands
+    // at r * 128 + ((c ^ (r & 7)) * 16), the 128-byte swizzle the MMA's
+    // shared-memory descriptor expects.  Rows past the expert's last token are
+    // zero-filled, not read.  A phase-1 tile of expert e first waits until
+    // every phase-0 tile of e has written its rows.
+    constexpr int kChunks = (BN == 16 ? 4 : 8) / kBProducers;
+    const int part = warp - kWarpProducerB;
     const int r = BN == 16 ? (lane & 15) : lane;
-    const int c0 = BN == 16 ? (lane >> 4) * 4 : 0;
+    const int c0 = (BN == 16 ? (lane >> 4) * 4 : 0) + part * kChunks;
     uint32_t dst_off[kChunks];
 #pragma unroll
     for (int j = 0; j < kChunks; ++j) dst_off[j] = (uint32_t)(r * 128 + (((c0 + j) ^ (r & 7)) * 16));
@@ -359,6 +362,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else {
       cp_async_wait_group<0>();  // nothing may land after the CTA exits
     }
+  } else if (warp >= kWarpProducerB) {
+    // TMA tiles: warp 22 is the producer above; warp 23 has nothing to do
   } else if (warp == kWarpMma) {
     // ---------------------------------------------------------- MMA issue
     // The whole warp waits and computes the (uniform) operands; one elected
@@ -375,8 +380,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t d_tmem = tmem_base + (uint32_t)(d * BN);
       for (int ks = 0; ks < KS; ++ks, ++i) {
         const int s = i % NSB, a = i % NA;
+        // gathered activation stages are waited on by the dequant group
+        // (afull implies fullb); TMA stages here
         const bool got = mbar_wait(afull_bar(a), (uint32_t)(i / NA) & 1u, abort_flag, status) &&
-                         mbar_wait(fullb_bar(s), (uint32_t)(i / NSB) & 1u, abort_flag, status);
+                         (C::kGatherB || mbar_wait(fullb_bar(s), (uint32_t)(i / NSB) & 1u, abort_flag, status));
         if (!__all_sync(0xFFFFFFFFu, got)) {
           ok = false;
           break;
@@ -445,6 +452,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_wait_st();
       tc_fence_before();
+      if (C::kGatherB && q == 0 && part == 0) {
+        // The stage's activation rows too, so that the MMA warp waits on one
+        // barrier per stage.  Gathered stages are released in order, so the
+        // in-order fullb phases cannot alias across the groups that wait here.
+        if (!__all_sync(0xFFFFFFFFu, mbar_wait(fullb_bar(i % C::NSB), (uint32_t)(i / C::NSB) & 1u, abort_flag,
+                                               status)))
+          break;
+      }
       __syncwarp();
       if (lane == 0) mbar_arrive(afull_bar(a));
     }
