@@ -193,6 +193,12 @@ def _max_over_ranks(dist, v: float, device) -> float:
     return float(t.item())
 
 
+def _job_throughput(dist, world: int, tokens_per_rank: int, seconds: float, device) -> float:
+    """Whole-job tokens/s of N replicas: the tokens all ranks processed over the
+    slowest rank's time."""
+    return world * tokens_per_rank / _max_over_ranks(dist, seconds, device)
+
+
 def _barrier(dist, device=None):
     if dist is not None:
         if device is not None and device.type == "cuda":
@@ -376,8 +382,7 @@ def run_ours(args, wl, dist, rank, world, local_rank):
     step_ms = [e[0].elapsed_time(e[5]) for e in evs]
     stage_ms = np.array([[e[i].elapsed_time(e[i + 1]) for i in range(5)] for e in stage_evs])
     total_s = sum(step_ms) / 1e3
-    total_s_max = _max_over_ranks(dist, total_s, dev)
-    value = world * wl.T * args.steps / total_s_max
+    value = _job_throughput(dist, world, wl.T * args.steps, total_s, dev)
 
     # ---- roofline of the dominant kernel (gate_up + SwiGLU), algorithmic bytes per launch
     counts = np.bincount(ids.cpu().numpy().reshape(-1), minlength=wl.E)
@@ -428,8 +433,7 @@ def run_ours(args, wl, dist, rank, world, local_rank):
         t0 = time.perf_counter()
         layer.forward_host(xh, lh, oh, e2e_stream)  # synchronises before returning
         e2e_times.append(time.perf_counter() - t0)
-    e2e_total = _max_over_ranks(dist, sum(e2e_times), dev)
-    e2e_value = world * wl.T * args.steps / e2e_total
+    e2e_value = _job_throughput(dist, world, wl.T * args.steps, sum(e2e_times), dev)
 
     # ---- CPU oracle baseline on a bounded sample (rank 0, N = 1 only)
     cpu = None
