@@ -414,6 +414,29 @@ def run_ours(args, wl, dist, rank, world, local_rank):
                      "launch_ms": gu_ms,
                      "other_roof_frac": (achieved / hbm_peak) if roofline["bound"] == "tensor"
                      else (achieved_tf / tf_peak)})
+    if roofline["bound"] == "hbm":
+        # What one kernel of the GEMM's shape reads in the same time budget when it
+        # does nothing else: the streaming probe over the same byte count, same flush.
+        nbytes = (gu_bytes // 18432) * 18432
+        probe_buf = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+        pev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
+        for _ in range(3):
+            flush_l2(0.0)
+            _lib.moe_debug_stream_read(probe_buf, nbytes, layer.ws, stream)
+        for st in range(args.steps):
+            flush_l2(float(st))
+            pev[st][0].record(stream)
+            _lib.moe_debug_stream_read(probe_buf, nbytes, layer.ws, stream)
+            pev[st][1].record(stream)
+        torch.cuda.synchronize(dev)
+        if layer.device_status() != _lib.MOE_OK:
+            raise RuntimeError("stream probe timed out")
+        probe_ms = float(np.mean([e[0].elapsed_time(e[1]) for e in pev]))
+        probe_gbs = nbytes / (probe_ms * 1e-3) / 1e9
+        roofline["stream_probe"] = {
+            "what": "one CTA per SM, 8 x 18432-byte bulk copies in flight, nothing else; same byte count and L2 flush",
+            "bytes": nbytes, "ms": probe_ms, "gbs": probe_gbs, "kernel_vs_probe": achieved / probe_gbs}
+        del probe_buf
     layer_bytes = wk.algorithmic_bytes(wl.T, wl.H, wl.I, wl.E, wl.k, counts)
     layer_flops = wk.algorithmic_flops(wl.T, wl.H, wl.I, wl.k)
     mean_step_ms = total_s * 1e3 / args.steps

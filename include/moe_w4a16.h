@@ -296,6 +296,15 @@ int moe_debug_timeout_probe(void *ws, uint64_t limit_ns, void *stream);
  * faults and the context stays usable. */
 int moe_debug_counter_timeout_probe(void *ws, uint64_t limit_ns, void *stream);
 
+/* Measurement hook: a streaming-read probe.  Reads floor(bytes / 18432) *
+ * 18432 bytes of device memory at src (16-byte aligned) with one CTA per SM,
+ * each issuing 18432-byte bulk copies into a ring of 8 shared-memory slots and
+ * doing nothing else -- the weight stream of the narrow-tile GEMM without its
+ * work -- so that a caller can time how fast one kernel of that shape reads
+ * that many bytes.  ws: the status word (and the int after it) of a workspace;
+ * a stalled copy records MOE_ERR_DEVICE_TIMEOUT there. */
+int moe_debug_stream_read(const void *src, size_t bytes, void *ws, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

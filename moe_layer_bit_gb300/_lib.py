@@ -72,6 +72,7 @@ _SIGS = {
     "moe_debug_dequant_table": (INT, [P, P]),
     "moe_debug_timeout_probe": (INT, [P, ctypes.c_uint64, P]),
     "moe_debug_counter_timeout_probe": (INT, [P, ctypes.c_uint64, P]),
+    "moe_debug_stream_read": (INT, [P, SZ, P, P]),
 }
 
 
@@ -234,6 +235,10 @@ def moe_debug_dequant_table(out, stream=None):
 
 def moe_debug_timeout_probe(ws, limit_ns: int, stream=None):
     _check(load().moe_debug_timeout_probe(_p(ws), int(limit_ns), _s(stream)), "moe_debug_timeout_probe")
+
+
+def moe_debug_stream_read(src, nbytes: int, ws, stream=None):
+    _check(load().moe_debug_stream_read(_p(src), int(nbytes), _p(ws), _s(stream)), "moe_debug_stream_read")
 
 
 def moe_debug_counter_timeout_probe(ws, limit_ns: int, stream=None):

@@ -141,6 +141,11 @@ struct GemmLaunch {
 // Kernel launches made by launch_route_group for these sizes.
 int route_group_launches(int T, int E, int k, bool shared);
 
+// Streaming-read probe (probe.cu): reads floor(bytes / 18432) stages of 18432
+// bytes from src with one CTA per SM and a ring of bulk copies, nothing else.
+// status: the status word (the int after it is a sink that is never written).
+cudaError_t launch_stream_probe(const void* src, size_t bytes, int* status, cudaStream_t s);
+
 // Bounded-wait self test: a kernel waits on a barrier nobody arrives at and
 // must give up after `limit_ns`, recording a timeout in `status`.
 cudaError_t launch_timeout_probe(int* status, unsigned long long limit_ns, cudaStream_t s);

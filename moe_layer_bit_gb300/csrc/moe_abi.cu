@@ -541,6 +541,11 @@ int moe_debug_timeout_probe(void* ws, uint64_t limit_ns, void* stream) {
                                                as_stream(stream)));
 }
 
+int moe_debug_stream_read(const void* src, size_t bytes, void* ws, void* stream) {
+  MOE_TRY(check_ptrs({src, ws}));
+  return cuda_status(moe::launch_stream_probe(src, bytes, static_cast<int*>(ws), as_stream(stream)));
+}
+
 int moe_debug_counter_timeout_probe(void* ws, uint64_t limit_ns, void* stream) {
   MOE_TRY(check_ptrs({ws}));
   int* base = static_cast<int*>(ws);
