@@ -325,9 +325,30 @@ __global__ void __launch_bounds__(kPermChunk) route_permute_small_kernel(
   __syncthreads();
   const bool valid = tid < n;
   const int e = valid ? s_ids[tid] : 0;
-  const int rank = warp_rank_and_count(e, valid, tab);
-  __syncthreads();
-  block_rank_scan(tab, base, EG);  // base[e] = count of e
+  const int t = tid / ks;
+  // When this block routed the tokens itself, a token meets an expert at most
+  // once, so the pairs of expert e in pair order are its tokens in token
+  // order.  Then, for T <= 256, the block keeps per expert a bitmap of its
+  // tokens (W words, in the zeroed rank table): the count is its popcount and
+  // a pair's rank the popcount of the lower bits.  Otherwise (ids given, or
+  // larger T) it uses the per-warp count table.
+  const int W = (T + 31) >> 5;
+  const bool bitmap = logits != nullptr && W <= 8;
+  uint32_t* bm = reinterpret_cast<uint32_t*>(tab);  // [EG][W]
+  int rank = 0;
+  if (bitmap) {
+    if (valid) atomicOr(&bm[e * W + (t >> 5)], 1u << (t & 31));
+    __syncthreads();
+    for (int ex = tid; ex < EG; ex += blockDim.x) {
+      int cnt = 0;
+      for (int w = 0; w < W; ++w) cnt += __popc(bm[ex * W + w]);
+      base[ex] = cnt;
+    }
+  } else {
+    rank = warp_rank_and_count(e, valid, tab);
+    __syncthreads();
+    block_rank_scan(tab, base, EG);  // base[e] = count of e
+  }
   __syncthreads();
   const int32_t c = tid < EG ? base[tid] : 0;
   int32_t total;
@@ -341,8 +362,14 @@ __global__ void __launch_bounds__(kPermChunk) route_permute_small_kernel(
   }
   __syncthreads();
   if (valid) {
-    const int pos = base[e] + tab[e * kRankWarps + warp] + rank;
-    sorted_token[pos] = tid / ks;
+    int pos = base[e];
+    if (bitmap) {
+      for (int w = 0; w < (t >> 5); ++w) pos += __popc(bm[e * W + w]);
+      pos += __popc(bm[e * W + (t >> 5)] & ((1u << (t & 31)) - 1u));
+    } else {
+      pos += tab[e * kRankWarps + warp] + rank;
+    }
+    sorted_token[pos] = t;
     inv_perm[tid] = pos;
   }
 }
