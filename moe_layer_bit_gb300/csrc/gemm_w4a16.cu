@@ -217,6 +217,37 @@ __global__ void __launch_bounds__(kThreads, 1)
     r.c = decode_tile(r.ph == 0 ? u : u - T0, s_tprefix, E, r.ph == 0 ? MT0 : MT1);
     return r;
   };
+  // A role warp reads the CTA's schedule 32 tiles at a time: lane l decodes
+  // the CTA's tile jb + l (a chain of dependent shared-memory loads and
+  // divisions, slow while the dequant warps keep the ALU busy), and tile j is
+  // then taken from lane j - jb by shuffles.  Tiles are read in increasing j
+  // and the refill is warp-uniform.
+  struct TileCache {
+    int jb, ph, e, mt, nt;
+  };
+  auto cache_fill = [&](TileCache& tc, int j) {
+    tc.jb = j;
+    const int u = (int)blockIdx.x + (j + lane) * (int)gridDim.x;
+    tc.ph = 0;
+    tc.e = tc.mt = tc.nt = 0;
+    if (u < total) {
+      const TileRef r = tile_of(u);
+      tc.ph = r.ph;
+      tc.e = r.c.e;
+      tc.mt = r.c.mt;
+      tc.nt = r.c.nt;
+    }
+  };
+  auto cached_tile = [&](TileCache& tc, int j) {
+    if (j - tc.jb >= 32) cache_fill(tc, j);
+    const int src = j - tc.jb;
+    TileRef r;
+    r.ph = __shfl_sync(0xFFFFFFFFu, tc.ph, src);
+    r.c.e = __shfl_sync(0xFFFFFFFFu, tc.e, src);
+    r.c.mt = __shfl_sync(0xFFFFFFFFu, tc.mt, src);
+    r.c.nt = __shfl_sync(0xFFFFFFFFu, tc.nt, src);
+    return r;
+  };
 
   if (warp == kWarpProducer || (warp == kWarpProducerB && !C::kGatherB)) {
     // ----------------------------------------------------------- producers
@@ -228,8 +259,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int ring = is_w ? NSW : NSB;
     int i = 0;
     bool ok = true;
-    for (int u = blockIdx.x; u < total && ok; u += gridDim.x) {
-      const TileRef tr = tile_of(u);
+    TileCache tcache;
+    tcache.jb = -32;
+    int jt = 0;
+    for (int u = blockIdx.x; u < total && ok; u += gridDim.x, ++jt) {
+      const TileRef tr = cached_tile(tcache, jt);
       const GemmPhase& P = L.ph[tr.ph];
       const int MT = tr.ph == 0 ? MT0 : MT1, KS = tr.ph == 0 ? KS0 : KS1;
       // experts 0 .. E_routed-1 are the routed ones; the next (if any) is the
@@ -301,18 +335,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     int known_ready = -1;  // this CTA's tiles 0 .. known_ready are ready to read
     bool ok = true;
     int j = 0;
+    TileCache tcache;
+    tcache.jb = -32;
     for (int u = blockIdx.x; u < total && ok; u += gridDim.x, ++j) {
-      const TileRef tr = tile_of(u);
-      const GemmPhase& P = L.ph[tr.ph];
-      const int KS = tr.ph == 0 ? KS0 : KS1;
-      const int p0 = s_off[tr.c.e] + tr.c.nt * BN;
+      TileRef tr = cached_tile(tcache, j);
       if (tr.ph == 1 && j > known_ready) {
+        // the cache is refilled from tile j, so lane l holds tile j + l
+        if (tcache.jb != j) {
+          cache_fill(tcache, j);
+          tr = cached_tile(tcache, j);
+        }
         const int ul = u + lane * (int)gridDim.x;
         bool lane_ready = true;
-        if (ul < total) {
-          const TileRef tl = tile_of(ul);
-          if (tl.ph == 1) lane_ready = counter_load_acquire(L.ready + tl.c.e) >= target_of(tl.c.e);
-        }
+        if (ul < total && tcache.ph == 1) lane_ready = counter_load_acquire(L.ready + tcache.e) >= target_of(tcache.e);
         const uint32_t not_ready = __ballot_sync(0xFFFFFFFFu, !lane_ready);
         __syncwarp();
         const int n_ready = not_ready != 0 ? __ffs(not_ready) - 1 : 32;
@@ -326,6 +361,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           known_ready = j;
         }
       }
+      const GemmPhase& P = L.ph[tr.ph];
+      const int KS = tr.ph == 0 ? KS0 : KS1;
+      const int p0 = s_off[tr.c.e] + tr.c.nt * BN;
       const bool valid = r < s_off[tr.c.e + 1] - p0;
       const size_t src_row = valid ? (size_t)(P.gather_rows != nullptr ? P.gather_rows[p0 + r] : p0 + r) : 0;
       const uint16_t* rowp = P.act + src_row * (size_t)P.K + c0 * 8;
@@ -467,8 +505,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ epilogue
     const int q = warp - kWarpEpi0;
     int it = 0;
+    TileCache tcache;
+    tcache.jb = -32;
     for (int u = blockIdx.x; u < total; u += gridDim.x, ++it) {
-      const TileRef tr = tile_of(u);
+      const TileRef tr = cached_tile(tcache, it);
       const GemmPhase& P = L.ph[tr.ph];
       const TileCoord c = tr.c;
       const int d = it % ND;
