@@ -366,6 +366,9 @@ def test_layer_host_entry_replays_its_graph():
         xh.copy_(x)
         lh.copy_(lg)
         ref = layer.forward(x.to(DEV), lg.to(DEV))
+        # both calls use the layer's one workspace: the device call must end
+        # before the host call starts on its own stream
+        torch.cuda.synchronize()
         layer.forward_host(xh, lh, oh, s)
         assert np.array_equal(bits(oh), bits(ref)), f"round {rnd}"
     assert layer.device_status() == _lib.MOE_OK
