@@ -37,8 +37,11 @@
 //    the schedule is the gate_up tiles, then the down tiles, the weight
 //    stream runs on without a break, and a down tile's activation loads wait
 //    (per expert, on a GPU-scope counter the gate_up epilogues publish with
-//    release semantics) until that expert's h rows are written; the launch is
-//    cooperative, so all CTAs are resident and the waits cannot deadlock;
+//    release semantics) until that expert's h rows are written; the grid is
+//    at most one CTA per SM and a CTA needs a whole SM's shared memory, so
+//    once the kernel before it exits every CTA is resident and the waits
+//    cannot deadlock (a kernel of another stream holding SMs for longer than
+//    the wait limit turns them into a recorded timeout);
 //  * every barrier wait is bounded (about 1 s); on expiry the CTA records a
 //    timeout in the status word, drains its copies and MMAs and exits.
 #include <cstdint>
@@ -644,15 +647,14 @@ static cudaError_t launch_gemm_cfg(const GemmLaunch& L, int rows, cudaStream_t s
   err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (err != cudaSuccess) return err;
   // Two phases: phase-1 CTAs wait on phase-0 tiles of other CTAs, so all CTAs
-  // must be resident together (one per SM, grid <= SMs): a cooperative launch.
-  const bool coop = L.nph > 1;
-  err = launch_ex(kern, dim3(grid), dim3(kThreads), smem, s, true, coop, tmap, L);
-  if (err != cudaSuccess && coop) {
-    // without the programmatic overlap if the driver does not combine the two
-    (void)cudaGetLastError();
-    err = launch_ex(kern, dim3(grid), dim3(kThreads), smem, s, false, true, tmap, L);
-  }
-  return err;
+  // must become resident (grid <= SMs, one CTA per SM).  A cooperative launch
+  // would guarantee it, but it is not overlapped with the kernel before it
+  // (measured: about 2.4 us more per decode step); a programmatic launch
+  // starts the CTAs on the free SMs at once and the rest as soon as the
+  // kernel before exits, and the library launches nothing that could hold an
+  // SM in between (the next kernel's CTAs start only after every CTA of this
+  // one has signalled launch_dependents).
+  return launch_pdl(kern, dim3(grid), dim3(kThreads), smem, s, tmap, L);
 }
 
 // Token tile width: the smallest of 16/32/64/128 that covers about twice the

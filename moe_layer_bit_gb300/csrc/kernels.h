@@ -10,36 +10,22 @@ namespace moe {
 
 // Launches `kern` with programmatic stream serialization: it may start its
 // on-chip set-up while the previous kernel in `s` finishes (the kernels call
-// pdl_wait() before touching global memory).  `cooperative` also asks for all
-// CTAs to be resident at once (kernels whose CTAs wait on one another).
+// pdl_wait() before touching global memory, and pdl_trigger() once the next
+// kernel may start its own set-up).
 template <typename... KArgs, typename... Args>
-inline cudaError_t launch_ex(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s, bool pdl,
-                             bool cooperative, Args&&... args) {
-  cudaLaunchAttribute attr[2];
-  int n = 0;
-  if (pdl) {
-    attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[n].val.programmaticStreamSerializationAllowed = 1;
-    ++n;
-  }
-  if (cooperative) {
-    attr[n].id = cudaLaunchAttributeCooperative;
-    attr[n].val.cooperative = 1;
-    ++n;
-  }
+inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                              Args&&... args) {
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = block;
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
   cfg.attrs = attr;
-  cfg.numAttrs = n;
+  cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
-}
-template <typename... KArgs, typename... Args>
-inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
-                              Args&&... args) {
-  return launch_ex(kern, grid, block, smem, s, true, false, std::forward<Args>(args)...);
 }
 
 // Packed NVFP4 layout: tiles of 128 weight rows x 64 K elements, 4608 bytes each.
