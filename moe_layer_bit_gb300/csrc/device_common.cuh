@@ -163,6 +163,11 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tmap, int3
       "l"(tmap), "r"(bar), "r"(c0), "r"(c1)
       : "memory");
 }
+// Hint: pull `bytes` (a multiple of 16, 16-byte aligned) of global memory
+// into L2.
+__device__ __forceinline__ void prefetch_l2_bulk(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
 __device__ __forceinline__ void prefetch_tmap(const void* tmap) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(tmap) : "memory");
 }

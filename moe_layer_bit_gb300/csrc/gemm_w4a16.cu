@@ -191,6 +191,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     fence_barrier_init();
   }
   if (!C::kGatherB && warp == kWarpProducerB && lane == 0) prefetch_tmap(&tmap_act);
+  if (C::kGatherB && warp == kWarpProducer && lane == 0) {
+    // The packed weights do not come from the kernels before, so while they
+    // run this CTA pulls into L2 the weights of its likely first tile: tile
+    // blockIdx.x of the phase-0 list if every expert had one token tile.  Of
+    // a decode step's first round of tiles most are these; a wrong guess
+    // only costs bandwidth that is idle at this point.
+    const GemmPhase& P0 = L.ph[0];
+    const int MT0 = P0.N / kTileM;
+    const int e = (int)blockIdx.x / MT0, mt = (int)blockIdx.x % MT0;
+    if (e < P0.E_routed) {
+      const uint32_t tile_bytes = (uint32_t)(P0.K / kBlockK) * kWBlockBytes;
+      const uint8_t* src = P0.packed + (size_t)(e * MT0 + mt) * tile_bytes;
+      for (uint32_t o = 0; o < tile_bytes; o += C::kWBytes)
+        prefetch_l2_bulk(src + o, min((uint32_t)C::kWBytes, tile_bytes - o));
+    }
+  }
   if (warp == kWarpMma) {
     tmem_alloc(sbase + C::kOffMisc, kTmemCols);
     tmem_relinquish();
