@@ -18,21 +18,25 @@
 //  * a pipeline stage is SB consecutive 64-column K blocks (a "superstage"),
 //    so the per-stage barrier round trips of the single MMA-issuing warp are
 //    paid once per SB*4 MMAs;
-//  * warp roles: one producer warp issues one 1-D bulk copy of the SB packed
-//    weight blocks (codes + E4M3 scales, SB * 4608 B) per stage into a weight
-//    ring that is freed as soon as the codes are in registers; a second one
-//    fills a ring of 128-byte-swizzled activation tiles, freed by the MMA
-//    commit: SB 2-D TMA copies of a permuted copy of the rows for wide token
-//    tiles, and for narrow ones (16 or 32 rows: decode) 16-byte cp.async of
-//    row sorted_token[p] of x itself, so no permuted copy is written; 16 dequant warps in
-//    groups of four (stages round-robin over groups) turn the codes into exact
-//    bf16 (value * 2^-7) and store them straight into tensor memory as the
-//    MMA's A operand (tcgen05.st), so no dequantised weight touches shared
-//    memory; one MMA warp (operands warp-uniform, one elected lane issuing)
-//    runs tcgen05.mma with A from TMEM, B from shared memory and an fp32
-//    accumulator in TMEM, a ring of 2 (wide tiles) or 4 (narrow) across tiles; four epilogue warps
-//    read the accumulator (tcgen05.ld), apply global_scale * 2^7 and write
-//    SwiGLU(bf16) or fp32 rows;
+//  * warp roles (24 warps):
+//    - one producer warp issues one 1-D bulk copy of the SB packed weight
+//      blocks (codes + E4M3 scales, SB * 4608 B) per stage into a weight ring
+//      that is freed as soon as the codes are in registers;
+//    - activation tiles, 128-byte swizzled, go into a second ring freed by
+//      the MMA commit: for wide token tiles one warp issues SB 2-D TMA copies
+//      of a permuted copy of the rows; for narrow ones (16 or 32 rows:
+//      decode) two warps copy row sorted_token[p] of x itself with 16-byte
+//      cp.async, so no permuted copy is written;
+//    - 16 dequant warps in groups (stages round-robin over groups) turn the
+//      codes into exact bf16 (value * 2^-7) and store them straight into
+//      tensor memory as the MMA's A operand (tcgen05.st), so no dequantised
+//      weight touches shared memory;
+//    - one MMA warp (operands warp-uniform, one elected lane issuing) runs
+//      tcgen05.mma with A from TMEM, B from shared memory and an fp32
+//      accumulator in TMEM, a ring of 2 (wide tiles) or 4 (narrow) across
+//      tiles;
+//    - four epilogue warps read the accumulator (tcgen05.ld), apply
+//      global_scale * 2^7 and write SwiGLU(bf16) or fp32 rows;
 //  * one launch can run both projections of the layer (narrow token tiles):
 //    the schedule is the gate_up tiles, then the down tiles, the weight
 //    stream runs on without a break, and a down tile's activation loads wait
@@ -57,7 +61,7 @@
 namespace moe {
 
 constexpr int kWarpEpi0 = 0;       // warps 0..3: epilogue (TMEM lane quadrant = warp)
-constexpr int kWarpDq0 = 4;        // warps 4..19: dequant (groups of 4 x split warps)
+constexpr int kWarpDq0 = 4;        // warps 4..19: dequant (groups of 4 * kSplit warps)
 constexpr int kDqWarps = 16;
 constexpr int kWarpProducer = 20;  // warp 20: weight copies
 constexpr int kWarpMma = 21;       // warp 21: TMEM owner + MMA issue
@@ -116,16 +120,19 @@ struct Cfg {
   // (b) Stage i - NSW (the slot's previous phase) must have landed; copies do
   //     not complete in issue order, so G | NSW makes it the group's own,
   //     already waited on.
-  // The activation ring is only waited on by the in-order MMA warp.
+  // The activation ring is waited on in stage order: by the MMA warp, or for
+  // gathered stages by the stage's dequant group, whose previous stage's wait
+  // (with the producer's in-order releases and NSB >= G) covers stage
+  // i - NSB, and whose own arrival the release of stage i + NSB waits behind.
   static constexpr int NSW = NSW1 < G ? G : (NSW1 / G) * G;
-  static_assert(G <= NA && NSW % G == 0, "dequant groups must fit the TMEM and weight rings");
+  static_assert(G <= NA && NSW % G == 0 && (!kGatherB || NSB >= G), "dequant groups must fit the rings");
   static constexpr int kOffB = 0;
   static constexpr int kOffW = NSB * kBTile;
   static constexpr int kOffBar = kOffW + NSW * kWBytes;
   // fullw[NSW], emptyw[NSW], fullb[NSB], emptyb[NSB], afull[NA], aempty[NA],
   // dfull[ND], dempty[ND], drain
   static constexpr int kNumBars = 2 * NSW + 2 * NSB + 2 * NA + 2 * ND + 1;
-  static constexpr int kOffMisc = kOffBar + kNumBars * 8;  // [0] tmem base, [1] abort, [2] total tiles
+  static constexpr int kOffMisc = kOffBar + kNumBars * 8;  // [0] tmem base, [1] abort, [2] token tiles
   static constexpr int kOffTables = kOffMisc + 16;         // offsets[E+1], prefix[E+1]
   static_assert(NA >= 1, "TMEM ring needs a slot");
   static_assert(kOffW % 1024 == 0, "swizzled tiles need 1024-byte alignment");
