@@ -252,11 +252,15 @@ int moe_layer_forward_shared(const uint16_t *x, const float *logits, const uint1
                              moe_w4 shared_down, moe_dims d, uint16_t *out, float *logits_out, int32_t *topk_ids,
                              float *topk_w, void *ws, size_t ws_bytes, void *stream);
 
-/* The whole layer from HOST buffers: copies host_x (bf16 [T][H]) and
- * host_logits (float [T][E]) into ws, runs moe_layer_forward, copies the
- * result to host_out (bf16 [T][H]) and synchronises `stream` before returning.
- * Host buffers should be page-locked for full copy speed.  Weights stay on the
- * device.  Needs moe_workspace_bytes(d) of ws.
+/* The whole layer from HOST buffers: copies host_x (bf16 [T][H]) into ws,
+ * runs moe_layer_forward on it and host_logits (float [T][E]), puts the
+ * result in host_out (bf16 [T][H]) and synchronises `stream` before returning.
+ * When host_logits and host_out are page-locked memory the device can address
+ * (mapped, 16-byte aligned), the routing kernel reads the logits and the
+ * combine writes the output through their device addresses; otherwise they
+ * are copied through ws as well.  Host buffers should be page-locked for full
+ * transfer speed.  Weights stay on the device.  Needs moe_workspace_bytes(d)
+ * of ws.
  * On a non-default stream with page-locked host buffers the first call with a
  * given set of arguments (pointers, dims, stream) records its copies and
  * kernels as a CUDA graph, and later calls with the same arguments replay it

@@ -395,18 +395,15 @@ int moe_layer_forward_shared(const uint16_t* x, const float* logits, const uint1
 namespace {
 
 // The copies and kernels of one host-buffer call, enqueued on `s`.
-int enqueue_host_call(const uint16_t* host_x, const float* host_logits, moe_w4 w_gate_up, moe_w4 w_down, moe_dims d,
-                      uint16_t* host_out, void* ws, size_t ws_bytes, cudaStream_t s) {
-  const Layout L = layout_of(d);
-  uint8_t* w = static_cast<uint8_t*>(ws);
-  const size_t xb = (size_t)d.T * d.H * 2, lb = (size_t)d.T * d.E * sizeof(float);
-  uint16_t* dx = reinterpret_cast<uint16_t*>(w + L.hx);
-  float* dl = reinterpret_cast<float*>(w + L.hlogits);
-  uint16_t* dout = reinterpret_cast<uint16_t*>(w + L.hout);
-  MOE_TRY(cuda_status(cudaMemcpyAsync(dx, host_x, xb, cudaMemcpyHostToDevice, s)));
-  MOE_TRY(cuda_status(cudaMemcpyAsync(dl, host_logits, lb, cudaMemcpyHostToDevice, s)));
-  MOE_TRY(moe_layer_forward(dx, dl, w_gate_up, w_down, d, dout, nullptr, nullptr, ws, ws_bytes, s));
-  return cuda_status(cudaMemcpyAsync(host_out, dout, xb, cudaMemcpyDeviceToHost, s));
+// The device address of page-locked host memory that kernels can access
+// directly (mapped), else nullptr.
+void* mapped_device_ptr(const void* p) {
+  cudaPointerAttributes a{};
+  if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return nullptr;
+  }
+  return a.type == cudaMemoryTypeHost ? a.devicePointer : nullptr;
 }
 
 bool page_locked(const void* p) {
@@ -416,6 +413,29 @@ bool page_locked(const void* p) {
     return false;
   }
   return a.type == cudaMemoryTypeHost;
+}
+
+// x is copied into the workspace (the GEMM reads its rows many times).  When
+// the host logits and output are mapped page-locked memory, the routing
+// kernel reads the logits and the combine writes the output through their
+// device addresses, so those two transfers need no copy of their own;
+// otherwise they are copied too.
+int enqueue_host_call(const uint16_t* host_x, const float* host_logits, moe_w4 w_gate_up, moe_w4 w_down, moe_dims d,
+                      uint16_t* host_out, void* ws, size_t ws_bytes, cudaStream_t s) {
+  const Layout L = layout_of(d);
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  const size_t xb = (size_t)d.T * d.H * 2, lb = (size_t)d.T * d.E * sizeof(float);
+  uint16_t* dx = reinterpret_cast<uint16_t*>(w + L.hx);
+  MOE_TRY(cuda_status(cudaMemcpyAsync(dx, host_x, xb, cudaMemcpyHostToDevice, s)));
+  const float* ml = static_cast<const float*>(mapped_device_ptr(host_logits));
+  uint16_t* mo = static_cast<uint16_t*>(mapped_device_ptr(host_out));
+  if (ml != nullptr && mo != nullptr && aligned16(ml) && aligned16(mo))
+    return moe_layer_forward(dx, ml, w_gate_up, w_down, d, mo, nullptr, nullptr, ws, ws_bytes, s);
+  float* dl = reinterpret_cast<float*>(w + L.hlogits);
+  uint16_t* dout = reinterpret_cast<uint16_t*>(w + L.hout);
+  MOE_TRY(cuda_status(cudaMemcpyAsync(dl, host_logits, lb, cudaMemcpyHostToDevice, s)));
+  MOE_TRY(moe_layer_forward(dx, dl, w_gate_up, w_down, d, dout, nullptr, nullptr, ws, ws_bytes, s));
+  return cuda_status(cudaMemcpyAsync(host_out, dout, xb, cudaMemcpyDeviceToHost, s));
 }
 
 // Replayed host-buffer calls: on a non-default stream with page-locked host
