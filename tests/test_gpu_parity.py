@@ -351,6 +351,23 @@ def test_layer_host_entry_matches_device_entry():
     assert np.array_equal(bits(out), bits(oh))
 
 
+@pytest.mark.parametrize("pinned", [False, True])
+def test_layer_host_entry_pageable_and_pinned(pinned):
+    # pageable host buffers take the copy path through the workspace; pinned
+    # ones let the kernels read the logits and write the output in place
+    wl, d = workload_inputs("decode")
+    layer = _layer(wl, d)
+    ref = layer.forward(d["x"].to(DEV), d["logits"].to(DEV))
+    torch.cuda.synchronize()
+    xh, lh = d["x"].clone(), d["logits"].clone()
+    oh = torch.full((wl.T, wl.H), float("nan"), dtype=torch.bfloat16)
+    if pinned:
+        xh, lh, oh = xh.pin_memory(), lh.pin_memory(), oh.pin_memory()
+    layer.forward_host(xh, lh, oh)
+    assert np.array_equal(bits(oh), bits(ref))
+    assert layer.device_status() == _lib.MOE_OK
+
+
 def test_layer_host_entry_replays_its_graph():
     # non-default stream + page-locked buffers: the first call records a graph,
     # the second replays it and must read the new host inputs
