@@ -23,7 +23,12 @@ class PackedProjection:
 
     @property
     def abi(self) -> _lib.W4:
-        return _lib.w4(self.packed, self.global_scale)
+        # built once per pair of device buffers (rebuilt if a field is replaced)
+        key = (self.packed.data_ptr(), self.global_scale.data_ptr())
+        cached = self.__dict__.get("_abi")
+        if cached is None or cached[0] != key:
+            cached = self.__dict__["_abi"] = (key, _lib.w4(self.packed, self.global_scale))
+        return cached[1]
 
 
 def pack_projection(codes: torch.Tensor, scales: torch.Tensor, global_scale: torch.Tensor, proj: int,
@@ -56,6 +61,7 @@ class MoELayer:
         if shared is not None:
             self.shared = (pack_projection(*shared[0], _lib.MOE_PROJ_GATE_UP, device),
                            pack_projection(*shared[1], _lib.MOE_PROJ_DOWN, device))
+        self._dims = {}
         d = _lib.dims(T_max, H, I, E, k)
         self.ws_bytes = _lib.moe_workspace_bytes(d)
         if self.ws_bytes == 0:
@@ -65,7 +71,10 @@ class MoELayer:
     def dims(self, T: int) -> _lib.Dims:
         if T > self.T_max:
             raise ValueError(f"T={T} > T_max={self.T_max}")
-        return _lib.dims(T, self.H, self.I, self.E, self.k)
+        d = self._dims.get(T)
+        if d is None:
+            d = self._dims[T] = _lib.dims(T, self.H, self.I, self.E, self.k)
+        return d
 
     def forward(self, x: torch.Tensor, logits: torch.Tensor, out: torch.Tensor | None = None,
                 topk_ids: torch.Tensor | None = None, topk_w: torch.Tensor | None = None, stream=None):
