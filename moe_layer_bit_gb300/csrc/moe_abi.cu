@@ -6,6 +6,7 @@
 #include <initializer_list>
 #include <mutex>
 #include <cuda_runtime.h>
+#include <nvtx3/nvToolsExt.h>
 
 #include "moe_w4a16.h"
 #include "kernels.h"
@@ -263,7 +264,24 @@ int layer_forward_impl(const uint16_t* x, const float* logits, moe_w4 w_gate_up,
   if (ws_bytes < L.total) return MOE_ERR_WORKSPACE_TOO_SMALL;
   uint8_t* w = static_cast<uint8_t*>(ws);
   cudaStream_t s = as_stream(stream);
+  // NVTX ranges name the launches of each stage for a profiler's timeline
+  // (no-ops when no tool is attached); the guard closes an open range on
+  // every return.
+  static const char* const kStageNames[5] = {"moe:route_group", "moe:gather", "moe:gate_up", "moe:down",
+                                             "moe:combine"};
+  struct NvtxStage {
+    bool open = false;
+    void next(int i) {
+      if (open) nvtxRangePop();
+      open = i < 5;
+      if (open) nvtxRangePushA(kStageNames[i]);
+    }
+    ~NvtxStage() {
+      if (open) nvtxRangePop();
+    }
+  } nvtx_stage;
   auto mark = [&](int i) -> int {
+    nvtx_stage.next(i);
     if (ev == nullptr || ev[i] == nullptr) return MOE_OK;
     return cuda_status(cudaEventRecord(reinterpret_cast<cudaEvent_t>(ev[i]), s));
   };
