@@ -205,7 +205,14 @@ int moe_unpermute_combine(const float *y_perm, const int32_t *inv_perm, const fl
 
 /* The whole layer: route -> permute -> gate_up+SwiGLU -> down -> combine,
  * stream-ordered, no host synchronisation.  topk_ids / topk_w may be NULL
- * (then they live in ws).  Needs moe_workspace_bytes(d) of ws. */
+ * (then they live in ws).  Needs moe_workspace_bytes(d) of ws.
+ * When moe_layer_projections_fused(d), both projections run as one launch
+ * of one CTA per SM whose CTAs wait on one another; it relies on all of them
+ * becoming resident, which holds when nothing else keeps SMs busy for long.
+ * Such launches of calls on several streams that start at the same moment
+ * can split the SMs between them; their waits then give up after about a
+ * second and report MOE_ERR_DEVICE_TIMEOUT (nothing hangs).  Issue
+ * concurrent layer calls on one stream. */
 int moe_layer_forward(const uint16_t *x, const float *logits, moe_w4 w_gate_up, moe_w4 w_down,
                       moe_dims d, uint16_t *out, int32_t *topk_ids, float *topk_w, void *ws,
                       size_t ws_bytes, void *stream);
