@@ -37,9 +37,12 @@
  *  - A kernel whose internal wait (a pipeline barrier) runs past about one
  *    second gives up, records MOE_ERR_DEVICE_TIMEOUT in the workspace's status
  *    word and returns; moe_get_device_status() reads it.
- *  - The library allocates no memory: every intermediate lives in the
- *    caller's workspace `ws`.  Apart from the fixed scratch array of
- *    moe_permute_noalloc, it keeps no global mutable state.
+ *  - The library allocates no device memory: every intermediate lives in the
+ *    caller's workspace `ws`.  The one allocation of any entry point is the
+ *    caller-owned host plan (moe_host_plan_create / _destroy).  Global
+ *    mutable state: the fixed scratch array of moe_permute_noalloc with its
+ *    per-device address record, and the once-resolved address of the
+ *    driver's tensor-map encoder; nothing else.
  */
 #ifndef MOE_W4A16_H
 #define MOE_W4A16_H
@@ -172,8 +175,9 @@ int moe_permute(const int32_t *topk_ids, const uint16_t *x, moe_dims d, int32_t 
  * Limit: ceil(T*k / 1024) * E <= 65536 (e.g. T*k <= 65536 with E <= 1024);
  * larger sizes return MOE_ERR_UNSUPPORTED_SHAPE before anything runs.
  * The first call on each device looks up the array's device address
- * (cudaGetSymbolAddress) with that device current; make that first call
- * before any stream capture.  Every call uses the same array, so calls whose
+ * (cudaGetSymbolAddress) with that device current, and so does the first
+ * call after the device's context was created anew (cudaDeviceReset); make
+ * those calls before any stream capture.  Every call uses the same array, so calls whose
  * work overlaps on the GPU (other streams, other host threads) race; the
  * array needs no clearing between calls. */
 int moe_permute_noalloc(const int32_t *topk_ids, const uint16_t *x, moe_dims d, int32_t *counts,
@@ -267,15 +271,38 @@ int moe_layer_forward_shared(const uint16_t *x, const float *logits, const uint1
  * combine writes the output through their device addresses; otherwise they
  * are copied through ws as well.  Host buffers should be page-locked for full
  * transfer speed.  Weights stay on the device.  Needs moe_workspace_bytes(d)
- * of ws.
- * On a non-default stream with page-locked host buffers the first call with a
- * given set of arguments (pointers, dims, stream) records its copies and
- * kernels as a CUDA graph, and later calls with the same arguments replay it
- * (the host buffers are read and written when it runs); the library keeps the
- * 8 most recent.  Other calls issue the copies and launches directly. */
+ * of ws.  Every call issues its copies and launches afresh and keeps nothing
+ * after it returns. */
 int moe_layer_forward_host(const uint16_t *host_x, const float *host_logits, moe_w4 w_gate_up,
                            moe_w4 w_down, moe_dims d, uint16_t *host_out, void *ws, size_t ws_bytes,
                            void *stream);
+
+/* A host plan: moe_layer_forward_host with fixed arguments, recorded once as
+ * a CUDA graph (its copies and kernels) and replayed by moe_host_plan_run, so
+ * that a serving loop calling the layer on the same buffers pays one graph
+ * launch per call instead of the individual copies and launches.
+ *   moe_host_plan_create: same arguments as moe_layer_forward_host, plus the
+ *     plan out-pointer.  host_x, host_logits and host_out must be page-locked
+ *     (cudaHostAlloc / cudaHostRegister); `stream` must be a created stream
+ *     (not NULL), current device = the device of ws.  Records nothing on the
+ *     GPU: the stream is captured, not run.  The plan holds the graph's
+ *     driver resources and a small host record -- the only memory any entry
+ *     point of this library allocates -- until moe_host_plan_destroy.
+ *   moe_host_plan_run: reads the host buffers' CURRENT contents, runs the
+ *     layer and writes host_out; synchronises the plan's stream before
+ *     returning.  Call it with the plan's device current.
+ *   moe_host_plan_destroy: frees the plan (NULL is a no-op).
+ * The plan keeps the raw addresses it was created with: destroy it before
+ * freeing, unregistering or reusing any of its buffers, its workspace or its
+ * weights, and before destroying its stream; then create a new one.  The
+ * library keeps no reference to a plan, so plans of different threads or
+ * streams are independent; runs of one plan must not overlap. */
+typedef struct moe_host_plan moe_host_plan;
+int moe_host_plan_create(const uint16_t *host_x, const float *host_logits, moe_w4 w_gate_up,
+                         moe_w4 w_down, moe_dims d, uint16_t *host_out, void *ws, size_t ws_bytes,
+                         void *stream, moe_host_plan **plan);
+int moe_host_plan_run(moe_host_plan *plan);
+int moe_host_plan_destroy(moe_host_plan *plan);
 
 /* Synchronises `stream`, then reads and clears the device status word in ws
  * (any workspace passed to the calls above).  Returns MOE_OK,

@@ -65,6 +65,9 @@ _SIGS = {
     "moe_layer_forward": (INT, [P, P, W4, W4, Dims, P, P, P, P, SZ, P]),
     "moe_layer_forward_profiled": (INT, [P, P, W4, W4, Dims, P, P, P, P, SZ, P, P]),
     "moe_layer_forward_host": (INT, [P, P, W4, W4, Dims, P, P, SZ, P]),
+    "moe_host_plan_create": (INT, [P, P, W4, W4, Dims, P, P, SZ, P, ctypes.POINTER(ctypes.c_void_p)]),
+    "moe_host_plan_run": (INT, [P]),
+    "moe_host_plan_destroy": (INT, [P]),
     "moe_layer_forward_router": (INT, [P, P, P, W4, W4, Dims, P, P, P, P, P, SZ, P]),
     "moe_layer_forward_shared": (INT, [P, P, P, P, W4, W4, W4, W4, Dims, P, P, P, P, P, SZ, P]),
     "moe_get_device_status": (INT, [P, P]),
@@ -223,6 +226,22 @@ def moe_layer_forward_profiled(x, logits, w_gate_up: W4, w_down: W4, d, out, top
 def moe_layer_forward_host(host_x, host_logits, w_gate_up: W4, w_down: W4, d, host_out, ws, ws_bytes, stream=None):
     _check(load().moe_layer_forward_host(_p(host_x), _p(host_logits), w_gate_up, w_down, d, _p(host_out), _p(ws),
                                          ws_bytes, _s(stream)), "moe_layer_forward_host")
+
+
+def moe_host_plan_create(host_x, host_logits, w_gate_up: W4, w_down: W4, d, host_out, ws, ws_bytes, stream):
+    """Returns the plan handle (an int); the caller destroys it with moe_host_plan_destroy."""
+    h = ctypes.c_void_p()
+    _check(load().moe_host_plan_create(_p(host_x), _p(host_logits), w_gate_up, w_down, d, _p(host_out), _p(ws),
+                                       ws_bytes, _s(stream), ctypes.byref(h)), "moe_host_plan_create")
+    return h.value
+
+
+def moe_host_plan_run(plan):
+    _check(load().moe_host_plan_run(ctypes.c_void_p(plan)), "moe_host_plan_run")
+
+
+def moe_host_plan_destroy(plan):
+    _check(load().moe_host_plan_destroy(ctypes.c_void_p(plan)), "moe_host_plan_destroy")
 
 
 def moe_get_device_status(ws, stream=None) -> int:

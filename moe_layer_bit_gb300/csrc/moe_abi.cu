@@ -4,7 +4,6 @@
 #include <cstdlib>
 #include <cstring>
 #include <initializer_list>
-#include <mutex>
 #include <cuda_runtime.h>
 #include <nvtx3/nvToolsExt.h>
 
@@ -412,7 +411,6 @@ int moe_layer_forward_shared(const uint16_t* x, const float* logits, const uint1
 
 namespace {
 
-// The copies and kernels of one host-buffer call, enqueued on `s`.
 // The device address of page-locked host memory that kernels can access
 // directly (mapped), else nullptr.
 void* mapped_device_ptr(const void* p) {
@@ -433,6 +431,7 @@ bool page_locked(const void* p) {
   return a.type == cudaMemoryTypeHost;
 }
 
+// The copies and kernels of one host-buffer call, enqueued on `s`.
 // x is copied into the workspace (the GEMM reads its rows many times).  When
 // the host logits and output are mapped page-locked memory, the routing
 // kernel reads the logits and the combine writes the output through their
@@ -456,35 +455,17 @@ int enqueue_host_call(const uint16_t* host_x, const float* host_logits, moe_w4 w
   return cuda_status(cudaMemcpyAsync(host_out, dout, xb, cudaMemcpyDeviceToHost, s));
 }
 
-// Replayed host-buffer calls: on a non-default stream with page-locked host
-// buffers, a call records its copies and kernels once as a CUDA graph and
-// later calls with the same arguments replay it (the host buffers are read
-// and written when the graph runs).  A small cache, most recent first.
-struct HostCall {
-  const void* hx;
-  const void* hl;
-  const void* ho;
-  moe_w4 gu, dn;
-  moe_dims d;
-  const void* ws;
-  size_t ws_bytes;
-  const void* stream;
-  int dev;
-  cudaGraphExec_t exec;  // nullptr: capturing failed, run directly
-  bool used;
-};
-bool same_call(const HostCall& a, const HostCall& b) {
-  return a.hx == b.hx && a.hl == b.hl && a.ho == b.ho && a.gu.packed == b.gu.packed &&
-         a.gu.global_scale == b.gu.global_scale && a.dn.packed == b.dn.packed &&
-         a.dn.global_scale == b.dn.global_scale && a.d.T == b.d.T && a.d.H == b.d.H && a.d.I == b.d.I &&
-         a.d.E == b.d.E && a.d.k == b.d.k && a.ws == b.ws && a.ws_bytes == b.ws_bytes && a.stream == b.stream &&
-         a.dev == b.dev;
-}
-constexpr int kHostCalls = 8;
-HostCall g_host_calls[kHostCalls];
-std::mutex g_host_calls_mutex;
-
 }  // namespace
+
+// A host plan: one host-buffer call recorded once as a CUDA graph (its
+// copies and kernels, bound to the plan's host buffers, workspace and
+// stream) and replayed by every run.  The caller owns it: the graph lives
+// until moe_host_plan_destroy, and the library keeps no reference to it.
+struct moe_host_plan {
+  cudaGraphExec_t exec;
+  cudaStream_t stream;
+  int dev;
+};
 
 extern "C" {
 
@@ -497,50 +478,65 @@ int moe_layer_forward_host(const uint16_t* host_x, const float* host_logits, moe
   const Layout L = layout_of(d);
   if (ws_bytes < L.total) return MOE_ERR_WORKSPACE_TOO_SMALL;
   cudaStream_t s = as_stream(stream);
-  if (s != nullptr && page_locked(host_x) && page_locked(host_logits) && page_locked(host_out)) {
-    HostCall key{};
-    key.hx = host_x;
-    key.hl = host_logits;
-    key.ho = host_out;
-    key.gu = w_gate_up;
-    key.dn = w_down;
-    key.d = d;
-    key.ws = ws;
-    key.ws_bytes = ws_bytes;
-    key.stream = stream;
-    if (cudaGetDevice(&key.dev) != cudaSuccess) return cuda_status(cudaErrorUnknown);
-    std::lock_guard<std::mutex> lock(g_host_calls_mutex);
-    int hit = -1;
-    for (int i = 0; i < kHostCalls; ++i)
-      if (g_host_calls[i].used && same_call(g_host_calls[i], key)) hit = i;
-    if (hit < 0) {
-      // record the call once; a call that cannot be recorded runs directly
-      cudaGraph_t graph = nullptr;
-      cudaGraphExec_t exec = nullptr;
-      if (cudaStreamBeginCapture(s, cudaStreamCaptureModeThreadLocal) == cudaSuccess) {
-        const int rc = enqueue_host_call(host_x, host_logits, w_gate_up, w_down, d, host_out, ws, ws_bytes, s);
-        const cudaError_t e = cudaStreamEndCapture(s, &graph);
-        if (rc == MOE_OK && e == cudaSuccess && graph != nullptr &&
-            cudaGraphInstantiate(&exec, graph, 0) != cudaSuccess)
-          exec = nullptr;
-        if (graph != nullptr) cudaGraphDestroy(graph);
-      }
-      (void)cudaGetLastError();
-      HostCall& slot = g_host_calls[kHostCalls - 1];
-      if (slot.used && slot.exec != nullptr) cudaGraphExecDestroy(slot.exec);
-      for (int i = kHostCalls - 1; i > 0; --i) g_host_calls[i] = g_host_calls[i - 1];
-      key.exec = exec;
-      key.used = true;
-      g_host_calls[0] = key;
-      hit = 0;
-    }
-    if (g_host_calls[hit].exec != nullptr) {
-      MOE_TRY(cuda_status(cudaGraphLaunch(g_host_calls[hit].exec, s)));
-      return cuda_status(cudaStreamSynchronize(s));
-    }
-  }
   MOE_TRY(enqueue_host_call(host_x, host_logits, w_gate_up, w_down, d, host_out, ws, ws_bytes, s));
   return cuda_status(cudaStreamSynchronize(s));
+}
+
+int moe_host_plan_create(const uint16_t* host_x, const float* host_logits, moe_w4 w_gate_up, moe_w4 w_down,
+                         moe_dims d, uint16_t* host_out, void* ws, size_t ws_bytes, void* stream,
+                         moe_host_plan** plan) {
+  if (plan == nullptr) return MOE_ERR_INVALID_ARG;
+  *plan = nullptr;
+  MOE_TRY(check_dims(d));
+  if (host_x == nullptr || host_logits == nullptr || host_out == nullptr) return MOE_ERR_INVALID_ARG;
+  MOE_TRY(check_ptrs({w_gate_up.packed, w_gate_up.global_scale, w_down.packed, w_down.global_scale, ws}));
+  const Layout L = layout_of(d);
+  if (ws_bytes < L.total) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  cudaStream_t s = as_stream(stream);
+  if (s == nullptr) return MOE_ERR_INVALID_ARG;  // the legacy default stream cannot be captured
+  if (!page_locked(host_x) || !page_locked(host_logits) || !page_locked(host_out)) return MOE_ERR_INVALID_ARG;
+  int dev = 0;
+  MOE_TRY(cuda_status(cudaGetDevice(&dev)));
+  cudaGraph_t graph = nullptr;
+  cudaGraphExec_t exec = nullptr;
+  MOE_TRY(cuda_status(cudaStreamBeginCapture(s, cudaStreamCaptureModeThreadLocal)));
+  const int rc = d.T == 0 ? MOE_OK
+                          : enqueue_host_call(host_x, host_logits, w_gate_up, w_down, d, host_out, ws, ws_bytes, s);
+  const cudaError_t ec = cudaStreamEndCapture(s, &graph);
+  if (rc != MOE_OK || ec != cudaSuccess || graph == nullptr) {
+    if (graph != nullptr) cudaGraphDestroy(graph);
+    (void)cudaGetLastError();
+    return rc != MOE_OK ? rc : MOE_ERR_CUDA;
+  }
+  const cudaError_t ei = cudaGraphInstantiate(&exec, graph, 0);
+  cudaGraphDestroy(graph);
+  if (ei != cudaSuccess) return cuda_status(ei);
+  moe_host_plan* p = static_cast<moe_host_plan*>(std::malloc(sizeof(moe_host_plan)));
+  if (p == nullptr) {
+    cudaGraphExecDestroy(exec);
+    return MOE_ERR_CUDA;
+  }
+  p->exec = exec;
+  p->stream = s;
+  p->dev = dev;
+  *plan = p;
+  return MOE_OK;
+}
+
+int moe_host_plan_run(moe_host_plan* plan) {
+  if (plan == nullptr) return MOE_ERR_INVALID_ARG;
+  int dev = 0;
+  MOE_TRY(cuda_status(cudaGetDevice(&dev)));
+  if (dev != plan->dev) return MOE_ERR_INVALID_ARG;
+  MOE_TRY(cuda_status(cudaGraphLaunch(plan->exec, plan->stream)));
+  return cuda_status(cudaStreamSynchronize(plan->stream));
+}
+
+int moe_host_plan_destroy(moe_host_plan* plan) {
+  if (plan == nullptr) return MOE_OK;
+  const cudaError_t e = cudaGraphExecDestroy(plan->exec);
+  std::free(plan);
+  return cuda_status(e);
 }
 
 int moe_get_device_status(void* ws, void* stream) {

@@ -12,6 +12,7 @@
 #include <cstdint>
 #include <mutex>
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include "kernels.h"
@@ -26,11 +27,51 @@ namespace {
 constexpr size_t kNoAllocScratchInts = 65536;
 __device__ __align__(256) int32_t g_permute_scratch[kNoAllocScratchInts];
 
-// Device address of g_permute_scratch, resolved once per device.  In host
-// code the symbol itself is only a host-side stand-in, never a device address.
+// Device address of g_permute_scratch, resolved once per device and
+// context.  In host code the symbol itself is only a host-side stand-in,
+// never a device address.  The address belongs to the module loaded into
+// the context that was current when it was looked up: after cudaDeviceReset
+// (or any other way the device's primary context is destroyed and created
+// again) the module is loaded anew, possibly elsewhere, so each record also
+// holds the context's process-unique ID and is looked up again when the
+// current context's ID differs.
+using PFN_ctxGetCurrent = CUresult (*)(CUcontext*);
+using PFN_ctxGetId = CUresult (*)(CUcontext, unsigned long long*);
+
+struct ScratchRecord {
+  unsigned long long ctx_id;
+  int32_t* addr;
+};
 constexpr int kMaxDevices = 64;
-int32_t* g_scratch_addr[kMaxDevices] = {};
+ScratchRecord g_scratch_addr[kMaxDevices] = {};
 std::mutex g_scratch_mutex;
+
+// The current context's process-unique ID (CUDA driver cuCtxGetId), or 0 if it
+// cannot be had.
+unsigned long long current_context_id() {
+  static PFN_ctxGetCurrent get_current = nullptr;
+  static PFN_ctxGetId get_id = nullptr;
+  static bool resolved = false;
+  if (!resolved) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<PFN_ctxGetCurrent>(p);
+    p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<PFN_ctxGetId>(p);
+    (void)cudaGetLastError();
+    resolved = true;
+  }
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (get_current == nullptr || get_id == nullptr || get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr ||
+      get_id(ctx, &id) != CUDA_SUCCESS)
+    return 0;
+  return id;
+}
 
 int scratch_address(int32_t** out) {
   int dev = 0;
@@ -39,15 +80,20 @@ int scratch_address(int32_t** out) {
     return MOE_ERR_CUDA;
   }
   std::lock_guard<std::mutex> lock(g_scratch_mutex);
-  if (g_scratch_addr[dev] == nullptr) {
+  ScratchRecord& rec = g_scratch_addr[dev];
+  // 0 while no context is current yet on this thread (nothing has touched
+  // the device): then the lookup below creates the primary context
+  const unsigned long long ctx = current_context_id();
+  if (rec.addr == nullptr || ctx == 0 || rec.ctx_id != ctx) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_permute_scratch) != cudaSuccess || p == nullptr) {
       (void)cudaGetLastError();
       return MOE_ERR_CUDA;
     }
-    g_scratch_addr[dev] = static_cast<int32_t*>(p);
+    rec.addr = static_cast<int32_t*>(p);
+    rec.ctx_id = current_context_id();
   }
-  *out = g_scratch_addr[dev];
+  *out = rec.addr;
   return MOE_OK;
 }
 

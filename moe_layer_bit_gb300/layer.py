@@ -118,5 +118,42 @@ class MoELayer:
                                     self.ws, self.ws_bytes, stream)
         return out_host
 
+    def host_plan(self, x_host: torch.Tensor, logits_host: torch.Tensor, out_host: torch.Tensor, stream):
+        """A recorded host-buffer call on these page-locked buffers and this stream (HostPlan.run() per
+        call; close() or the context manager frees it)."""
+        return HostPlan(self, x_host, logits_host, out_host, stream)
+
     def device_status(self, stream=None) -> int:
         return _lib.moe_get_device_status(self.ws, stream)
+
+
+class HostPlan:
+    """Caller-owned moe_host_plan: the layer on fixed page-locked host buffers, replayed as one graph."""
+
+    def __init__(self, layer: MoELayer, x_host, logits_host, out_host, stream):
+        self.handle = None
+        self._keep = (x_host, logits_host, out_host, stream, layer)
+        self.handle = _lib.moe_host_plan_create(x_host, logits_host, layer.w_gate_up.abi, layer.w_down.abi,
+                                                layer.dims(x_host.shape[0]), out_host, layer.ws, layer.ws_bytes,
+                                                stream)
+
+    def run(self):
+        _lib.moe_host_plan_run(self.handle)
+
+    def close(self):
+        if self.handle is not None:
+            _lib.moe_host_plan_destroy(self.handle)
+            self.handle = None
+            self._keep = None
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.close()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

@@ -33,7 +33,7 @@
  * E4M3 block scale per 16 consecutive elements along K and one fp32 global
  * scale per expert matrix.
  *
- * Readings where the pages are silent (each is also listed in the design doc):
+ * Readings where the pages are silent:
  *  - packed codes: element 2i in the low nibble, 2i+1 in the high nibble;
  *  - gate_up rows 0..I-1 are the gate projection, rows I..2I-1 the up
  *    projection, and SwiGLU = silu(gate) * up;

@@ -113,3 +113,22 @@ def test_null_misaligned_and_small_workspace(lib):
         _lib.MOE_ERR_WORKSPACE_TOO_SMALL
     assert lib.moe_layer_forward_router(ok, ok, None, w, w, d, ok, odd, None, None, ok, 1 << 30, None) == \
         _lib.MOE_ERR_MISALIGNED
+
+
+def test_host_plan_argument_checks(lib):
+    # rejected before any CUDA call: no plan pointer, null host buffers, small workspace
+    d = _lib.dims(4, 128, 64, 8, 2)
+    ok = ctypes.c_void_p(0x10000)
+    w = _lib.W4(0x10000, 0x10000)
+    plan = ctypes.c_void_p(0x1234)
+    big = _lib.moe_workspace_bytes(d)
+    assert lib.moe_host_plan_create(ok, ok, w, w, d, ok, ok, big, ok, None) == _lib.MOE_ERR_INVALID_ARG
+    assert lib.moe_host_plan_create(None, ok, w, w, d, ok, ok, big, ok, ctypes.byref(plan)) == \
+        _lib.MOE_ERR_INVALID_ARG
+    assert plan.value is None                       # cleared on every failure
+    assert lib.moe_host_plan_create(ok, ok, w, w, d, ok, ok, big - 1, ok, ctypes.byref(plan)) == \
+        _lib.MOE_ERR_WORKSPACE_TOO_SMALL
+    assert lib.moe_host_plan_create(ok, ok, w, w, _lib.dims(4, 100, 64, 8, 2), ok, ok, big, ok,
+                                    ctypes.byref(plan)) == _lib.MOE_ERR_UNSUPPORTED_SHAPE
+    assert lib.moe_host_plan_run(None) == _lib.MOE_ERR_INVALID_ARG
+    assert lib.moe_host_plan_destroy(None) == _lib.MOE_OK

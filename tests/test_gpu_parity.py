@@ -368,27 +368,69 @@ def test_layer_host_entry_pageable_and_pinned(pinned):
     assert layer.device_status() == _lib.MOE_OK
 
 
-def test_layer_host_entry_replays_its_graph():
-    # non-default stream + page-locked buffers: the first call records a graph,
-    # the second replays it and must read the new host inputs
+def test_host_plan_replays_with_new_host_contents():
+    # a caller-owned plan (recorded graph) on page-locked buffers and a created
+    # stream: every run must read the host inputs' current contents
     wl, d = workload_inputs("decode")
     layer = _layer(wl, d)
     s = torch.cuda.Stream()
     xh = d["x"].pin_memory()
     lh = d["logits"].pin_memory()
     oh = torch.empty(wl.T, wl.H, dtype=torch.bfloat16).pin_memory()
-    for rnd in range(3):
-        x = torch.roll(d["x"], shifts=rnd, dims=0)
-        lg = torch.roll(d["logits"], shifts=2 * rnd, dims=1)
-        xh.copy_(x)
-        lh.copy_(lg)
-        ref = layer.forward(x.to(DEV), lg.to(DEV))
-        # both calls use the layer's one workspace: the device call must end
-        # before the host call starts on its own stream
-        torch.cuda.synchronize()
-        layer.forward_host(xh, lh, oh, s)
-        assert np.array_equal(bits(oh), bits(ref)), f"round {rnd}"
+    with layer.host_plan(xh, lh, oh, s) as plan:
+        for rnd in range(3):
+            x = torch.roll(d["x"], shifts=rnd, dims=0)
+            lg = torch.roll(d["logits"], shifts=2 * rnd, dims=1)
+            xh.copy_(x)
+            lh.copy_(lg)
+            ref = layer.forward(x.to(DEV), lg.to(DEV))
+            # both calls use the layer's one workspace: the device call must end
+            # before the plan runs on its own stream
+            torch.cuda.synchronize()
+            plan.run()
+            assert np.array_equal(bits(oh), bits(ref)), f"round {rnd}"
     assert layer.device_status() == _lib.MOE_OK
+
+
+def test_host_entries_with_freed_and_recreated_buffers():
+    # page-locked buffers freed and allocated again (often at the same
+    # address) between calls: the stateless host entry and a plan created on
+    # the new buffers both equal the device entry bit for bit
+    wl, d = workload_inputs("decode")
+    layer = _layer(wl, d)
+    s = torch.cuda.Stream()
+    for rnd in range(3):
+        x = torch.roll(d["x"], shifts=3 * rnd, dims=0)
+        lg = torch.roll(d["logits"], shifts=rnd, dims=1)
+        ref = layer.forward(x.to(DEV), lg.to(DEV))
+        torch.cuda.synchronize()
+        xh, lh = x.clone().pin_memory(), lg.clone().pin_memory()
+        oh = torch.full((wl.T, wl.H), float("nan"), dtype=torch.bfloat16).pin_memory()
+        layer.forward_host(xh, lh, oh, s)
+        assert np.array_equal(bits(oh), bits(ref)), f"host entry, round {rnd}"
+        oh.fill_(float("nan"))
+        with layer.host_plan(xh, lh, oh, s) as plan:
+            plan.run()
+        assert np.array_equal(bits(oh), bits(ref)), f"host plan, round {rnd}"
+        del xh, lh, oh
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+        # torch keeps freed page-locked blocks for reuse, so the next round's
+        # buffers usually come back at the same host addresses
+    assert layer.device_status() == _lib.MOE_OK
+
+
+def test_host_plan_rejects_pageable_buffers_and_default_stream():
+    wl, d = workload_inputs("tiny")
+    layer = _layer(wl, d)
+    xh, lh = d["x"].clone(), d["logits"].clone()
+    oh = torch.empty(wl.T, wl.H, dtype=torch.bfloat16)
+    with pytest.raises(_lib.MoeError) as exc:
+        layer.host_plan(xh, lh, oh, torch.cuda.Stream())
+    assert exc.value.status == _lib.MOE_ERR_INVALID_ARG
+    with pytest.raises(_lib.MoeError) as exc:
+        layer.host_plan(xh.pin_memory(), lh.pin_memory(), oh.pin_memory(), 0)
+    assert exc.value.status == _lib.MOE_ERR_INVALID_ARG
 
 
 @pytest.mark.parametrize("T,H,I,E,k", [
