@@ -1,6 +1,7 @@
 """Benchmark of the W4A16 NVFP4 MoE layer on GB300 (one JSON line on rank 0).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload NAME]
+                    [--workloads grouped,prefill,skewed]
 
 A step is one pass of the whole layer (route -> permute -> gate_up+SwiGLU ->
 down -> combine) over one batch of seeded synthetic input of the decode-shaped
@@ -10,8 +11,11 @@ ours:      inputs resident in HBM; each timed step is moe_layer_forward_profiled
            (same kernels as moe_layer_forward) bracketed by CUDA events on the
            launching stream, the L2 flushed between steps (a 2x-L2 buffer written, then a
            second 2x-L2 buffer read so that the flush's own write-backs finish before the step)
-           outside the events.  `e2e` runs moe_layer_forward_host: pinned host
-           x / logits in, host out back, copies inside the timed region.
+           outside the events.  `e2e` runs a caller-owned host plan (moe_host_plan_run):
+           pinned host x / logits in, host out back, copies inside the timed region.
+           The other workloads of the metric (grouped: the Atlas article's 800 tokens x
+           256 experts; prefill; skewed) are timed the same way after the headline one and
+           reported under "workloads".
 reference: the fp64 CPU oracle (single thread) on a bounded token sample of the
            same workload; rank 0 only.
 N > 1 ranks run independent replicas (the path needs no exchange between GPUs);
@@ -240,6 +244,18 @@ def oracle_baseline(d, wl, budget_s: float):
     return total, toks, reps, n
 
 
+NOMINAL_HBM_GBS = 7900.0  # GB300 nominal HBM3e bandwidth, for context beside the measured copy peak
+EXTRA_WORKLOADS = ("grouped", "prefill", "skewed")
+
+
+def bench_config(wl, world: int) -> dict:
+    """The `config` object of both arms' JSON lines (same keys, same values)."""
+    return {"workload": wl.name, "T": wl.T, "H": wl.H, "I": wl.I, "E": wl.E, "k": wl.k,
+            "parallelism": f"replicas x{world}" if world > 1 else "single",
+            "l2": "flushed between steps, outside the timed events: a 2x-L2 buffer written, then another "
+                  "2x-L2 buffer read (the flush's dirty lines reach HBM before the step)"}
+
+
 def run_reference(args, wl, dist, rank, world):
     if rank != 0:
         return
@@ -258,8 +274,7 @@ def run_reference(args, wl, dist, rank, world):
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
-        "config": {"workload": wl.name, "T": wl.T, "H": wl.H, "I": wl.I, "E": wl.E, "k": wl.k,
-                   "parallelism": "replicas" if args.gpus > 1 else "single"},
+        "config": bench_config(wl, world if world > 1 else args.gpus),
         "impl": "reference",
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -296,9 +311,204 @@ def _traffic_from_profile(wl):
         return None
 
 
+class DeviceBench:
+    """One workload on one GPU: the layer built from seeded inputs, an L2 flush
+    between steps, and CUDA events on the launching stream."""
+
+    def __init__(self, wl, dev, rank):
+        from moe_layer_bit_gb300 import _lib
+        from moe_layer_bit_gb300.layer import MoELayer
+        self.lib = _lib
+        self.wl, self.dev = wl, dev
+        self.d = wk.generate(wl, seed=wl.seed + rank)
+        self.layer = MoELayer(self.d["gu"], self.d["dn"], wl.H, wl.I, wl.E, wl.k, wl.T, dev)
+        self.x = self.d["x"].to(dev)
+        self.logits = self.d["logits"].to(dev)
+        self.out = torch.empty(wl.T, wl.H, dtype=torch.bfloat16, device=dev)
+        self.ids = torch.empty(wl.T, wl.k, dtype=torch.int32, device=dev)
+        self.tw = torch.empty(wl.T, wl.k, dtype=torch.float32, device=dev)
+        self.dims = self.layer.dims(wl.T)
+        l2 = getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 126 * 2 ** 20)
+        self.flush = torch.empty(2 * l2 // 4 + 1024, dtype=torch.float32, device=dev)
+        self.clean = torch.ones(2 * l2 // 4 + 1024, dtype=torch.float32, device=dev)
+        self.stream = torch.cuda.current_stream(dev)
+
+    def flush_l2(self, v):
+        # Write a 2x-L2 buffer (evicts everything the layer touched), then read
+        # another 2x-L2 buffer, so the written lines are back in HBM before the
+        # next step instead of being written back during it.
+        self.flush.fill_(v)
+        return self.clean.sum()
+
+    def step(self, evs):
+        self.lib.moe_layer_forward_profiled(self.x, self.logits, self.layer.w_gate_up.abi, self.layer.w_down.abi,
+                                            self.dims, self.out, self.ids, self.tw, self.layer.ws,
+                                            self.layer.ws_bytes, evs, self.stream)
+
+    def check_status(self, when):
+        st = self.layer.device_status()
+        if st != self.lib.MOE_OK:
+            raise RuntimeError(f"{self.wl.name}: device status {when}: {self.lib.status_string(st)}")
+
+    def _events(self, steps):
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(steps)]
+        # torch only reports elapsed time between events it has recorded itself; record
+        # each once here (the library records them again inside every timed step)
+        for e in evs:
+            for ev in e:
+                ev.record(self.stream)
+        return evs
+
+    def _timed_region(self, dist, evs, stage_marks):
+        """K steps; the L2 flush sits between steps, outside the events.  With
+        stage_marks False only the step's first and last events are recorded, so
+        nothing separates the layer's kernels (their programmatic launch overlap
+        is kept); with True all six are, for the per-stage times."""
+        _barrier(dist, self.dev)
+        torch.cuda.synchronize(self.dev)
+        t0 = time.perf_counter()
+        for s in range(len(evs)):
+            self.flush_l2(float(s))
+            e = evs[s] if stage_marks else [evs[s][0], None, None, None, None, evs[s][5]]
+            self.step(e)
+        torch.cuda.synchronize(self.dev)
+        _barrier(dist, self.dev)
+        return time.perf_counter() - t0
+
+    def measure(self, steps, warmup, dist, world):
+        wl = self.wl
+        warm_evs = [torch.cuda.Event(enable_timing=True) for _ in range(6)]
+        for _ in range(warmup):
+            self.flush_l2(1.0)
+            self.step(warm_evs)
+        torch.cuda.synchronize(self.dev)
+        self.check_status("after warm-up")
+        evs = self._events(steps)
+        stage_evs = self._events(steps)
+        torch.cuda.synchronize(self.dev)
+        clocks = ClockSampler(self.dev)
+        clocks.start()
+        t_wall = self._timed_region(dist, evs, False)           # the measured steps
+        t_wall_stages = self._timed_region(dist, stage_evs, True)  # the same steps again, per-stage events
+        clk = clocks.stop()
+        self.check_status("after timing")
+        step_ms = [e[0].elapsed_time(e[5]) for e in evs]
+        stage_ms = np.array([[e[i].elapsed_time(e[i + 1]) for i in range(5)] for e in stage_evs])
+        total_s = sum(step_ms) / 1e3
+        value = _job_throughput(dist, world, wl.T * steps, total_s, self.dev)
+        counts = np.bincount(self.ids.cpu().numpy().reshape(-1), minlength=wl.E)
+        touched = int(np.count_nonzero(counts))
+        mean_step_ms = total_s * 1e3 / steps
+        roofline = self.roofline(stage_ms, touched)
+        layer_bytes = wk.algorithmic_bytes(wl.T, wl.H, wl.I, wl.E, wl.k, counts)
+        layer_flops = wk.algorithmic_flops(wl.T, wl.H, wl.I, wl.k)
+        hbm_peak, tf_peak, _, _ = _peaks()
+        return {
+            "value": value, "unit": UNIT, "ms_per_step": mean_step_ms, "steps": steps, "warmup": warmup,
+            "touched_experts": touched, "layer_bytes": layer_bytes, "layer_flops": layer_flops,
+            "roofline": roofline,
+            "layer_roofline": {"achieved_gbs": layer_bytes / (mean_step_ms * 1e-3) / 1e9,
+                               "frac_hbm": layer_bytes / (mean_step_ms * 1e-3) / 1e9 / hbm_peak,
+                               "achieved_tflops": layer_flops / (mean_step_ms * 1e-3) / 1e12,
+                               "frac_tensor": layer_flops / (mean_step_ms * 1e-3) / 1e12 / tf_peak},
+            "stages_ms": {nm: float(stage_ms[:, i].mean()) for i, nm in
+                          enumerate(["route_group", "gather", "gate_up_swiglu", "down", "combine"])},
+            "wall_s_timed_loop": t_wall, "wall_s_stage_loop": t_wall_stages,
+            "gpu_launches": self.lib.moe_layer_kernel_launches(self.dims) * steps,
+            "clocks": clk,
+        }
+
+    def roofline(self, stage_ms, touched):
+        """Roofline of the dominant kernel: gate_up + SwiGLU, or both projections
+        when the layer runs them as one launch (then stage 2 spans that launch and
+        stage 3 is empty).  Algorithmic bytes / flops per launch over the launch's
+        mean event-timed duration; the bound is the roof it is closer to."""
+        wl = self.wl
+        n = wl.T * wl.k
+        fused = self.lib.moe_layer_projections_fused(self.dims)
+        gu_bytes = touched * (2 * wl.I * wl.H * 9 // 16 + 4) + n * wl.H * 2 + n * wl.I * 2
+        if fused:
+            gu_bytes += touched * (wl.H * wl.I * 9 // 16 + 4) + n * wl.I * 2 + n * wl.H * 4
+        gu_ms = float(stage_ms[:, 2].mean())
+        hbm_peak, tf_peak, tf_sus, peak_kind = _peaks()
+        achieved = gu_bytes / (gu_ms * 1e-3) / 1e9
+        gu_flops = 2 * n * (3 if fused else 2) * wl.I * wl.H
+        achieved_tf = gu_flops / (gu_ms * 1e-3) / 1e12
+        if achieved_tf / tf_peak > achieved / hbm_peak:
+            r = {"bound": "tensor", "achieved": achieved_tf, "peak": tf_peak, "unit": "TFLOP/s",
+                 "frac": achieved_tf / tf_peak, "peak_kind": f"{peak_kind} burst cuBLAS bf16 GEMM",
+                 "frac_sustained_peak": achieved_tf / tf_sus, "algorithmic_flops_per_launch": gu_flops}
+        else:
+            r = {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
+                 "frac": achieved / hbm_peak, "peak_kind": f"{peak_kind} burst copy bandwidth",
+                 "frac_nominal_7900": achieved / NOMINAL_HBM_GBS, "algorithmic_bytes_per_launch": gu_bytes}
+        r.update({"kernel": "w4a16_gemm_kernel (gate_up + SwiGLU" + (", then down, one launch)" if fused else ")"),
+                  "traffic": _traffic_from_profile(wl),
+                  "launch_ms": gu_ms,
+                  "other_roof_frac": (achieved / hbm_peak) if r["bound"] == "tensor" else (achieved_tf / tf_peak)})
+        if not fused:
+            dn_ms = float(stage_ms[:, 3].mean())
+            dn_bytes = touched * (wl.H * wl.I * 9 // 16 + 4) + n * wl.I * 2 + n * wl.H * 4
+            dn_flops = 2 * n * wl.I * wl.H
+            r["down"] = {"launch_ms": dn_ms, "achieved_gbs": dn_bytes / (dn_ms * 1e-3) / 1e9,
+                         "frac_hbm": dn_bytes / (dn_ms * 1e-3) / 1e9 / hbm_peak,
+                         "achieved_tflops": dn_flops / (dn_ms * 1e-3) / 1e12,
+                         "frac_tensor": dn_flops / (dn_ms * 1e-3) / 1e12 / tf_peak}
+        return r
+
+    def stream_probe(self, nbytes_alg, steps):
+        """What one kernel of the GEMM's shape reads in the same time budget when it
+        does nothing else: the streaming probe over the same byte count, same flush."""
+        nbytes = (nbytes_alg // 18432) * 18432
+        probe_buf = torch.empty(nbytes, dtype=torch.uint8, device=self.dev)
+        pev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(steps)]
+        for _ in range(3):
+            self.flush_l2(0.0)
+            self.lib.moe_debug_stream_read(probe_buf, nbytes, self.layer.ws, self.stream)
+        for st in range(steps):
+            self.flush_l2(float(st))
+            pev[st][0].record(self.stream)
+            self.lib.moe_debug_stream_read(probe_buf, nbytes, self.layer.ws, self.stream)
+            pev[st][1].record(self.stream)
+        torch.cuda.synchronize(self.dev)
+        self.check_status("after the stream probe")
+        probe_ms = float(np.mean([e[0].elapsed_time(e[1]) for e in pev]))
+        return {"what": "one CTA per SM, 8 x 18432-byte bulk copies in flight, nothing else; same byte count "
+                        "and L2 flush", "bytes": nbytes, "ms": probe_ms, "gbs": nbytes / (probe_ms * 1e-3) / 1e9}
+
+    def e2e(self, steps, warmup, dist, world):
+        """End to end through the public host-buffer API: a caller-owned host plan
+        on page-locked x / logits / out and a stream of its own; each step copies x
+        host->device, the routing kernel reads the logits and the combine writes the
+        output through their mapped addresses, and the call synchronises."""
+        wl = self.wl
+        xh = self.d["x"].pin_memory()
+        lh = self.d["logits"].pin_memory()
+        oh = torch.empty(wl.T, wl.H, dtype=torch.bfloat16).pin_memory()
+        e2e_stream = torch.cuda.Stream(self.dev)
+        times = []
+        with self.layer.host_plan(xh, lh, oh, e2e_stream) as plan:
+            for _ in range(max(3, warmup)):
+                plan.run()
+            for s in range(steps):
+                self.flush_l2(float(s))
+                torch.cuda.synchronize(self.dev)
+                t0 = time.perf_counter()
+                plan.run()  # synchronises before returning
+                times.append(time.perf_counter() - t0)
+        self.check_status("after the host-plan steps")
+        value = _job_throughput(dist, world, wl.T * steps, sum(times), self.dev)
+        return {"value": value, "unit": UNIT, "h2d_bytes_per_step": wl.T * wl.H * 2 + wl.T * wl.E * 4,
+                "d2h_bytes_per_step": wl.T * wl.H * 2, "api": "moe_host_plan_run (page-locked host buffers)"}
+
+    def close(self):
+        del self.layer, self.x, self.logits, self.out, self.flush, self.clean
+        torch.cuda.synchronize(self.dev)
+        torch.cuda.empty_cache()
+
+
 def run_ours(args, wl, dist, rank, world, local_rank):
     from moe_layer_bit_gb300 import _lib, build
-    from moe_layer_bit_gb300.layer import MoELayer
 
     if not torch.cuda.is_available():
         raise RuntimeError("bench.py --impl ours needs a CUDA device")
@@ -308,190 +518,59 @@ def run_ours(args, wl, dist, rank, world, local_rank):
         build.build()
     _barrier(dist)
     _lib.load()
-    d = wk.generate(wl, seed=wl.seed + rank)
-    layer = MoELayer(d["gu"], d["dn"], wl.H, wl.I, wl.E, wl.k, wl.T, dev)
-    x = d["x"].to(dev)
-    logits = d["logits"].to(dev)
-    out = torch.empty(wl.T, wl.H, dtype=torch.bfloat16, device=dev)
-    ids = torch.empty(wl.T, wl.k, dtype=torch.int32, device=dev)
-    tw = torch.empty(wl.T, wl.k, dtype=torch.float32, device=dev)
-    dims = layer.dims(wl.T)
-    l2 = getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 126 * 2 ** 20)
-    flush = torch.empty(2 * l2 // 4 + 1024, dtype=torch.float32, device=dev)
-    clean = torch.ones(2 * l2 // 4 + 1024, dtype=torch.float32, device=dev)
 
-    def flush_l2(v):
-        # Write a 2x-L2 buffer (evicts everything the layer touched), then read
-        # another 2x-L2 buffer, so the written lines are back in HBM before the
-        # next step instead of being written back during it.
-        flush.fill_(v)
-        return clean.sum()
-
-    stream = torch.cuda.current_stream(dev)
-
-    def step(evs):
-        _lib.moe_layer_forward_profiled(x, logits, layer.w_gate_up.abi, layer.w_down.abi, dims, out, ids, tw,
-                                        layer.ws, layer.ws_bytes, evs, stream)
-
-    warm_evs = [torch.cuda.Event(enable_timing=True) for _ in range(6)]
-    for _ in range(args.warmup):
-        flush_l2(1.0)
-        step(warm_evs)
-    torch.cuda.synchronize(dev)
-    status = layer.device_status()
-    if status != _lib.MOE_OK:
-        raise RuntimeError(f"device status after warm-up: {_lib.status_string(status)}")
-
-    def new_events():
-        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(args.steps)]
-        # torch only reports elapsed time between events it has recorded itself; record
-        # each once here (the library records them again inside every timed step)
-        for e in evs:
-            for ev in e:
-                ev.record(stream)
-        return evs
-
-    def timed_region(evs, stage_marks):
-        """K steps; the L2 flush sits between steps, outside the events.  With
-        stage_marks False only the step's first and last events are recorded, so
-        nothing separates the layer's kernels (their programmatic launch overlap
-        is kept); with True all six are, for the per-stage times."""
-        _barrier(dist, dev)
-        torch.cuda.synchronize(dev)
-        t0 = time.perf_counter()
-        for s in range(args.steps):
-            flush_l2(float(s))
-            e = evs[s] if stage_marks else [evs[s][0], None, None, None, None, evs[s][5]]
-            step(e)
-        torch.cuda.synchronize(dev)
-        _barrier(dist, dev)
-        return time.perf_counter() - t0
-
-    evs = new_events()
-    stage_evs = new_events()
-    torch.cuda.synchronize(dev)
-    clocks = ClockSampler(dev)
-    clocks.start()
-    t_wall = timed_region(evs, False)          # the measured steps
-    t_wall_stages = timed_region(stage_evs, True)  # the same steps again, with per-stage events
-    clk = clocks.stop()
-    status = layer.device_status()
-    if status != _lib.MOE_OK:
-        raise RuntimeError(f"device status after timing: {_lib.status_string(status)}")
-
-    step_ms = [e[0].elapsed_time(e[5]) for e in evs]
-    stage_ms = np.array([[e[i].elapsed_time(e[i + 1]) for i in range(5)] for e in stage_evs])
-    total_s = sum(step_ms) / 1e3
-    value = _job_throughput(dist, world, wl.T * args.steps, total_s, dev)
-
-    # ---- roofline of the dominant kernel (gate_up + SwiGLU), algorithmic bytes per launch
-    counts = np.bincount(ids.cpu().numpy().reshape(-1), minlength=wl.E)
-    touched = int(np.count_nonzero(counts))
-    n = wl.T * wl.k
-    # the dominant kernel: gate_up + SwiGLU, or both projections when the layer runs
-    # them as one launch (then stage 2 spans that launch and stage 3 is empty)
-    fused = _lib.moe_layer_projections_fused(dims)
-    gu_bytes = touched * (2 * wl.I * wl.H * 9 // 16 + 4) + n * wl.H * 2 + n * wl.I * 2
-    if fused:
-        gu_bytes += touched * (wl.H * wl.I * 9 // 16 + 4) + n * wl.I * 2 + n * wl.H * 4
-    gu_ms = float(stage_ms[:, 2].mean())
-    hbm_peak, tf_peak, tf_sus, peak_kind = _peaks()
-    achieved = gu_bytes / (gu_ms * 1e-3) / 1e9
-    gu_flops = 2 * n * (3 if fused else 2) * wl.I * wl.H
-    achieved_tf = gu_flops / (gu_ms * 1e-3) / 1e12
-    # the bound is whichever roof the kernel is closer to: HBM for decode-sized
-    # batches, the bf16 tensor pipe for prefill-sized ones
-    if achieved_tf / tf_peak > achieved / hbm_peak:
-        roofline = {"bound": "tensor", "achieved": achieved_tf, "peak": tf_peak, "unit": "TFLOP/s",
-                    "frac": achieved_tf / tf_peak, "peak_kind": f"{peak_kind} burst cuBLAS bf16 GEMM",
-                    "algorithmic_flops_per_launch": gu_flops}
-    else:
-        roofline = {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
-                    "frac": achieved / hbm_peak, "peak_kind": f"{peak_kind} burst copy bandwidth",
-                    "algorithmic_bytes_per_launch": gu_bytes}
-    roofline.update({"kernel": "w4a16_gemm_kernel (gate_up + SwiGLU" + (", then down, one launch)" if fused else ")"),
-                     "traffic": _traffic_from_profile(wl),
-                     "launch_ms": gu_ms,
-                     "other_roof_frac": (achieved / hbm_peak) if roofline["bound"] == "tensor"
-                     else (achieved_tf / tf_peak)})
+    b = DeviceBench(wl, dev, rank)
+    m = b.measure(args.steps, args.warmup, dist, world)
+    roofline = m["roofline"]
     if roofline["bound"] == "hbm":
-        # What one kernel of the GEMM's shape reads in the same time budget when it
-        # does nothing else: the streaming probe over the same byte count, same flush.
-        nbytes = (gu_bytes // 18432) * 18432
-        probe_buf = torch.empty(nbytes, dtype=torch.uint8, device=dev)
-        pev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
-        for _ in range(3):
-            flush_l2(0.0)
-            _lib.moe_debug_stream_read(probe_buf, nbytes, layer.ws, stream)
-        for st in range(args.steps):
-            flush_l2(float(st))
-            pev[st][0].record(stream)
-            _lib.moe_debug_stream_read(probe_buf, nbytes, layer.ws, stream)
-            pev[st][1].record(stream)
-        torch.cuda.synchronize(dev)
-        if layer.device_status() != _lib.MOE_OK:
-            raise RuntimeError("stream probe timed out")
-        probe_ms = float(np.mean([e[0].elapsed_time(e[1]) for e in pev]))
-        probe_gbs = nbytes / (probe_ms * 1e-3) / 1e9
-        roofline["stream_probe"] = {
-            "what": "one CTA per SM, 8 x 18432-byte bulk copies in flight, nothing else; same byte count and L2 flush",
-            "bytes": nbytes, "ms": probe_ms, "gbs": probe_gbs, "kernel_vs_probe": achieved / probe_gbs}
-        del probe_buf
-    layer_bytes = wk.algorithmic_bytes(wl.T, wl.H, wl.I, wl.E, wl.k, counts)
-    layer_flops = wk.algorithmic_flops(wl.T, wl.H, wl.I, wl.k)
-    mean_step_ms = total_s * 1e3 / args.steps
-
-    # ---- end to end through the host-buffer entry point, on a stream of its own
-    # (there the library replays its recorded graph of copies and kernels)
-    xh = d["x"].pin_memory()
-    lh = d["logits"].pin_memory()
-    oh = torch.empty(wl.T, wl.H, dtype=torch.bfloat16).pin_memory()
-    e2e_stream = torch.cuda.Stream(dev)
-    for _ in range(max(3, args.warmup)):
-        layer.forward_host(xh, lh, oh, e2e_stream)
-    e2e_times = []
-    for s in range(args.steps):
-        flush_l2(float(s))
-        torch.cuda.synchronize(dev)
-        t0 = time.perf_counter()
-        layer.forward_host(xh, lh, oh, e2e_stream)  # synchronises before returning
-        e2e_times.append(time.perf_counter() - t0)
-    e2e_value = _job_throughput(dist, world, wl.T * args.steps, sum(e2e_times), dev)
+        probe = b.stream_probe(roofline["algorithmic_bytes_per_launch"], args.steps)
+        probe["kernel_vs_probe"] = roofline["achieved"] / probe["gbs"]
+        roofline["stream_probe"] = probe
+    e2e = b.e2e(args.steps, args.warmup, dist, world)
 
     # ---- CPU oracle baseline on a bounded sample (rank 0, N = 1 only)
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        dt, nt, reps, n_tok = oracle_baseline(d, wl, args.cpu_seconds)
+        dt, nt, reps, n_tok = oracle_baseline(b.d, wl, args.cpu_seconds)
         cpu = {"value": nt / dt, "unit": UNIT, "cores": 1, "kind": "oracle",
                "sample": f"{reps} x {n_tok} of {wl.T} tokens (seeded) after routing all {wl.T}; fp64, "
                          f"single thread, {dt:.1f} s"}
+    b.close()
+
+    # ---- the other workloads of the metric, same method, same run (context lines, not the headline)
+    extra = {}
+    names = [n for n in (EXTRA_WORKLOADS if args.workloads is None else args.workloads.split(",")) if n]
+    for name in names:
+        xwl = wk.by_name(name)
+        if xwl.name == wl.name:
+            continue
+        xb = DeviceBench(xwl, dev, rank)
+        xm = xb.measure(args.steps, args.warmup, dist, world)
+        xm["config"] = bench_config(xwl, world)
+        extra[xwl.name] = xm
+        xb.close()
 
     if rank != 0:
         return
     line = {
-        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": mean_step_ms, "higher_is_better": True, "scaling": "weak",
+        "metric": METRIC, "value": m["value"], "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": m["ms_per_step"], "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16 x nvfp4 (fp32 accumulate)", "data": "synthetic (seeded, random-init)",
-        "config": {"workload": wl.name, "T": wl.T, "H": wl.H, "I": wl.I, "E": wl.E, "k": wl.k,
-                   "parallelism": f"replicas x{world}" if world > 1 else "single",
-                   "l2": "flushed between steps, outside the timed events: a 2x-L2 buffer written, then "
-                         "another 2x-L2 buffer read (the flush's dirty lines reach HBM before the step)",
-                   "touched_experts": touched, "layer_bytes": layer_bytes, "layer_flops": layer_flops},
+        "config": bench_config(wl, world),
+        "workload_detail": {"touched_experts": m["touched_experts"], "layer_bytes": m["layer_bytes"],
+                            "layer_flops": m["layer_flops"]},
         "roofline": roofline,
-        "layer_roofline": {"achieved_gbs": layer_bytes / (mean_step_ms * 1e-3) / 1e9,
-                           "frac_hbm": layer_bytes / (mean_step_ms * 1e-3) / 1e9 / hbm_peak,
-                           "achieved_tflops": layer_flops / (mean_step_ms * 1e-3) / 1e12},
-        "stages_ms": {nm: float(stage_ms[:, i].mean()) for i, nm in
-                      enumerate(["route_group", "gather", "gate_up_swiglu", "down", "combine"])},
-        "wall_s_timed_loop": t_wall,
-        "wall_s_stage_loop": t_wall_stages,
-        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": wl.T * wl.H * 2 + wl.T * wl.E * 4,
-                "d2h_bytes_per_step": wl.T * wl.H * 2},
+        "layer_roofline": m["layer_roofline"],
+        "stages_ms": m["stages_ms"],
+        "wall_s_timed_loop": m["wall_s_timed_loop"],
+        "wall_s_stage_loop": m["wall_s_stage_loop"],
+        "e2e": e2e,
         "cpu_baseline": cpu,
         # the library's own kernels per step (routing + grouping, row gather unless the
         # GEMM gathers, gate_up, down, combine) times the timed steps
-        "gpu_launches": _lib.moe_layer_kernel_launches(dims) * args.steps,
-        "clocks": clk,
+        "gpu_launches": m["gpu_launches"],
+        "clocks": m["clocks"],
+        "workloads": extra,
     }
     print(json.dumps(line), flush=True)
 
@@ -506,6 +585,9 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target length of the CPU oracle sample")
     ap.add_argument("--ref-step-seconds", type=float, default=1.5)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--workloads", default=None,
+                    help="comma-separated extra workloads timed after the headline one (default: "
+                         + ",".join(EXTRA_WORKLOADS) + "; '' for none)")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         ap.error("--warmup must be >= 3")

@@ -55,12 +55,35 @@ def check_layer(out_gpu_bf16: np.ndarray, ref: np.ndarray, what: str = ""):
     return rel_fro, worst
 
 
-def sample_tokens(ids: np.ndarray, E: int, n: int, seed: int) -> np.ndarray:
+def seam_tokens(ids: np.ndarray, E: int, tile: int) -> np.ndarray:
+    """Tokens at the seams of the GEMMs' token tiles: for every expert and every
+    `tile`-row tile of its rows (rows grouped by expert, then token), the tokens
+    of the tile's first and last row."""
+    flat = ids.reshape(-1)
+    order = np.argsort(flat, kind="stable")          # rows sorted by (expert, token)
+    tok = order // ids.shape[1]
+    counts = np.bincount(flat, minlength=E)
+    off = np.concatenate([[0], np.cumsum(counts)])
+    out = set()
+    for e in np.nonzero(counts)[0]:
+        for r0 in range(int(off[e]), int(off[e + 1]), tile):
+            out.add(int(tok[r0]))
+            out.add(int(tok[min(r0 + tile, int(off[e + 1])) - 1]))
+    return np.array(sorted(out), np.int32)
+
+
+def sample_tokens(ids: np.ndarray, E: int, n: int, seed: int, tile: int = 0, seams: int = 0) -> np.ndarray:
     """Seeded token sample covering every expert that has tokens (stratified: for
-    each expert not yet covered, one of its tokens), topped up to n tokens."""
+    each expert not yet covered, one of its tokens), plus up to `seams` tokens
+    at the seams of `tile`-row token tiles, topped up to n tokens."""
     rng = np.random.default_rng(seed)
     T = ids.shape[0]
     chosen, covered = set(), set()
+    if tile > 0 and seams > 0:
+        st = seam_tokens(ids, E, tile)
+        if st.size > seams:
+            st = rng.choice(st, size=seams, replace=False)
+        chosen.update(int(t) for t in st)
     for e in rng.permutation(E):
         if e in covered:
             continue

@@ -22,8 +22,17 @@ if torch.cuda.is_available():
 DEV = "cuda"
 ALL = [w.name.split("_")[0] for w in wk.WORKLOADS]
 # the layer at full size is checked on all tokens where the oracle is quick,
-# on a stratified token sample otherwise
-LAYER_SAMPLE = {"tiny": None, "decode": None, "grouped": 48, "prefill": 6, "skewed": 48}
+# on a stratified token sample otherwise: every expert that has tokens, the
+# first and last token of (up to SEAMS of) the experts' 128-row token tiles,
+# then random tokens up to the count
+LAYER_SAMPLE = {"tiny": None, "decode": None, "grouped": 96, "prefill": 128, "skewed": 256}
+SEAMS = {"grouped": 64, "prefill": 128, "skewed": 128}
+
+
+def _layer_rows(name, rids, E, seed):
+    if LAYER_SAMPLE[name] is None:
+        return np.arange(rids.shape[0], dtype=np.int32)
+    return sample_tokens(rids, E, LAYER_SAMPLE[name], seed=seed, tile=128, seams=SEAMS[name])
 
 
 def _route_gpu(logits: torch.Tensor, k: int):
@@ -172,10 +181,7 @@ def test_layer_with_shared_expert(name):
     assert np.array_equal(bits(out), bits(out2)), "not deterministic"
     rids, rw = orc.route(d["logits"].numpy(), wl.k)
     assert np.array_equal(ids.cpu().numpy(), rids)
-    if LAYER_SAMPLE[name] is None:
-        rows = np.arange(wl.T, dtype=np.int32)
-    else:
-        rows = sample_tokens(rids, wl.E, LAYER_SAMPLE[name], seed=9)
+    rows = _layer_rows(name, rids, wl.E, seed=9)
     sgu_np = tuple(a.numpy() for a in sgu)
     sdn_np = tuple(a.numpy() for a in sdn)
     ref = orc.layer_rows(bits(d["x"]), rids, rw, gu, dn, rows) + orc.shared_rows(bits(d["x"]), sgu_np, sdn_np, rows)
@@ -332,10 +338,7 @@ def test_layer_parity(name):
     rids, rw = orc.route(d["logits"].numpy(), wl.k)
     assert np.array_equal(ids.cpu().numpy(), rids)
     assert np.abs(w.cpu().numpy() - rw).max() <= 2e-6
-    if LAYER_SAMPLE[name] is None:
-        rows = np.arange(wl.T, dtype=np.int32)
-    else:
-        rows = sample_tokens(rids, wl.E, LAYER_SAMPLE[name], seed=7)
+    rows = _layer_rows(name, rids, wl.E, seed=7)
     ref = orc.layer_rows(bits(d["x"]), rids, rw, gu, dn, rows)
     check_layer(got[rows], ref, name)
 

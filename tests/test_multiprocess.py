@@ -65,3 +65,8 @@ def test_reference_arm_under_torchrun_prints_one_line():
     j = json.loads(lines[0])
     assert j["impl"] == "reference" and j["n_gpus"] == 2 and j["value"] > 0
     assert j["e2e"]["h2d_bytes_per_step"] == 0 and j["cpu_baseline"]["kind"] == "oracle"
+    # the same config object as the measured arm prints for this workload and world size
+    sys.path.insert(0, ROOT)
+    import bench
+    from moe_layer_bit_gb300 import workloads as wk
+    assert j["config"] == bench.bench_config(wk.by_name("tiny"), 2)
