@@ -334,6 +334,25 @@ int moe_debug_timeout_probe(void *ws, uint64_t limit_ns, void *stream);
  * faults and the context stays usable. */
 int moe_debug_counter_timeout_probe(void *ws, uint64_t limit_ns, void *stream);
 
+/* Measurement hook for choosing the GEMM's tile schedule and token-tile
+ * width by measurement: moe_layer_forward_profiled with those two choices
+ * forced.  token_tile: 16, 32, 64 or 128 rows per token tile (-1: the
+ * library's choice); schedule: 0 static (a persistent CTA per SM takes
+ * tiles blockIdx.x, + gridDim.x, ...), 1 claim (a persistent CTA per SM
+ * takes the next tile of a global counter), 2 grid3d (one CTA per (weight
+ * tile, token tile, expert), the Atlas article's 3-D grid
+ * (ceil(N/BN), max token tiles, experts); one launch per projection), -1:
+ * the library's choice.  16- and 32-row tiles gather activation rows in the
+ * GEMM and, unless grid3d, run both projections as one launch; 64- and
+ * 128-row tiles read a permuted copy of x.  Same results as
+ * moe_layer_forward within the layer tolerance (the fp32 sums are the same
+ * for every choice: a token tile's MMA K order does not depend on them).
+ * Same workspace. */
+int moe_debug_layer_forward_config(const uint16_t *x, const float *logits, moe_w4 w_gate_up, moe_w4 w_down,
+                                   moe_dims d, uint16_t *out, int32_t *topk_ids, float *topk_w, void *ws,
+                                   size_t ws_bytes, int32_t token_tile, int32_t schedule, void *stream,
+                                   void *const *stage_events);
+
 /* Measurement hook: a streaming-read probe.  Reads floor(bytes / 18432) *
  * 18432 bytes of device memory at src (16-byte aligned) with one CTA per SM,
  * each issuing 18432-byte bulk copies into a ring of 8 shared-memory slots and

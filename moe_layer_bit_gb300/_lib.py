@@ -76,6 +76,7 @@ _SIGS = {
     "moe_debug_timeout_probe": (INT, [P, ctypes.c_uint64, P]),
     "moe_debug_counter_timeout_probe": (INT, [P, ctypes.c_uint64, P]),
     "moe_debug_stream_read": (INT, [P, SZ, P, P]),
+    "moe_debug_layer_forward_config": (INT, [P, P, W4, W4, Dims, P, P, P, P, SZ, I32, I32, P, P]),
 }
 
 
@@ -263,3 +264,14 @@ def moe_debug_stream_read(src, nbytes: int, ws, stream=None):
 def moe_debug_counter_timeout_probe(ws, limit_ns: int, stream=None):
     _check(load().moe_debug_counter_timeout_probe(_p(ws), int(limit_ns), _s(stream)),
            "moe_debug_counter_timeout_probe")
+
+
+def moe_debug_layer_forward_config(x, logits, w_gate_up: W4, w_down: W4, d, out, topk_ids, topk_w, ws, ws_bytes,
+                                   token_tile: int, schedule: int, events=None, stream=None):
+    """The layer with the GEMM's token-tile width and tile schedule forced (-1: the library's choice)."""
+    arr = None
+    if events is not None:
+        arr = (ctypes.c_void_p * 6)(*[(e.cuda_event if e is not None else None) for e in events])
+    _check(load().moe_debug_layer_forward_config(_p(x), _p(logits), w_gate_up, w_down, d, _p(out), _p(topk_ids),
+                                                 _p(topk_w), _p(ws), ws_bytes, int(token_tile), int(schedule),
+                                                 _s(stream), arr), "moe_debug_layer_forward_config")

@@ -126,21 +126,36 @@ struct Cfg {
   // i - NSB, and whose own arrival the release of stage i + NSB waits behind.
   static constexpr int NSW = NSW1 < G ? G : (NSW1 / G) * G;
   static_assert(G <= NA && NSW % G == 0 && (!kGatherB || NSB >= G), "dequant groups must fit the rings");
+  // The tile ring: the weight producer publishes each tile of the CTA's
+  // schedule (phase, expert, weight tile, token tile) into entry j % kRing;
+  // the MMA warp, the epilogue warps and the activation producers read it.
+  static constexpr int kRing = 32;
+  static constexpr int kRingReaders = 1 + 4 + (kGatherB ? kBProducers : 1);
   static constexpr int kOffB = 0;
   static constexpr int kOffW = NSB * kBTile;
   static constexpr int kOffBar = kOffW + NSW * kWBytes;
   // fullw[NSW], emptyw[NSW], fullb[NSB], emptyb[NSB], afull[NA], aempty[NA],
-  // dfull[ND], dempty[ND], drain
-  static constexpr int kNumBars = 2 * NSW + 2 * NSB + 2 * NA + 2 * ND + 1;
-  static constexpr int kOffMisc = kOffBar + kNumBars * 8;  // [0] tmem base, [1] abort, [2] token tiles
-  static constexpr int kOffTables = kOffMisc + 16;         // offsets[E+1], prefix[E+1]
+  // dfull[ND], dempty[ND], drain, tfull[kRing], tempty[kRing]
+  static constexpr int kNumBars = 2 * NSW + 2 * NSB + 2 * NA + 2 * ND + 1 + 2 * kRing;
+  static constexpr int kOffRing = ((kOffBar + kNumBars * 8 + 15) / 16) * 16;  // int4 [kRing]
+  static constexpr int kOffWFlag = kOffRing + kRing * 16;           // int [NSW]: 1 = weight stage, 0 = end
+  static constexpr int kOffMisc = kOffWFlag + ((NSW * 4 + 15) / 16) * 16;  // [0] tmem base, [1] abort, [2] tiles
+  static constexpr int kOffTables = kOffMisc + 16;                  // offsets[E+1], prefix[E+1]
   static_assert(NA >= 1, "TMEM ring needs a slot");
   static_assert(kOffW % 1024 == 0, "swizzled tiles need 1024-byte alignment");
+  static_assert(kOffRing % 16 == 0, "ring entries are 16-byte vectors");
   static int bytes(int E) {
     int b = kOffTables + 2 * (E + 1) * 4 + 1024;  // + alignment slack
     return b < kMinSmem ? kMinSmem : b;
   }
 };
+
+__device__ __forceinline__ int4 ld_shared_v4(uint32_t addr) {
+  int4 v;
+  asm volatile("ld.shared.v4.s32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr)
+               : "memory");
+  return v;
+}
 
 // MODE 0 / 1: one phase, gate_up + SwiGLU / down, fixed at compile time;
 // MODE 2: the phases' own modes (the one-launch layer).
@@ -148,7 +163,7 @@ template <int BN, int SB, int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
     w4a16_gemm_kernel(const __grid_constant__ CUtensorMap tmap_act, const __grid_constant__ GemmLaunch L) {
   using C = Cfg<BN, SB>;
-  constexpr int NSW = C::NSW, NSB = C::NSB, NA = C::NA;
+  constexpr int NSW = C::NSW, NSB = C::NSB, NA = C::NA, R = C::kRing;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
@@ -165,6 +180,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto dfull_bar = [&](int d) { return bar0 + 8u * (2 * NSW + 2 * NSB + 2 * NA + d); };
   auto dempty_bar = [&](int d) { return bar0 + 8u * (2 * NSW + 2 * NSB + 2 * NA + ND + d); };
   const uint32_t drain_bar = bar0 + 8u * (2 * NSW + 2 * NSB + 2 * NA + 2 * ND);
+  auto tfull_bar = [&](int t) { return drain_bar + 8u * (1 + t); };
+  auto tempty_bar = [&](int t) { return drain_bar + 8u * (1 + R + t); };
+  const uint32_t s_ring = sbase + C::kOffRing;
+  volatile int* s_wflag = reinterpret_cast<volatile int*>(smem + C::kOffWFlag);
   volatile uint32_t* misc = reinterpret_cast<volatile uint32_t*>(smem + C::kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 4);
   const int E = L.E;
@@ -194,16 +213,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(dempty_bar(d), 4);
     }
     mbar_init(drain_bar, 1);
+    for (int t = 0; t < R; ++t) {
+      mbar_init(tfull_bar(t), 1);                 // the weight producer
+      mbar_init(tempty_bar(t), C::kRingReaders);  // every reader of the entry
+    }
     *abort_flag = 0;
     fence_barrier_init();
   }
   if (!C::kGatherB && warp == kWarpProducerB && lane == 0) prefetch_tmap(&tmap_act);
-  if (C::kGatherB && warp == kWarpProducer && lane == 0) {
+  if (C::kGatherB && L.sched != kSchedGrid3D && warp == kWarpProducer && lane == 0) {
     // The packed weights do not come from the kernels before, so while they
-    // run this CTA pulls into L2 the weights of its likely first tile: tile
+    // run this CTA pulls into L2 the weights of one likely early tile: tile
     // blockIdx.x of the phase-0 list if every expert had one token tile.  Of
-    // a decode step's first round of tiles most are these; a wrong guess
-    // only costs bandwidth that is idle at this point.
+    // a decode step's first round of tiles most are these (whichever CTA
+    // takes them); a wrong guess only costs bandwidth that is idle here.
     const GemmPhase& P0 = L.ph[0];
     const int MT0 = P0.N / kTileM;
     const int e = (int)blockIdx.x / MT0, mt = (int)blockIdx.x % MT0;
@@ -218,18 +241,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_alloc(sbase + C::kOffMisc, kTmemCols);
     tmem_relinquish();
   }
-  // everything above is on-chip; the offsets and activations come from the
-  // kernels before
+  // everything above is on-chip; the offsets, the activations and the
+  // schedule counters come from the kernels before
   pdl_wait();
   pdl_trigger();
+  // the claim schedule's first tile: issued now, its latency hidden behind
+  // the table build
+  int first_claim = 0;
+  if (L.sched == kSchedClaim && warp == kWarpProducer && lane == 0) first_claim = atomicAdd(L.claim, 1);
   build_tile_table(L.offsets, E, BN, s_off, s_tprefix, misc + 2);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = misc[0];
 
-  // The CTA's schedule: tiles u = blockIdx.x, + gridDim.x, ... of the
-  // concatenated tile lists of the phases (phase 0, then phase 1).
+  // Tiles of the launch: the phase-0 tile list, then the phase-1 list.
   const int ntok = (int)misc[2];
   const int MT0 = L.ph[0].N / kTileM;
   const int MT1 = L.nph > 1 ? L.ph[1].N / kTileM : 0;
@@ -238,7 +264,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int KS0 = L.ph[0].K / (kBlockK * SB);
   const int KS1 = L.nph > 1 ? L.ph[1].K / (kBlockK * SB) : 0;
   struct TileRef {
-    int ph;  // phase
+    int ph;  // phase; -1: the end of the CTA's schedule
     TileCoord c;
   };
   auto tile_of = [&](int u) {
@@ -247,53 +273,72 @@ __global__ void __launch_bounds__(kThreads, 1)
     r.c = decode_tile(r.ph == 0 ? u : u - T0, s_tprefix, E, r.ph == 0 ? MT0 : MT1);
     return r;
   };
-  // A role warp reads the CTA's schedule 32 tiles at a time: lane l decodes
-  // the CTA's tile jb + l (a chain of dependent shared-memory loads and
-  // divisions, slow while the dequant warps keep the ALU busy), and tile j is
-  // then taken from lane j - jb by shuffles.  Tiles are read in increasing j
-  // and the refill is warp-uniform.
-  struct TileCache {
-    int jb, ph, e, mt, nt;
-  };
-  auto cache_fill = [&](TileCache& tc, int j) {
-    tc.jb = j;
-    const int u = (int)blockIdx.x + (j + lane) * (int)gridDim.x;
-    tc.ph = 0;
-    tc.e = tc.mt = tc.nt = 0;
-    if (u < total) {
-      const TileRef r = tile_of(u);
-      tc.ph = r.ph;
-      tc.e = r.c.e;
-      tc.mt = r.c.mt;
-      tc.nt = r.c.nt;
-    }
-  };
-  auto cached_tile = [&](TileCache& tc, int j) {
-    if (j - tc.jb >= 32) cache_fill(tc, j);
-    const int src = j - tc.jb;
-    TileRef r;
-    r.ph = __shfl_sync(0xFFFFFFFFu, tc.ph, src);
-    r.c.e = __shfl_sync(0xFFFFFFFFu, tc.e, src);
-    r.c.mt = __shfl_sync(0xFFFFFFFFu, tc.mt, src);
-    r.c.nt = __shfl_sync(0xFFFFFFFFu, tc.nt, src);
-    return r;
+  // A reader's wait for entry j of the tile ring; every lane reads it, then
+  // one lane frees it.  False if the CTA aborted.
+  auto ring_read = [&](int j, TileRef& tr) -> bool {
+    const int slot = j % R;
+    if (!__all_sync(0xFFFFFFFFu, mbar_wait(tfull_bar(slot), (uint32_t)(j / R) & 1u, abort_flag, status)))
+      return false;
+    const int4 v = ld_shared_v4(s_ring + 16u * slot);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(tempty_bar(slot));
+    tr.ph = v.x;
+    tr.c.e = v.y;
+    tr.c.mt = v.z;
+    tr.c.nt = v.w;
+    return true;
   };
 
-  if (warp == kWarpProducer || (warp == kWarpProducerB && !C::kGatherB)) {
-    // ----------------------------------------------------------- producers
-    // One warp streams the packed weight blocks (phase after phase, with no
-    // break in between), the other (wide token tiles, one phase) the permuted
-    // activation tiles by TMA; each walks the schedule with uniform values and
-    // one elected lane issues the copies.
-    const bool is_w = warp == kWarpProducer;
-    const int ring = is_w ? NSW : NSB;
-    int i = 0;
+  if (warp == kWarpProducer) {
+    // --------------------------------------------------- schedule + weights
+    // This warp decides the CTA's tiles -- u = blockIdx.x, + gridDim.x, ...
+    // (static); u = the next value of a global counter (claim: tiles are
+    // taken in list order, so every phase-0 tile belongs to a running CTA
+    // before any phase-1 tile is handed out); or the one tile of a 3-D grid
+    // CTA -- publishes each in the tile ring and streams its packed weight
+    // blocks (phase after phase, with no break in between) into the weight
+    // ring, one bulk copy per stage issued by one lane.  After the last
+    // tile it publishes the end, then one empty weight stage per dequant
+    // group flagged as the end of the stream.
+    int u;
+    if (L.sched == kSchedStatic) {
+      u = (int)blockIdx.x;
+    } else if (L.sched == kSchedClaim) {
+      u = __shfl_sync(0xFFFFFFFFu, first_claim, 0);
+    } else {
+      // 3-D grid (weight tile, token tile, expert): one tile, if it exists
+      const int e = (int)blockIdx.z, nt = (int)blockIdx.y, mt = (int)blockIdx.x;
+      const int ntc = e < E ? s_tprefix[e + 1] - s_tprefix[e] : 0;
+      u = (e < E && nt < ntc && mt < MT0) ? s_tprefix[e] * MT0 + mt * ntc + nt : total;
+    }
+    int i = 0;  // weight stages issued
     bool ok = true;
-    TileCache tcache;
-    tcache.jb = -32;
-    int jt = 0;
-    for (int u = blockIdx.x; u < total && ok; u += gridDim.x, ++jt) {
-      const TileRef tr = cached_tile(tcache, jt);
+    for (int j = 0; ok; ++j) {
+      const bool have = u < total;
+      TileRef tr;
+      if (have) {
+        tr = tile_of(u);
+      } else {
+        tr.ph = -1;
+        tr.c.e = tr.c.mt = tr.c.nt = 0;
+      }
+      const int slot = j % R;
+      if (!__all_sync(0xFFFFFFFFu, mbar_wait(tempty_bar(slot), ((uint32_t)(j / R) & 1u) ^ 1u, abort_flag, status))) {
+        ok = false;
+        break;
+      }
+      if (lane == 0) {
+        asm volatile("st.shared.v4.s32 [%0], {%1, %2, %3, %4};" ::"r"(s_ring + 16u * slot), "r"(tr.ph), "r"(tr.c.e),
+                     "r"(tr.c.mt), "r"(tr.c.nt)
+                     : "memory");
+        mbar_arrive(tfull_bar(slot));
+      }
+      __syncwarp();
+      if (!have) break;
+      // the next tile of the claim schedule: issued now, used after this
+      // tile's copies
+      int next_claim = 0;
+      if (L.sched == kSchedClaim && lane == 0) next_claim = atomicAdd(L.claim, 1);
       const GemmPhase& P = L.ph[tr.ph];
       const int MT = tr.ph == 0 ? MT0 : MT1, KS = tr.ph == 0 ? KS0 : KS1;
       // experts 0 .. E_routed-1 are the routed ones; the next (if any) is the
@@ -301,33 +346,65 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint8_t* wsrc = tr.c.e < P.E_routed
                                 ? P.packed + (size_t)(tr.c.e * MT + tr.c.mt) * KS * SB * kWBlockBytes
                                 : P.shared_packed + (size_t)tr.c.mt * KS * SB * kWBlockBytes;
-      const int row0 = s_off[tr.c.e] + tr.c.nt * BN;
       for (int ks = 0; ks < KS; ++ks, ++i) {
-        const int s = i % ring;
-        const uint32_t ph = (uint32_t)(i / ring) & 1u;
-        const uint32_t ebar = is_w ? emptyw_bar(s) : emptyb_bar(s);
-        if (!__all_sync(0xFFFFFFFFu, mbar_wait(ebar, ph ^ 1u, abort_flag, status))) {
+        const int s = i % NSW;
+        if (!__all_sync(0xFFFFFFFFu, mbar_wait(emptyw_bar(s), ((uint32_t)(i / NSW) & 1u) ^ 1u, abort_flag, status))) {
           ok = false;
           break;
         }
         if (elect_one_sync()) {
-          if (is_w) {
-            mbar_arrive_expect_tx(fullw_bar(s), (uint32_t)C::kWBytes);
-            bulk_copy_g2s(sW + s * C::kWBytes, wsrc + (size_t)ks * C::kWBytes, C::kWBytes, fullw_bar(s));
-          } else {
-            mbar_arrive_expect_tx(fullb_bar(s), (uint32_t)C::kBTile);
+          s_wflag[s] = 1;
+          mbar_arrive_expect_tx(fullw_bar(s), (uint32_t)C::kWBytes);
+          bulk_copy_g2s(sW + s * C::kWBytes, wsrc + (size_t)ks * C::kWBytes, C::kWBytes, fullw_bar(s));
+        }
+        __syncwarp();
+      }
+      if (L.sched == kSchedStatic) u += (int)gridDim.x;
+      else if (L.sched == kSchedClaim) u = __shfl_sync(0xFFFFFFFFu, next_claim, 0);
+      else u = total;
+    }
+    // the end of the weight stream: one flagged stage per dequant group
+    for (int g = 0; g < C::G && ok; ++g, ++i) {
+      const int s = i % NSW;
+      if (!__all_sync(0xFFFFFFFFu, mbar_wait(emptyw_bar(s), ((uint32_t)(i / NSW) & 1u) ^ 1u, abort_flag, status)))
+        break;
+      if (lane == 0) {
+        s_wflag[s] = 0;
+        mbar_arrive(fullw_bar(s));
+      }
+      __syncwarp();
+    }
+    // drain: every copy this warp issued has landed before the CTA exits
+    for (int j = (i > NSW ? i - NSW : 0); j < i; ++j)
+      mbar_wait(fullw_bar(j % NSW), (uint32_t)(j / NSW) & 1u, nullptr, status, kDrainTimeoutNs);
+  } else if (!C::kGatherB && warp == kWarpProducerB) {
+    // ------------------------------------------- activation tiles by TMA
+    // (wide token tiles, one phase): SB 2-D boxes of the permuted rows per
+    // stage, issued by one lane.
+    int i = 0;
+    bool ok = true;
+    for (int j = 0; ok; ++j) {
+      TileRef tr;
+      if (!ring_read(j, tr) || tr.ph < 0) break;
+      const int KS = tr.ph == 0 ? KS0 : KS1;
+      const int row0 = s_off[tr.c.e] + tr.c.nt * BN;
+      for (int ks = 0; ks < KS; ++ks, ++i) {
+        const int s = i % NSB;
+        if (!__all_sync(0xFFFFFFFFu, mbar_wait(emptyb_bar(s), ((uint32_t)(i / NSB) & 1u) ^ 1u, abort_flag, status))) {
+          ok = false;
+          break;
+        }
+        if (elect_one_sync()) {
+          mbar_arrive_expect_tx(fullb_bar(s), (uint32_t)C::kBTile);
 #pragma unroll
-            for (int b = 0; b < SB; ++b)
-              tma_load_2d(sB + s * C::kBTile + b * C::kBSub, &tmap_act, (ks * SB + b) * kBlockK, row0, fullb_bar(s));
-          }
+          for (int b = 0; b < SB; ++b)
+            tma_load_2d(sB + s * C::kBTile + b * C::kBSub, &tmap_act, (ks * SB + b) * kBlockK, row0, fullb_bar(s));
         }
         __syncwarp();
       }
     }
-    // drain: every copy this warp issued has landed before the CTA exits
-    for (int j = (i > ring ? i - ring : 0); j < i; ++j)
-      mbar_wait(is_w ? fullw_bar(j % ring) : fullb_bar(j % ring), (uint32_t)(j / ring) & 1u, nullptr, status,
-                kDrainTimeoutNs);
+    for (int j = (i > NSB ? i - NSB : 0); j < i; ++j)
+      mbar_wait(fullb_bar(j % NSB), (uint32_t)(j / NSB) & 1u, nullptr, status, kDrainTimeoutNs);
   } else if (C::kGatherB && warp >= kWarpProducerB && warp < kWarpProducerB + kBProducers) {
     // ------------------------------------- activation rows, gathered (BN <= 32)
     // Two warps split every row's 16-byte chunks.  Lane -> (row r, chunks
@@ -357,27 +434,34 @@ __global__ void __launch_bounds__(kThreads, 1)
       released = issued;
     };
     // A phase-1 tile of expert e needs every phase-0 tile of e finished (4
-    // epilogue warps each).  Readiness is checked for 32 tiles at once, lane
-    // l loading the counter of this CTA's tile j + l, so most tiles need no
-    // check of their own; each lane's acquire load, followed by the warp
-    // sync, orders the whole warp's later reads of those rows.
+    // epilogue warps each).  Readiness is checked for the published tiles
+    // j, j + 1, ... at once, lane l loading the counter of tile j + l if
+    // the weight producer has already published it (a non-blocking test of
+    // its ring entry: tile j + l < j + kRing, so the entry's barrier is on
+    // that tile's lap), so most tiles need no check of their own; each lane's
+    // acquire load, followed by the warp sync, orders the whole warp's later
+    // reads of those rows.
     auto target_of = [&](int e) { return 4 * MT0 * (s_tprefix[e + 1] - s_tprefix[e]); };
     int known_ready = -1;  // this CTA's tiles 0 .. known_ready are ready to read
     bool ok = true;
-    int j = 0;
-    TileCache tcache;
-    tcache.jb = -32;
-    for (int u = blockIdx.x; u < total && ok; u += gridDim.x, ++j) {
-      TileRef tr = cached_tile(tcache, j);
+    for (int j = 0; ok; ++j) {
+      TileRef tr;
+      if (!ring_read(j, tr) || tr.ph < 0) break;
       if (tr.ph == 1 && j > known_ready) {
-        // the cache is refilled from tile j, so lane l holds tile j + l
-        if (tcache.jb != j) {
-          cache_fill(tcache, j);
-          tr = cached_tile(tcache, j);
-        }
-        const int ul = u + lane * (int)gridDim.x;
+        const int jl = j + lane;
         bool lane_ready = true;
-        if (ul < total && tcache.ph == 1) lane_ready = counter_load_acquire(L.ready + tcache.e) >= target_of(tcache.e);
+        if (lane > 0) {
+          const int slot = jl % R;
+          if (mbar_test_wait(tfull_bar(slot), (uint32_t)(jl / R) & 1u)) {
+            const int4 v = ld_shared_v4(s_ring + 16u * slot);
+            if (v.x == 1) lane_ready = counter_load_acquire(L.ready + v.y) >= target_of(v.y);
+            else if (v.x < 0) lane_ready = true;  // the end: nothing to read
+          } else {
+            lane_ready = false;  // not published yet
+          }
+        } else {
+          lane_ready = counter_load_acquire(L.ready + tr.c.e) >= target_of(tr.c.e);
+        }
         const uint32_t not_ready = __ballot_sync(0xFFFFFFFFu, !lane_ready);
         __syncwarp();
         const int n_ready = not_ready != 0 ? __ffs(not_ready) - 1 : 32;
@@ -410,7 +494,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int b = 0; b < SB; ++b) {
           const uint16_t* src = rowp + (ks * SB + b) * kBlockK;
 #pragma unroll
-          for (int j = 0; j < kChunks; ++j) cp_async16(dst + b * C::kBSub + dst_off[j], src + j * 8, nbytes);
+          for (int c = 0; c < kChunks; ++c) cp_async16(dst + b * C::kBSub + dst_off[c], src + c * 8, nbytes);
         }
         cp_async_commit();
         ++issued;
@@ -437,10 +521,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     // The whole warp waits and computes the (uniform) operands; one elected
     // lane issues the MMAs and commits.
     constexpr uint32_t idesc = idesc_bf16_f32(kTileM, BN);
-    int i = 0, it = 0;
+    int i = 0;
     bool ok = true;
-    for (int u = blockIdx.x; u < total && ok; u += gridDim.x, ++it) {
-      const int KS = u < T0 ? KS0 : KS1;
+    for (int it = 0; ok; ++it) {
+      TileRef tr;
+      if (!ring_read(it, tr) || tr.ph < 0) break;
+      const int KS = tr.ph == 0 ? KS0 : KS1;
       const int d = it % ND;
       if (!__all_sync(0xFFFFFFFFu, mbar_wait(dempty_bar(d), ((uint32_t)(it / ND) & 1u) ^ 1u, abort_flag, status)))
         break;
@@ -482,6 +568,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_wait(drain_bar, 0, nullptr, status, kDrainTimeoutNs);
   } else if (warp >= kWarpDq0) {
     // ------------------------------------------------------------- dequant
+    // Stages round-robin over the groups, in the weight ring's order, until a
+    // stage flagged as the end of the stream.
     constexpr int G = C::G, kBlocksPerWarp = SB / C::kSplit;
     const int dw = warp - kWarpDq0;
     const int q = warp & 3;  // TMEM lane quadrant this warp may access
@@ -489,15 +577,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int part = (dw % C::kGroupWarps) >> 2;
     const int r = 32 * q + lane;
     const uint32_t t_row = tmem_base + ((uint32_t)(32 * q) << 16) + (uint32_t)C::A0;
-    // stages of this CTA: its tiles of phase 0 times KS0, then of phase 1
-    const int n_all = total > (int)blockIdx.x ? (total - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x : 0;
-    const int n0 = T0 > (int)blockIdx.x ? (T0 - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x : 0;
-    const int my_stages = n0 * KS0 + (n_all - n0) * KS1;
 #pragma unroll 1
-    for (int i = group; group < G && i < my_stages; i += G) {
+    for (int i = group; group < G; i += G) {
       const int s = i % NSW, a = i % NA;
       // every lane waits (each acquires the copied bytes); the warp acts as one
       if (!__all_sync(0xFFFFFFFFu, mbar_wait(fullw_bar(s), (uint32_t)(i / NSW) & 1u, abort_flag, status))) break;
+      if (s_wflag[s] == 0) break;  // the end of the weight stream
       if (!__all_sync(0xFFFFFFFFu, mbar_wait(aempty_bar(a), ((uint32_t)(i / NA) & 1u) ^ 1u, abort_flag, status)))
         break;
       tc_fence_after();
@@ -534,11 +619,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     // ------------------------------------------------------------ epilogue
     const int q = warp - kWarpEpi0;
-    int it = 0;
-    TileCache tcache;
-    tcache.jb = -32;
-    for (int u = blockIdx.x; u < total; u += gridDim.x, ++it) {
-      const TileRef tr = cached_tile(tcache, it);
+    for (int it = 0;; ++it) {
+      TileRef tr;
+      if (!ring_read(it, tr) || tr.ph < 0) break;
       const GemmPhase& P = L.ph[tr.ph];
       const TileCoord c = tr.c;
       const int d = it % ND;
@@ -641,7 +724,7 @@ static GemmPhase phase_of(int mode, const GemmArgs& a) {
 
 // `rows` activation rows (T*k); the phases of L share them and the offsets.
 template <int BN, int SB, int MODE>
-static cudaError_t launch_gemm_cfg(const GemmLaunch& L, int rows, cudaStream_t s) {
+static cudaError_t launch_gemm_cfg(const GemmLaunch& L, int rows, int T, cudaStream_t s) {
   using C = Cfg<BN, SB>;
   CUtensorMap tmap;
   memset(&tmap, 0, sizeof(tmap));
@@ -659,8 +742,20 @@ static cudaError_t launch_gemm_cfg(const GemmLaunch& L, int rows, cudaStream_t s
                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
   }
+  const int smem = C::bytes(L.E);
+  auto kern = w4a16_gemm_kernel<BN, SB, MODE>;
+  cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (err != cudaSuccess) return err;
+  if (L.sched == kSchedGrid3D) {
+    // (weight tiles, token tiles of the largest possible expert, experts): an
+    // expert receives each token at most once, so it has at most T rows
+    if (L.nph != 1 || T <= 0) return cudaErrorInvalidValue;
+    const dim3 grid((unsigned)(L.ph[0].N / kTileM), (unsigned)((T + BN - 1) / BN), (unsigned)L.E);
+    return launch_pdl(kern, grid, dim3(kThreads), smem, s, tmap, L);
+  }
+  if (L.sched == kSchedClaim && L.claim == nullptr) return cudaErrorInvalidValue;
   int dev = 0, sms = 0;
-  cudaError_t err = cudaGetDevice(&dev);
+  err = cudaGetDevice(&dev);
   if (err != cudaSuccess) return err;
   err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (err != cudaSuccess) return err;
@@ -669,18 +764,13 @@ static cudaError_t launch_gemm_cfg(const GemmLaunch& L, int rows, cudaStream_t s
   for (int p = 0; p < L.nph; ++p) max_tiles += (long long)(L.ph[p].N / kTileM) * (n / BN + (n < L.E ? n : L.E));
   const int grid = (int)(max_tiles < sms ? max_tiles : sms);
   if (grid <= 0) return cudaSuccess;
-  const int smem = C::bytes(L.E);
-  auto kern = w4a16_gemm_kernel<BN, SB, MODE>;
-  err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-  if (err != cudaSuccess) return err;
-  // Two phases: phase-1 CTAs wait on phase-0 tiles of other CTAs, so all CTAs
-  // must become resident (grid <= SMs, one CTA per SM).  A cooperative launch
-  // would guarantee it, but it is not overlapped with the kernel before it
-  // (measured: about 2.4 us more per decode step); a programmatic launch
-  // starts the CTAs on the free SMs at once and the rest as soon as the
-  // kernel before exits, and the library launches nothing that could hold an
-  // SM in between (the next kernel's CTAs start only after every CTA of this
-  // one has signalled launch_dependents).
+  // Persistent: at most one CTA per SM (a CTA takes a whole SM's shared
+  // memory and TMEM).  The one-launch layer's down tiles wait on gate_up
+  // tiles of other CTAs; with the claim schedule every gate_up tile is taken
+  // by a running CTA before any down tile is handed out, so the waits end
+  // whatever the residency.  The launch is programmatic, so its CTAs start
+  // on the free SMs while the kernel before finishes (a cooperative launch
+  // measured about 2.4 us more per decode step).
   return launch_pdl(kern, dim3(grid), dim3(kThreads), smem, s, tmap, L);
 }
 
@@ -710,39 +800,47 @@ static int pick_sb(int bn, const int* kb, int nph) {
 }
 
 template <int BN, int MODE>
-static cudaError_t launch_gemm_mode(const GemmLaunch& L, int rows, cudaStream_t s) {
+static cudaError_t launch_gemm_mode(const GemmLaunch& L, int rows, int T, cudaStream_t s) {
   int kb[2];
   for (int p = 0; p < L.nph; ++p) kb[p] = L.ph[p].K / kBlockK;
   switch (pick_sb(BN, kb, L.nph)) {
-    case 4: return launch_gemm_cfg<BN, (BN <= 16 ? 4 : 2), MODE>(L, rows, s);
-    case 2: return launch_gemm_cfg<BN, 2, MODE>(L, rows, s);
-    default: return launch_gemm_cfg<BN, 1, MODE>(L, rows, s);
+    case 4: return launch_gemm_cfg<BN, (BN <= 16 ? 4 : 2), MODE>(L, rows, T, s);
+    case 2: return launch_gemm_cfg<BN, 2, MODE>(L, rows, T, s);
+    default: return launch_gemm_cfg<BN, 1, MODE>(L, rows, T, s);
   }
 }
 
 template <int BN>
-static cudaError_t launch_gemm_bn(const GemmLaunch& L, int rows, cudaStream_t s) {
+static cudaError_t launch_gemm_bn(const GemmLaunch& L, int rows, int T, cudaStream_t s) {
   if (L.nph > 1) {
-    if constexpr (BN <= 32) return launch_gemm_mode<BN, 2>(L, rows, s);
+    if constexpr (BN <= 32) return launch_gemm_mode<BN, 2>(L, rows, T, s);
     return cudaErrorInvalidValue;  // one-launch layers use narrow token tiles only
   }
-  return L.ph[0].mode == 0 ? launch_gemm_mode<BN, 0>(L, rows, s) : launch_gemm_mode<BN, 1>(L, rows, s);
+  return L.ph[0].mode == 0 ? launch_gemm_mode<BN, 0>(L, rows, T, s) : launch_gemm_mode<BN, 1>(L, rows, T, s);
 }
 
-static cudaError_t launch_gemm_any(const GemmLaunch& L, int rows, cudaStream_t s) {
-  switch (pick_bn(rows, L.E)) {
-    case 16: return launch_gemm_bn<16>(L, rows, s);
-    case 32: return launch_gemm_bn<32>(L, rows, s);
-    case 64: return launch_gemm_bn<64>(L, rows, s);
-    default: return launch_gemm_bn<128>(L, rows, s);
+static cudaError_t launch_gemm_any(const GemmLaunch& L, int rows, int T, int bn, cudaStream_t s) {
+  switch (bn) {
+    case 16: return launch_gemm_bn<16>(L, rows, T, s);
+    case 32: return launch_gemm_bn<32>(L, rows, T, s);
+    case 64: return launch_gemm_bn<64>(L, rows, T, s);
+    case 128: return launch_gemm_bn<128>(L, rows, T, s);
+    default: return cudaErrorInvalidValue;
   }
 }
 
-bool gemm_gathers_rows(int rows, int E, int /*K*/) { return pick_bn(rows, E) <= 32; }
+GemmPlan plan_layer(int rows, int E, int /*H*/, int /*I*/, int force_bn, int force_sched) {
+  GemmPlan p;
+  p.bn = force_bn > 0 ? force_bn : pick_bn(rows, E);
+  p.gathers = p.bn <= 32;
+  // narrow tiles: both projections in one launch, claim schedule; wide
+  // tiles: one launch per projection, static schedule
+  p.sched = force_sched >= 0 ? force_sched : (p.gathers ? kSchedClaim : kSchedStatic);
+  p.fused = rows > 0 && p.gathers && p.sched != kSchedGrid3D;
+  return p;
+}
 
-bool gemm_fuses_layer(int rows, int E, int /*H*/, int /*I*/) { return rows > 0 && pick_bn(rows, E) <= 32; }
-
-cudaError_t launch_gemm(int mode, const GemmArgs& a, cudaStream_t s) {
+cudaError_t launch_gemm_planned(int mode, const GemmArgs& a, const GemmPlan& plan, cudaStream_t s) {
   if (a.rows == 0) return cudaSuccess;
   GemmLaunch L;
   memset(&L, 0, sizeof(L));
@@ -750,13 +848,22 @@ cudaError_t launch_gemm(int mode, const GemmArgs& a, cudaStream_t s) {
   L.nph = 1;
   L.offsets = a.offsets;
   L.status = a.status;
+  L.claim = a.claim;
   L.E = a.E;
-  return launch_gemm_any(L, a.rows, s);
+  L.sched = plan.sched;
+  if (a.gather_rows != nullptr && !plan.gathers) return cudaErrorInvalidValue;
+  return launch_gemm_any(L, a.rows, a.T, plan.bn, s);
 }
 
-cudaError_t launch_gemm_layer(const GemmArgs& gate_up, const GemmArgs& down, int32_t* ready, cudaStream_t s) {
+cudaError_t launch_gemm(int mode, const GemmArgs& a, cudaStream_t s) {
+  GemmPlan p = plan_layer(a.rows, a.E, 0, 0, -1, kSchedStatic);
+  return launch_gemm_planned(mode, a, p, s);
+}
+
+cudaError_t launch_gemm_layer(const GemmArgs& gate_up, const GemmArgs& down, int32_t* ready, const GemmPlan& plan,
+                              cudaStream_t s) {
   if (gate_up.rows == 0) return cudaSuccess;
-  if (!gemm_fuses_layer(gate_up.rows, gate_up.E, gate_up.K, down.K) || ready == nullptr) return cudaErrorInvalidValue;
+  if (!plan.fused || ready == nullptr) return cudaErrorInvalidValue;
   GemmLaunch L;
   memset(&L, 0, sizeof(L));
   L.ph[0] = phase_of(0, gate_up);
@@ -764,9 +871,11 @@ cudaError_t launch_gemm_layer(const GemmArgs& gate_up, const GemmArgs& down, int
   L.nph = 2;
   L.offsets = gate_up.offsets;
   L.ready = ready;
+  L.claim = gate_up.claim;
   L.status = gate_up.status;
   L.E = gate_up.E;
-  return launch_gemm_any(L, gate_up.rows, s);
+  L.sched = plan.sched;
+  return launch_gemm_any(L, gate_up.rows, gate_up.T, plan.bn, s);
 }
 
 // ------------------------------------------------------------------ prepack

@@ -48,8 +48,8 @@ cudaError_t launch_permute(const int32_t* ids, const uint16_t* x, int T, int H, 
 // Routing and grouping of the layer: top-k routing (ids / w [T][k]), then
 // counts, offsets, sorted_token and inv_perm of the grouped view: with
 // `shared`, every token has a (k+1)-th slot for the shared expert, grouped as
-// expert E (so E+1 groups, T*(k+1) rows).  zero_e (one int32 per group, may
-// be null) is zeroed.  T*(k+shared) <= 1024 with T*E <= 32768 runs as one
+// expert E (so E+1 groups, T*(k+1) rows).  zero_e (one int32 per group,
+// then kSchedInts more; may be null) is zeroed.  T*(k+shared) <= 1024 with T*E <= 32768 runs as one
 // single-block launch; otherwise routing, then one grouping block or
 // histogram + scan + scatter.
 cudaError_t launch_route_group(const float* logits, int T, int E, int k, bool shared, int32_t* ids, float* w,
@@ -68,13 +68,29 @@ cudaError_t launch_prepack(const uint8_t* codes, const uint8_t* scales, int E, i
 
 cudaError_t launch_dequant_table(uint16_t* out, cudaStream_t s);
 
+// Tile schedules of the grouped GEMM (how a CTA learns its tiles):
+//  static: a persistent CTA per SM takes tiles blockIdx.x, + gridDim.x, ...
+//  claim:  a persistent CTA per SM takes the next tile of a global counter
+//          (list order: all gate_up tiles are handed out before any down tile,
+//          so the one-launch layer never waits on a CTA that has not started);
+//  grid3d: one CTA per (weight tile, token tile, expert), the token-tile
+//          count bounded by ceil(rows per expert bound / BN) -- the article's
+//          3-D grid; CTAs without a tile exit.  One projection per launch.
+constexpr int kSchedStatic = 0;
+constexpr int kSchedClaim = 1;
+constexpr int kSchedGrid3D = 2;
+// Schedule counters after the per-group readiness counters in the layer's
+// workspace (zeroed by the grouping kernel): [0] the one-launch layer's or
+// the gate_up launch's claim counter, [1] the down launch's.
+constexpr int kSchedInts = 4;
+
 // Grouped W4A16 GEMM.  mode 0: gate_up + SwiGLU -> bf16 h [rows][I];
 // mode 1: down -> fp32 y [rows][H].  `act` is the bf16 activation matrix
 // [rows = T*k][K]; N = rows of the weight per expert (2I or H).
 struct GemmArgs {
   const uint16_t* act;
   // nullptr: activation row p is act row p (a permuted copy); otherwise it is
-  // act row gather_rows[p] (narrow token tiles only, see gemm_gathers_rows)
+  // act row gather_rows[p] (narrow token tiles only, see GemmPlan::gathers)
   const int32_t* gather_rows;
   const uint8_t* packed;
   const float* gscale;
@@ -85,23 +101,40 @@ struct GemmArgs {
   const int32_t* offsets;
   void* out;
   int* status;
-  int rows;  // T*k (T*(k+1) with a shared expert)
+  int32_t* claim;  // the claim schedule's counter (zero before the launch), else unused
+  int rows;        // T*k (T*(k+1) with a shared expert)
   int E, N, K;
-  int out_ld;  // I (mode 0) or H (mode 1)
+  int out_ld;      // I (mode 0) or H (mode 1)
   int T, k;
 };
-cudaError_t launch_gemm(int mode, const GemmArgs& a, cudaStream_t s);
 
-// True when launch_gemm picks narrow token tiles (16 or 32 rows) for these
-// sizes; those gather activation rows themselves (GemmArgs::gather_rows).
-bool gemm_gathers_rows(int rows, int E, int K);
+// How the layer's projections run for given sizes: the token-tile width, the
+// tile schedule, whether the GEMM gathers activation rows itself (narrow
+// tiles) and whether both projections run as one launch.
+struct GemmPlan {
+  int bn;
+  int sched;
+  bool gathers;
+  bool fused;
+};
+// force_bn (16/32/64/128) and force_sched (kSched*) override the choice when
+// >= 0 (a measurement hook); -1 keeps the library's choice.  fused needs
+// narrow tiles and a persistent schedule.
+GemmPlan plan_layer(int rows, int E, int H, int I, int force_bn = -1, int force_sched = -1);
+
+// One projection with the library's choice of tile width and the static
+// schedule (the stage entry points).
+cudaError_t launch_gemm(int mode, const GemmArgs& a, cudaStream_t s);
+// One projection with the given plan's tile width and schedule.
+cudaError_t launch_gemm_planned(int mode, const GemmArgs& a, const GemmPlan& plan, cudaStream_t s);
 
 // Both projections of the layer in one persistent launch (narrow token tiles
 // only): gate_up + SwiGLU tiles first, then down tiles, whose activation
 // loads wait per expert until that expert's h rows are written.  `ready`:
-// E int32 zeroed before the launch.
-bool gemm_fuses_layer(int rows, int E, int H, int I);
-cudaError_t launch_gemm_layer(const GemmArgs& gate_up, const GemmArgs& down, int32_t* ready, cudaStream_t s);
+// E int32 zeroed before the launch (and the claim counter, plan.sched ==
+// kSchedClaim, in gate_up.claim).
+cudaError_t launch_gemm_layer(const GemmArgs& gate_up, const GemmArgs& down, int32_t* ready, const GemmPlan& plan,
+                              cudaStream_t s);
 
 // Kernel-side view of one projection (a phase) of a launch.
 struct GemmPhase {
@@ -120,8 +153,10 @@ struct GemmLaunch {
   int nph;
   const int32_t* offsets;
   int32_t* ready;  // per expert: epilogue warps done with phase-0 tiles (nph == 2)
+  int32_t* claim;  // kSchedClaim: the global tile counter
   int* status;
   int E;
+  int sched;
 };
 
 // Kernel launches made by launch_route_group for these sizes.

@@ -45,8 +45,8 @@ Layout layout_of(const moe_dims& d, bool shared) {
   o = align_up(o + (size_t)EG * sizeof(int32_t));
   L.offsets = o;
   o = align_up(o + (size_t)(EG + 1) * sizeof(int32_t));
-  L.ready = o;
-  o = align_up(o + (size_t)EG * sizeof(int32_t));
+  L.ready = o;  // per-group readiness counters, then the schedule counters
+  o = align_up(o + (size_t)(EG + moe::kSchedInts) * sizeof(int32_t));
   L.sorted_token = o;
   o = align_up(o + n * sizeof(int32_t));
   L.inv_perm = o;
@@ -135,14 +135,13 @@ size_t moe_workspace_bytes(moe_dims d) {
 int moe_layer_kernel_launches(moe_dims d) {
   MOE_TRY_NEG(check_dims(d));
   if (d.T == 0) return 0;
-  const bool gemm_gathers = moe::gemm_gathers_rows(d.T * d.k, d.E, d.H);
-  const bool fused = moe::gemm_fuses_layer(d.T * d.k, d.E, d.H, d.I);
-  return moe::route_group_launches(d.T, d.E, d.k, false) + (gemm_gathers ? 0 : 1) + (fused ? 1 : 2) + 1;
+  const moe::GemmPlan p = moe::plan_layer(d.T * d.k, d.E, d.H, d.I);
+  return moe::route_group_launches(d.T, d.E, d.k, false) + (p.gathers ? 0 : 1) + (p.fused ? 1 : 2) + 1;
 }
 
 int moe_layer_projections_fused(moe_dims d) {
   MOE_TRY_NEG(check_dims(d));
-  return d.T > 0 && moe::gemm_fuses_layer(d.T * d.k, d.E, d.H, d.I) ? 1 : 0;
+  return d.T > 0 && moe::plan_layer(d.T * d.k, d.E, d.H, d.I).fused ? 1 : 0;
 }
 
 size_t moe_stage_workspace_bytes(moe_dims d) {
@@ -246,7 +245,8 @@ namespace {
 // matrices of the routed experts' shapes.
 int layer_forward_impl(const uint16_t* x, const float* logits, moe_w4 w_gate_up, moe_w4 w_down,
                        const moe_w4* shared_gu, const moe_w4* shared_dn, moe_dims d, uint16_t* out,
-                       int32_t* topk_ids, float* topk_w, void* ws, size_t ws_bytes, void* stream, void* const* ev) {
+                       int32_t* topk_ids, float* topk_w, void* ws, size_t ws_bytes, void* stream, void* const* ev,
+                       int force_bn = -1, int force_sched = -1) {
   MOE_TRY(check_dims(d));
   if (d.T == 0) return MOE_OK;
   MOE_TRY(check_ptrs({x, logits, w_gate_up.packed, w_gate_up.global_scale, w_down.packed, w_down.global_scale, out,
@@ -298,24 +298,26 @@ int layer_forward_impl(const uint16_t* x, const float* logits, moe_w4 w_gate_up,
   const int rows = d.T * (d.k + (shared ? 1 : 0));
   const int EG = d.E + (shared ? 1 : 0);
   MOE_TRY(mark(0));
+  // readiness counters [EG], then the schedule counters; the grouping kernel zeroes them
   int32_t* ready = reinterpret_cast<int32_t*>(w + L.ready);
-  const bool fused = moe::gemm_fuses_layer(rows, EG, d.H, d.I);
+  int32_t* claim = ready + EG;
+  const moe::GemmPlan plan = moe::plan_layer(rows, EG, d.H, d.I, force_bn, force_sched);
   MOE_TRY(cuda_status(moe::launch_route_group(logits, d.T, d.E, d.k, shared, ids, wts, counts, offs, sorted, inv,
-                                              reinterpret_cast<int32_t*>(w + L.perm), fused ? ready : nullptr, s)));
+                                              reinterpret_cast<int32_t*>(w + L.perm), ready, s)));
   MOE_TRY(mark(1));
   // the narrow-tile GEMM gathers the rows of x itself; the wide one reads x_perm
-  const bool gemm_gathers = moe::gemm_gathers_rows(rows, EG, d.H);
-  if (!gemm_gathers) MOE_TRY(cuda_status(moe::launch_gather(x, sorted, rows, d.H, xp, s)));
+  if (!plan.gathers) MOE_TRY(cuda_status(moe::launch_gather(x, sorted, rows, d.H, xp, s)));
   MOE_TRY(mark(2));
   moe::GemmArgs a{};
   a.offsets = offs;
   a.status = reinterpret_cast<int*>(w + L.status);
+  a.claim = claim;
   a.rows = rows;
   a.E = EG;
   a.T = d.T;
   a.k = d.k;
-  a.act = gemm_gathers ? x : xp;
-  a.gather_rows = gemm_gathers ? sorted : nullptr;
+  a.act = plan.gathers ? x : xp;
+  a.gather_rows = plan.gathers ? sorted : nullptr;
   a.packed = static_cast<const uint8_t*>(w_gate_up.packed);
   a.gscale = w_gate_up.global_scale;
   a.shared_packed = shared ? static_cast<const uint8_t*>(shared_gu->packed) : nullptr;
@@ -327,6 +329,7 @@ int layer_forward_impl(const uint16_t* x, const float* logits, moe_w4 w_gate_up,
   moe::GemmArgs b = a;
   b.act = h;
   b.gather_rows = nullptr;
+  b.claim = claim + 1;
   b.packed = static_cast<const uint8_t*>(w_down.packed);
   b.gscale = w_down.global_scale;
   b.shared_packed = shared ? static_cast<const uint8_t*>(shared_dn->packed) : nullptr;
@@ -335,14 +338,14 @@ int layer_forward_impl(const uint16_t* x, const float* logits, moe_w4 w_gate_up,
   b.N = d.H;
   b.K = d.I;
   b.out_ld = d.H;
-  if (fused) {
+  if (plan.fused) {
     // one launch for both projections: stage 2 spans it, stage 3 is empty
-    MOE_TRY(cuda_status(moe::launch_gemm_layer(a, b, ready, s)));
+    MOE_TRY(cuda_status(moe::launch_gemm_layer(a, b, ready, plan, s)));
     MOE_TRY(mark(3));
   } else {
-    MOE_TRY(cuda_status(run_gemm(0, a, s)));
+    MOE_TRY(cuda_status(moe::launch_gemm_planned(0, a, plan, s)));
     MOE_TRY(mark(3));
-    MOE_TRY(cuda_status(run_gemm(1, b, s)));
+    MOE_TRY(cuda_status(moe::launch_gemm_planned(1, b, plan, s)));
   }
   MOE_TRY(mark(4));
   MOE_TRY(cuda_status(moe::launch_combine(y, inv, wts, d.T, d.H, d.k, shared, out, s)));
@@ -364,6 +367,17 @@ int moe_layer_forward_profiled(const uint16_t* x, const float* logits, moe_w4 w_
                                void* stream, void* const* stage_events) {
   return layer_forward_impl(x, logits, w_gate_up, w_down, nullptr, nullptr, d, out, topk_ids, topk_w, ws, ws_bytes,
                             stream, stage_events);
+}
+
+int moe_debug_layer_forward_config(const uint16_t* x, const float* logits, moe_w4 w_gate_up, moe_w4 w_down,
+                                   moe_dims d, uint16_t* out, int32_t* topk_ids, float* topk_w, void* ws,
+                                   size_t ws_bytes, int32_t token_tile, int32_t schedule, void* stream,
+                                   void* const* stage_events) {
+  if (token_tile != -1 && token_tile != 16 && token_tile != 32 && token_tile != 64 && token_tile != 128)
+    return MOE_ERR_INVALID_ARG;
+  if (schedule < -1 || schedule > moe::kSchedGrid3D) return MOE_ERR_INVALID_ARG;
+  return layer_forward_impl(x, logits, w_gate_up, w_down, nullptr, nullptr, d, out, topk_ids, topk_w, ws, ws_bytes,
+                            stream, stage_events, token_tile, schedule);
 }
 
 int moe_layer_forward_router(const uint16_t* x, const uint16_t* router_weight, const float* router_bias,

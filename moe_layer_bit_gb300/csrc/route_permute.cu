@@ -245,6 +245,7 @@ __global__ void __launch_bounds__(1024) perm_scan_kernel(int32_t* __restrict__ c
     counts[e] = run;
     if (zero_e != nullptr) zero_e[e] = 0;
   }
+  if (zero_e != nullptr && e < kSchedInts) zero_e[E + e] = 0;  // the schedule counters after them
   int32_t total;
   const int32_t excl = block_exclusive_scan(run, warp_tot, &total);
   if (e < E) {
@@ -360,6 +361,7 @@ __global__ void __launch_bounds__(kPermChunk) route_permute_small_kernel(
     if (tid == EG - 1) offsets[EG] = excl + c;
     if (zero_e != nullptr) zero_e[tid] = 0;
   }
+  if (zero_e != nullptr && tid < kSchedInts) zero_e[EG + tid] = 0;  // the schedule counters after them
   __syncthreads();
   if (valid) {
     int pos = base[e];
