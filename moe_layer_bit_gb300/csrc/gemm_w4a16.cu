@@ -14,18 +14,22 @@
 //    are N (16..128), so a decode step with 2 tokens per expert still runs a
 //    legal tcgen05 shape and every weight byte is read once per token tile;
 //  * a persistent CTA per SM walks a device-side tile list built from the
-//    expert offsets (no host sync, no empty CTAs);
+//    expert offsets (no host sync, no empty CTAs): one producer warp decides
+//    the CTA's tiles (a fixed stride, or the next value of a global counter)
+//    and publishes each through a shared-memory ring that every other role
+//    follows; the article's 3-D grid is kept as a measured alternative;
 //  * a pipeline stage is SB consecutive 64-column K blocks (a "superstage"),
 //    so the per-stage barrier round trips of the single MMA-issuing warp are
 //    paid once per SB*4 MMAs;
 //  * warp roles (24 warps):
-//    - one producer warp issues one 1-D bulk copy of the SB packed weight
-//      blocks (codes + E4M3 scales, SB * 4608 B) per stage into a weight ring
-//      that is freed as soon as the codes are in registers;
+//    - one producer warp decides and publishes the tiles and issues one 1-D
+//      bulk copy of the SB packed weight blocks (codes + E4M3 scales,
+//      SB * 4608 B) per stage into a weight ring that is freed as soon as the
+//      codes are in registers;
 //    - activation tiles, 128-byte swizzled, go into a second ring freed by
 //      the MMA commit: for wide token tiles one warp issues SB 2-D TMA copies
 //      of a permuted copy of the rows; for narrow ones (16 or 32 rows:
-//      decode) two warps copy row sorted_token[p] of x itself with 16-byte
+//      decode) one warp copies row sorted_token[p] of x itself with 16-byte
 //      cp.async, so no permuted copy is written;
 //    - 16 dequant warps in groups (stages round-robin over groups) turn the
 //      codes into exact bf16 (value * 2^-7) and store them straight into
@@ -37,15 +41,16 @@
 //      tiles;
 //    - four epilogue warps read the accumulator (tcgen05.ld), apply
 //      global_scale * 2^7 and write SwiGLU(bf16) or fp32 rows;
+//    - in the one-launch layer, one readiness warp (below);
 //  * one launch can run both projections of the layer (narrow token tiles):
 //    the schedule is the gate_up tiles, then the down tiles, the weight
 //    stream runs on without a break, and a down tile's activation loads wait
 //    (per expert, on a GPU-scope counter the gate_up epilogues publish with
-//    release semantics) until that expert's h rows are written; the grid is
-//    at most one CTA per SM and a CTA needs a whole SM's shared memory, so
-//    once the kernel before it exits every CTA is resident and the waits
-//    cannot deadlock (a kernel of another stream holding SMs for longer than
-//    the wait limit turns them into a recorded timeout);
+//    release semantics, watched by the readiness warp) until that expert's
+//    h rows are written.  CTAs take tiles from a global counter in list
+//    order, so every gate_up tile belongs to a running CTA before any down
+//    tile is handed out, and the waits end whatever the SM residency (other
+//    streams, other processes, a partitioned GPU);
 //  * every barrier wait is bounded (about 1 s); on expiry the CTA records a
 //    timeout in the status word, drains its copies and MMAs and exits.
 #include <cstdint>
@@ -65,9 +70,10 @@ constexpr int kWarpDq0 = 4;        // warps 4..19: dequant (groups of 4 * kSplit
 constexpr int kDqWarps = 16;
 constexpr int kWarpProducer = 20;  // warp 20: weight copies
 constexpr int kWarpMma = 21;       // warp 21: TMEM owner + MMA issue
-constexpr int kWarpProducerB = 22; // warps 22, 23: activation rows (gathered; warp 22 alone for TMA tiles)
-constexpr int kBProducers = 2;
-constexpr int kThreads = 24 * 32;
+constexpr int kWarpProducerB = 22; // warps 22 ..: activation rows (gathered; warp 22 alone for TMA tiles)
+constexpr int kBProducers = 1;     // gathering warps
+constexpr int kWarpReady = kWarpProducerB + kBProducers;  // readiness of down tiles (one-launch layer)
+constexpr int kThreads = (kWarpReady + 1) * 32;
 constexpr uint32_t kTmemCols = 512;
 constexpr int kMinSmem = 120 * 1024;  // keeps one CTA (one TMEM allocation) per SM
 constexpr int kSmemBudget = 216 * 1024;  // rings; the tile table (<= 8 KiB) and alignment slack on top
@@ -128,15 +134,16 @@ struct Cfg {
   static_assert(G <= NA && NSW % G == 0 && (!kGatherB || NSB >= G), "dequant groups must fit the rings");
   // The tile ring: the weight producer publishes each tile of the CTA's
   // schedule (phase, expert, weight tile, token tile) into entry j % kRing;
-  // the MMA warp, the epilogue warps and the activation producers read it.
+  // the MMA warp, the epilogue warps and the activation producers read it,
+  // and in the one-launch layer the readiness warp too.
   static constexpr int kRing = 32;
   static constexpr int kRingReaders = 1 + 4 + (kGatherB ? kBProducers : 1);
   static constexpr int kOffB = 0;
   static constexpr int kOffW = NSB * kBTile;
   static constexpr int kOffBar = kOffW + NSW * kWBytes;
   // fullw[NSW], emptyw[NSW], fullb[NSB], emptyb[NSB], afull[NA], aempty[NA],
-  // dfull[ND], dempty[ND], drain, tfull[kRing], tempty[kRing]
-  static constexpr int kNumBars = 2 * NSW + 2 * NSB + 2 * NA + 2 * ND + 1 + 2 * kRing;
+  // dfull[ND], dempty[ND], drain, tfull[kRing], tempty[kRing], rdy[kRing]
+  static constexpr int kNumBars = 2 * NSW + 2 * NSB + 2 * NA + 2 * ND + 1 + 3 * kRing;
   static constexpr int kOffRing = ((kOffBar + kNumBars * 8 + 15) / 16) * 16;  // int4 [kRing]
   static constexpr int kOffWFlag = kOffRing + kRing * 16;           // int [NSW]: 1 = weight stage, 0 = end
   static constexpr int kOffMisc = kOffWFlag + ((NSW * 4 + 15) / 16) * 16;  // [0] tmem base, [1] abort, [2] tiles
@@ -182,6 +189,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t drain_bar = bar0 + 8u * (2 * NSW + 2 * NSB + 2 * NA + 2 * ND);
   auto tfull_bar = [&](int t) { return drain_bar + 8u * (1 + t); };
   auto tempty_bar = [&](int t) { return drain_bar + 8u * (1 + R + t); };
+  // tile j's rows of h are written (down tiles of the one-launch layer)
+  auto rdy_bar = [&](int t) { return drain_bar + 8u * (1 + 2 * R + t); };
+  const bool ready_warp = C::kGatherB && L.nph > 1;
   const uint32_t s_ring = sbase + C::kOffRing;
   volatile int* s_wflag = reinterpret_cast<volatile int*>(smem + C::kOffWFlag);
   volatile uint32_t* misc = reinterpret_cast<volatile uint32_t*>(smem + C::kOffMisc);
@@ -214,8 +224,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(drain_bar, 1);
     for (int t = 0; t < R; ++t) {
-      mbar_init(tfull_bar(t), 1);                 // the weight producer
-      mbar_init(tempty_bar(t), C::kRingReaders);  // every reader of the entry
+      mbar_init(tfull_bar(t), 1);                                          // the weight producer
+      mbar_init(tempty_bar(t), C::kRingReaders + (ready_warp ? 1 : 0));  // every reader of the entry
+      mbar_init(rdy_bar(t), 1);                                            // the readiness warp
     }
     *abort_flag = 0;
     fence_barrier_init();
@@ -267,21 +278,42 @@ __global__ void __launch_bounds__(kThreads, 1)
     int ph;  // phase; -1: the end of the CTA's schedule
     TileCoord c;
   };
+  // Tile u of the launch, decoded by a whole warp: the expert is the last e
+  // with tprefix[e] * MT <= t, found by ballots over 32 candidates at a time
+  // (two rounds for up to 1024 experts, three for 1025), so the producer's
+  // per-tile decode is a few dependent steps, not a serial binary search.
   auto tile_of = [&](int u) {
     TileRef r;
     r.ph = u < T0 ? 0 : 1;
-    r.c = decode_tile(r.ph == 0 ? u : u - T0, s_tprefix, E, r.ph == 0 ? MT0 : MT1);
+    const int t = r.ph == 0 ? u : u - T0;
+    const int MT = r.ph == 0 ? MT0 : MT1;
+    int lo = 0, span = E;
+    while (span > 1) {
+      const int part = (span + 31) >> 5;
+      const int b = lo + lane * part;
+      const bool p = lane * part < span && s_tprefix[b] * MT <= t;
+      const uint32_t m = __ballot_sync(0xFFFFFFFFu, p);
+      const int last = 31 - __clz(m);  // lane 0 always holds: tprefix[lo] * MT <= t
+      lo += last * part;
+      span = min(part, span - last * part);
+    }
+    const int ntc = s_tprefix[lo + 1] - s_tprefix[lo];
+    const int local = t - s_tprefix[lo] * MT;
+    r.c.e = lo;
+    r.c.mt = local / ntc;
+    r.c.nt = local - r.c.mt * ntc;
     return r;
   };
   // A reader's wait for entry j of the tile ring; every lane reads it, then
-  // one lane frees it.  False if the CTA aborted.
-  auto ring_read = [&](int j, TileRef& tr) -> bool {
+  // one lane frees it (unless `release` is false: then the reader frees it
+  // itself later).  False if the CTA aborted.
+  auto ring_read = [&](int j, TileRef& tr, bool release = true) -> bool {
     const int slot = j % R;
     if (!__all_sync(0xFFFFFFFFu, mbar_wait(tfull_bar(slot), (uint32_t)(j / R) & 1u, abort_flag, status)))
       return false;
     const int4 v = ld_shared_v4(s_ring + 16u * slot);
     __syncwarp();
-    if (lane == 0) mbar_arrive(tempty_bar(slot));
+    if (release && lane == 0) mbar_arrive(tempty_bar(slot));
     tr.ph = v.x;
     tr.c.e = v.y;
     tr.c.mt = v.z;
@@ -313,20 +345,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     int i = 0;  // weight stages issued
     bool ok = true;
-    for (int j = 0; ok; ++j) {
-      const bool have = u < total;
-      TileRef tr;
-      if (have) {
-        tr = tile_of(u);
+    // Publish tile j (the end when u >= total).  False if the CTA aborted.
+    auto publish = [&](int j, int uj, TileRef& tr) -> bool {
+      if (uj < total) {
+        tr = tile_of(uj);
       } else {
         tr.ph = -1;
         tr.c.e = tr.c.mt = tr.c.nt = 0;
       }
       const int slot = j % R;
-      if (!__all_sync(0xFFFFFFFFu, mbar_wait(tempty_bar(slot), ((uint32_t)(j / R) & 1u) ^ 1u, abort_flag, status))) {
-        ok = false;
-        break;
-      }
+      if (!__all_sync(0xFFFFFFFFu, mbar_wait(tempty_bar(slot), ((uint32_t)(j / R) & 1u) ^ 1u, abort_flag, status)))
+        return false;
       if (lane == 0) {
         asm volatile("st.shared.v4.s32 [%0], {%1, %2, %3, %4};" ::"r"(s_ring + 16u * slot), "r"(tr.ph), "r"(tr.c.e),
                      "r"(tr.c.mt), "r"(tr.c.nt)
@@ -334,18 +363,28 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive(tfull_bar(slot));
       }
       __syncwarp();
-      if (!have) break;
-      // the next tile of the claim schedule: issued now, used after this
-      // tile's copies
-      int next_claim = 0;
-      if (L.sched == kSchedClaim && lane == 0) next_claim = atomicAdd(L.claim, 1);
-      const GemmPhase& P = L.ph[tr.ph];
-      const int MT = tr.ph == 0 ? MT0 : MT1, KS = tr.ph == 0 ? KS0 : KS1;
+      return true;
+    };
+    // Tile j + 1 is published right after tile j's first weight copy, so
+    // that the readers (the gathering warp above all) never wait for it at a
+    // tile boundary and the first copy is not held up.  The claim schedule
+    // keeps one claim in flight ahead of that: the claim of tile j + 2 is
+    // issued when tile j + 1 is published and read a tile later, so its
+    // latency is not waited for.  A CTA's claims are increasing, so a claimed
+    // but unpublished tile is never a phase-0 tile behind a phase-1 one.
+    TileRef tr;
+    ok = publish(0, u, tr);
+    int pending = 0;  // lane 0: the claim in flight (the claim schedule)
+    if (ok && L.sched == kSchedClaim && tr.ph >= 0 && lane == 0) pending = atomicAdd(L.claim, 1);
+    for (int j = 0; ok && tr.ph >= 0; ++j) {
+      const TileRef cur = tr;
+      const GemmPhase& P = L.ph[cur.ph];
+      const int MT = cur.ph == 0 ? MT0 : MT1, KS = cur.ph == 0 ? KS0 : KS1;
       // experts 0 .. E_routed-1 are the routed ones; the next (if any) is the
       // shared expert, whose weights are a separate one-expert matrix
-      const uint8_t* wsrc = tr.c.e < P.E_routed
-                                ? P.packed + (size_t)(tr.c.e * MT + tr.c.mt) * KS * SB * kWBlockBytes
-                                : P.shared_packed + (size_t)tr.c.mt * KS * SB * kWBlockBytes;
+      const uint8_t* wsrc = cur.c.e < P.E_routed
+                                ? P.packed + (size_t)(cur.c.e * MT + cur.c.mt) * KS * SB * kWBlockBytes
+                                : P.shared_packed + (size_t)cur.c.mt * KS * SB * kWBlockBytes;
       for (int ks = 0; ks < KS; ++ks, ++i) {
         const int s = i % NSW;
         if (!__all_sync(0xFFFFFFFFu, mbar_wait(emptyw_bar(s), ((uint32_t)(i / NSW) & 1u) ^ 1u, abort_flag, status))) {
@@ -358,10 +397,19 @@ __global__ void __launch_bounds__(kThreads, 1)
           bulk_copy_g2s(sW + s * C::kWBytes, wsrc + (size_t)ks * C::kWBytes, C::kWBytes, fullw_bar(s));
         }
         __syncwarp();
+        if (ks == 0) {
+          int u_next;
+          if (L.sched == kSchedStatic) u_next = u + (int)gridDim.x;
+          else if (L.sched == kSchedClaim) u_next = __shfl_sync(0xFFFFFFFFu, pending, 0);
+          else u_next = total;
+          if (!publish(j + 1, u_next, tr)) {
+            ok = false;
+            break;
+          }
+          if (L.sched == kSchedClaim && tr.ph >= 0 && lane == 0) pending = atomicAdd(L.claim, 1);
+          u = u_next;
+        }
       }
-      if (L.sched == kSchedStatic) u += (int)gridDim.x;
-      else if (L.sched == kSchedClaim) u = __shfl_sync(0xFFFFFFFFu, next_claim, 0);
-      else u = total;
     }
     // the end of the weight stream: one flagged stage per dequant group
     for (int g = 0; g < C::G && ok; ++g, ++i) {
@@ -407,7 +455,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_wait(fullb_bar(j % NSB), (uint32_t)(j / NSB) & 1u, nullptr, status, kDrainTimeoutNs);
   } else if (C::kGatherB && warp >= kWarpProducerB && warp < kWarpProducerB + kBProducers) {
     // ------------------------------------- activation rows, gathered (BN <= 32)
-    // Two warps split every row's 16-byte chunks.  Lane -> (row r, chunks
+    // The gathering warps split every row's 16-byte chunks (with one warp,
+    // a 16-row tile takes two lanes per row).  Lane -> (row r, chunks
     // c0 .. c0 + kChunks - 1 of every 64-column block); chunk c of row r lands
     // at r * 128 + ((c ^ (r & 7)) * 16), the 128-byte swizzle the MMA's
     // shared-memory descriptor expects.  Rows past the expert's last token are
@@ -434,47 +483,29 @@ __global__ void __launch_bounds__(kThreads, 1)
       released = issued;
     };
     // A phase-1 tile of expert e needs every phase-0 tile of e finished (4
-    // epilogue warps each).  Readiness is checked for the published tiles
-    // j, j + 1, ... at once, lane l loading the counter of tile j + l if
-    // the weight producer has already published it (a non-blocking test of
-    // its ring entry: tile j + l < j + kRing, so the entry's barrier is on
-    // that tile's lap), so most tiles need no check of their own; each lane's
-    // acquire load, followed by the warp sync, orders the whole warp's later
-    // reads of those rows.
-    auto target_of = [&](int e) { return 4 * MT0 * (s_tprefix[e + 1] - s_tprefix[e]); };
-    int known_ready = -1;  // this CTA's tiles 0 .. known_ready are ready to read
+    // epilogue warps each); the readiness warp waits for that and signals
+    // the tile's rdy barrier, so this warp only waits on shared memory.  Its
+    // ring entry is freed after that wait, which keeps the rdy barrier on
+    // this tile's lap.
     bool ok = true;
     for (int j = 0; ok; ++j) {
       TileRef tr;
-      if (!ring_read(j, tr) || tr.ph < 0) break;
-      if (tr.ph == 1 && j > known_ready) {
-        const int jl = j + lane;
-        bool lane_ready = true;
-        if (lane > 0) {
-          const int slot = jl % R;
-          if (mbar_test_wait(tfull_bar(slot), (uint32_t)(jl / R) & 1u)) {
-            const int4 v = ld_shared_v4(s_ring + 16u * slot);
-            if (v.x == 1) lane_ready = counter_load_acquire(L.ready + v.y) >= target_of(v.y);
-            else if (v.x < 0) lane_ready = true;  // the end: nothing to read
-          } else {
-            lane_ready = false;  // not published yet
-          }
-        } else {
-          lane_ready = counter_load_acquire(L.ready + tr.c.e) >= target_of(tr.c.e);
-        }
-        const uint32_t not_ready = __ballot_sync(0xFFFFFFFFu, !lane_ready);
-        __syncwarp();
-        const int n_ready = not_ready != 0 ? __ffs(not_ready) - 1 : 32;
-        if (n_ready > 0) {
-          known_ready = j + n_ready - 1;
-        } else {
+      const int slot = j % R;
+      // about to wait for the next tile's entry: hand the pending stages over
+      // first, so that the MMA never waits on them meanwhile
+      if (!__all_sync(0xFFFFFFFFu, mbar_test_wait(tfull_bar(slot), (uint32_t)(j / R) & 1u))) release_all();
+      if (!ring_read(j, tr, false)) break;
+      if (tr.ph == 1) {
+        const uint32_t par = (uint32_t)(j / R) & 1u;
+        if (!__all_sync(0xFFFFFFFFu, mbar_test_wait(rdy_bar(slot), par))) {
           // hand every pending stage over before waiting on other CTAs
           release_all();
-          ok = __all_sync(0xFFFFFFFFu, wait_counter(L.ready + tr.c.e, target_of(tr.c.e), abort_flag, status));
-          if (!ok) break;
-          known_ready = j;
+          ok = __all_sync(0xFFFFFFFFu, mbar_wait(rdy_bar(slot), par, abort_flag, status));
         }
       }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(tempty_bar(slot));
+      if (!ok || tr.ph < 0) break;
       const GemmPhase& P = L.ph[tr.ph];
       const int KS = tr.ph == 0 ? KS0 : KS1;
       const int p0 = s_off[tr.c.e] + tr.c.nt * BN;
@@ -514,6 +545,33 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else {
       cp_async_wait_group<0>();  // nothing may land after the CTA exits
     }
+  } else if (warp == kWarpReady) {
+    // ------------------------------------------- readiness (one-launch layer)
+    // Follows the tile ring; for a phase-1 tile of expert e waits (bounded,
+    // acquire loads) until every phase-0 tile of e has published its rows of
+    // h (4 epilogue warps each), then arrives on the tile's rdy barrier, whose
+    // release / acquire hands that ordering on to the gathering warps.  It
+    // runs ahead of them, so their phase-1 tiles rarely wait.  Phase-0 tiles
+    // are passed at once.  A CTA's phase-0 tiles all come before its phase-1
+    // tiles, so this wait never holds back the CTA's own gate_up work.
+    if (ready_warp) {
+      for (int j = 0;; ++j) {
+        const int slot = j % R;
+        if (!__all_sync(0xFFFFFFFFu, mbar_wait(tfull_bar(slot), (uint32_t)(j / R) & 1u, abort_flag, status))) break;
+        const int4 v = ld_shared_v4(s_ring + 16u * slot);
+        bool ok = true;
+        if (v.x == 1) {
+          const int target = 4 * MT0 * (s_tprefix[v.y + 1] - s_tprefix[v.y]);
+          ok = __all_sync(0xFFFFFFFFu, wait_counter(L.ready + v.y, target, abort_flag, status));
+        }
+        __syncwarp();
+        if (lane == 0) {
+          if (ok) mbar_arrive(rdy_bar(slot));
+          mbar_arrive(tempty_bar(slot));
+        }
+        if (!ok || v.x < 0) break;
+      }
+    }
   } else if (warp >= kWarpProducerB) {
     // TMA tiles: warp 22 is the producer above; warp 23 has nothing to do
   } else if (warp == kWarpMma) {
@@ -523,9 +581,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr uint32_t idesc = idesc_bf16_f32(kTileM, BN);
     int i = 0;
     bool ok = true;
+    // one entry of lookahead: tile it + 1 is usually published when tile it
+    // starts, and reading it then keeps the ring read off the path between
+    // the tiles' MMAs
+    TileRef nxt;
+    bool have_nxt = false;
     for (int it = 0; ok; ++it) {
       TileRef tr;
-      if (!ring_read(it, tr) || tr.ph < 0) break;
+      if (have_nxt) {
+        tr = nxt;
+      } else if (!ring_read(it, tr)) {
+        break;
+      }
+      have_nxt = false;
+      if (tr.ph < 0) break;
+      if (__all_sync(0xFFFFFFFFu, mbar_test_wait(tfull_bar((it + 1) % R), (uint32_t)((it + 1) / R) & 1u)))
+        have_nxt = ring_read(it + 1, nxt);
       const int KS = tr.ph == 0 ? KS0 : KS1;
       const int d = it % ND;
       if (!__all_sync(0xFFFFFFFFu, mbar_wait(dempty_bar(d), ((uint32_t)(it / ND) & 1u) ^ 1u, abort_flag, status)))
@@ -582,15 +653,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int s = i % NSW, a = i % NA;
       // every lane waits (each acquires the copied bytes); the warp acts as one
       if (!__all_sync(0xFFFFFFFFu, mbar_wait(fullw_bar(s), (uint32_t)(i / NSW) & 1u, abort_flag, status))) break;
-      if (s_wflag[s] == 0) break;  // the end of the weight stream
-      if (!__all_sync(0xFFFFFFFFu, mbar_wait(aempty_bar(a), ((uint32_t)(i / NA) & 1u) ^ 1u, abort_flag, status)))
-        break;
-      tc_fence_after();
+      // the stage's flag is loaded with its first block's codes (an end stage
+      // holds no codes; what is loaded there is dropped)
       const uint8_t* stage_w = smem + C::kOffW + s * C::kWBytes + part * kBlocksPerWarp * kWBlockBytes;
+      const int wflag = s_wflag[s];
       // software-pipelined: the next block's codes are loaded while this one is
       // converted, hiding the shared-memory latency
       BlockCodes cur = load_block(stage_w, r);
-#pragma unroll 1
+      if (wflag == 0) break;  // the end of the weight stream
+      if (!__all_sync(0xFFFFFFFFu, mbar_wait(aempty_bar(a), ((uint32_t)(i / NA) & 1u) ^ 1u, abort_flag, status)))
+        break;
+      tc_fence_after();
+      // 16-row tiles unroll the loop, so the conversions of a warp's two
+      // blocks interleave (measured: a steadier weight stream on decode);
+      // wider tiles measured faster one block at a time
+#pragma unroll(C::kSplit == 2 ? kBlocksPerWarp : 1)
       for (int bb = 0; bb < kBlocksPerWarp; ++bb) {
         BlockCodes nxt = cur;
         if (bb + 1 < kBlocksPerWarp) nxt = load_block(stage_w + (bb + 1) * kWBlockBytes, r);
@@ -833,8 +910,11 @@ GemmPlan plan_layer(int rows, int E, int /*H*/, int /*I*/, int force_bn, int for
   GemmPlan p;
   p.bn = force_bn > 0 ? force_bn : pick_bn(rows, E);
   p.gathers = p.bn <= 32;
-  // narrow tiles: both projections in one launch, claim schedule; wide
-  // tiles: one launch per projection, static schedule
+  // narrow tiles: both projections in one launch with the claim schedule
+  // (its down tiles wait on gate_up tiles of other CTAs; claim keeps that
+  // independent of SM residency); wide tiles: one launch per projection with
+  // the static stride.  Measured: the 3-D grid is 2-10x slower on every
+  // workload; static and claim are within a few per cent of each other.
   p.sched = force_sched >= 0 ? force_sched : (p.gathers ? kSchedClaim : kSchedStatic);
   p.fused = rows > 0 && p.gathers && p.sched != kSchedGrid3D;
   return p;
