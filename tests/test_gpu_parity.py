@@ -571,13 +571,13 @@ def test_layer_every_tile_width_and_schedule(name):
     # every token-tile width (16/32 gather rows in the GEMM and run both
     # projections in one launch unless grid3d; 64/128 read a permuted copy)
     # and every schedule (static, claim, the 3-D grid): within tolerance of
-    # the oracle, deterministic, and the same schedule choice never changes
-    # a bit for a given width
+    # the oracle and bit-identical to the library's default choice
     wl, d = workload_inputs(name)
     layer = _layer(wl, d)
     x, logits = d["x"].to(DEV), d["logits"].to(DEV)
     dims = layer.dims(wl.T)
     rows, ref = _oracle_ref(name)
+    default = bits(layer.forward(x, logits))
     for bn in (16, 32, 64, 128):
         outs = []
         for sched in (0, 1, 2):
@@ -587,8 +587,10 @@ def test_layer_every_tile_width_and_schedule(name):
             assert layer.device_status() == _lib.MOE_OK, (bn, sched)
             check_layer(bits(out)[rows], ref, f"{name} bn={bn} sched={sched}")
             outs.append(bits(out))
-        for o in outs[1:]:
-            assert np.array_equal(o, outs[0]), f"{name} bn={bn}: schedules differ"
+        # every MMA runs the same K order for a given output element, whatever
+        # the token-tile width or schedule: the results are the same bits
+        for o in outs:
+            assert np.array_equal(o, default), f"{name} bn={bn}: differs from the default choice"
 
 
 def test_forced_config_rejects_bad_choices():
