@@ -387,3 +387,133 @@ void oracle_layer(const uint16_t *x, const float *logits,
                       H, I, k, rows, T, out);
     free(rows);
 }
+
+/* ====================================================== W4A4 (NVFP4 activations)
+ *
+ * The block-scaled FP4 variant of the layer: weights as above, and the
+ * activations entering each projection (x for gate_up, h for down) quantized
+ * to NVFP4 too, then multiplied in fp64.  The pages give no activation
+ * quantizer (the ATOM article's section 8.2 lists a 4-bit-activation format
+ * as an execution contract of its own; the Atlas article notes GB10 lacks the
+ * native FP4 MMA that GB300 has); the reading taken here is the weights'
+ * NVFP4 format without a global scale: per 16 consecutive elements one E4M3
+ * scale s = RNE_e4m3(min(amax16 / 6, 448)) and codes RNE_e2m1(v / e4m3(s)),
+ * ties to the even mantissa, saturating at +-6 (all codes 0 when e4m3(s) is
+ * 0), every step of that decision taken in fp32.  h is quantized from its
+ * value rounded to fp32. */
+
+/* fp32 -> E4M3 code, round to nearest even, for 0 <= v <= 448 (finite). */
+unsigned oracle_e4m3_rne(float v)
+{
+    /* candidates: every non-negative finite code, nearest by |value - v|;
+     * on a tie the code with the even mantissa (even code) wins */
+    unsigned best = 0;
+    double bd = INFINITY;
+    for (unsigned c = 0; c < 0x7F; ++c) {
+        double d = fabs(oracle_dec_e4m3(c) - (double)v);
+        if (d < bd || (d == bd && (c & 1u) == 0u && (best & 1u) == 1u)) {
+            bd = d;
+            best = c;
+        }
+    }
+    return best;
+}
+
+/* fp32 -> E2M1 code: nearest of the 15 values, ties to the even mantissa,
+ * saturating at +-6; -0 and values rounding to 0 give code 0. */
+unsigned oracle_e2m1_rne(float v)
+{
+    double a = fabs((double)v);
+    unsigned best = 0;
+    double bd = INFINITY;
+    for (unsigned c = 0; c < 8; ++c) {
+        double d = fabs(oracle_dec_e2m1(c) - a);
+        if (d < bd || (d == bd && (c & 1u) == 0u && (best & 1u) == 1u)) {
+            bd = d;
+            best = c;
+        }
+    }
+    if (a > 6.0) best = 7;
+    return (best != 0 && v < 0.0f) ? (best | 8u) : best;
+}
+
+/* Quantize n fp32 values (n a multiple of 16) to NVFP4: codes [n/2] (element
+ * 2i in the low nibble), E4M3 scales [n/16]. */
+void oracle_quant_nvfp4(const float *v, int n, uint8_t *codes, uint8_t *scales)
+{
+    for (int b = 0; b < n / 16; ++b) {
+        float amax = 0.0f;
+        for (int i = 0; i < 16; ++i) {
+            float a = fabsf(v[16 * b + i]);
+            if (a > amax) amax = a;
+        }
+        float q = amax / 6.0f;
+        if (q > 448.0f) q = 448.0f;
+        unsigned s = oracle_e4m3_rne(q);
+        float d = (float)oracle_dec_e4m3(s);
+        scales[b] = (uint8_t)s;
+        for (int i = 0; i < 16; i += 2) {
+            unsigned c0 = 0, c1 = 0;
+            if (d != 0.0f) {
+                c0 = oracle_e2m1_rne(v[16 * b + i] / d);
+                c1 = oracle_e2m1_rne(v[16 * b + i + 1] / d);
+            }
+            codes[8 * b + i / 2] = (uint8_t)(c0 | (c1 << 4));
+        }
+    }
+}
+
+/* NVFP4 values (codes [n/2], scales [n/16], no global scale) -> fp64 [n]. */
+static void dequant_nvfp4(const uint8_t *codes, const uint8_t *scales, int n, double *out)
+{
+    for (int i = 0; i < n; ++i) {
+        unsigned c = (codes[i / 2] >> (4 * (i & 1))) & 15u;
+        out[i] = oracle_dec_e2m1(c) * oracle_dec_e4m3(scales[i / 16]);
+    }
+}
+
+/* The W4A4 layer for the tokens rows[0..nrows): x bf16 bits [T][H] quantized
+ * per token, gate_up + SwiGLU in fp64 on the dequantized values, h rounded to
+ * fp32 and quantized, down in fp64, the weighted sum over the k slots in
+ * fp64.  out [nrows][H]. */
+void oracle_w4a4_layer_rows(const uint16_t *x, const int32_t *ids, const double *w,
+                            const uint8_t *gu_codes, const uint8_t *gu_scales, const float *gu_gs,
+                            const uint8_t *dn_codes, const uint8_t *dn_scales, const float *dn_gs,
+                            int H, int I, int k, const int32_t *rows, int nrows, double *out)
+{
+    float *xf = (float *)malloc(sizeof(float) * (size_t)H);
+    uint8_t *xc = (uint8_t *)malloc((size_t)H / 2), *xs = (uint8_t *)malloc((size_t)H / 16);
+    double *xq = (double *)malloc(sizeof(double) * (size_t)H);
+    double *wr = (double *)malloc(sizeof(double) * (size_t)(H > I ? H : I));
+    float *hf = (float *)malloc(sizeof(float) * (size_t)I);
+    uint8_t *hc = (uint8_t *)malloc((size_t)I / 2), *hs = (uint8_t *)malloc((size_t)I / 16);
+    double *hq = (double *)malloc(sizeof(double) * (size_t)I);
+    for (int r = 0; r < nrows; ++r) {
+        int t = rows[r];
+        double *o = out + (size_t)r * (size_t)H;
+        for (int i = 0; i < H; ++i) xf[i] = bf16_to_float(x[(size_t)t * H + i]);
+        oracle_quant_nvfp4(xf, H, xc, xs);
+        dequant_nvfp4(xc, xs, H, xq);
+        for (int n = 0; n < H; ++n) o[n] = 0.0;
+        for (int j = 0; j < k; ++j) {
+            int e = ids[(size_t)t * k + j];
+            for (int f = 0; f < I; ++f) {
+                double g = 0.0, u = 0.0;
+                oracle_decode_row(gu_codes, gu_scales, gu_gs, 2 * I, H, e, f, wr);
+                for (int i = 0; i < H; ++i) g += xq[i] * wr[i];
+                oracle_decode_row(gu_codes, gu_scales, gu_gs, 2 * I, H, e, I + f, wr);
+                for (int i = 0; i < H; ++i) u += xq[i] * wr[i];
+                hf[f] = (float)(g / (1.0 + exp(-g)) * u);
+            }
+            oracle_quant_nvfp4(hf, I, hc, hs);
+            dequant_nvfp4(hc, hs, I, hq);
+            for (int n = 0; n < H; ++n) {
+                double acc = 0.0;
+                oracle_decode_row(dn_codes, dn_scales, dn_gs, H, I, e, n, wr);
+                for (int i = 0; i < I; ++i) acc += hq[i] * wr[i];
+                o[n] += w[(size_t)t * k + j] * acc;
+            }
+        }
+    }
+    free(xf); free(xc); free(xs); free(xq); free(wr); free(hf); free(hc); free(hs); free(hq);
+}

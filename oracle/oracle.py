@@ -71,6 +71,14 @@ def _load():
             lib.oracle_combine.argtypes = [P, P, P, i, i, i, P]
             lib.oracle_layer_rows.restype = None
             lib.oracle_layer_rows.argtypes = [P, P, P, P, P, P, P, P, P, i, i, i, P, i, P]
+            lib.oracle_e4m3_rne.restype = ctypes.c_uint
+            lib.oracle_e4m3_rne.argtypes = [ctypes.c_float]
+            lib.oracle_e2m1_rne.restype = ctypes.c_uint
+            lib.oracle_e2m1_rne.argtypes = [ctypes.c_float]
+            lib.oracle_quant_nvfp4.restype = None
+            lib.oracle_quant_nvfp4.argtypes = [P, i, P, P]
+            lib.oracle_w4a4_layer_rows.restype = None
+            lib.oracle_w4a4_layer_rows.argtypes = [P, P, P, P, P, P, P, P, P, i, i, i, P, i, P]
             lib.oracle_layer.restype = None
             lib.oracle_layer.argtypes = [P, P, P, P, P, P, P, P, i, i, i, i, i, P, P, P]
             _lib = lib
@@ -244,3 +252,51 @@ def shared_rows(x_bf16, sgu, sdn, rows):
     x = _c(x_bf16, np.uint16)
     T = x.shape[0]
     return layer_rows(x, np.zeros((T, 1), np.int32), np.ones((T, 1), np.float64), sgu, sdn, rows)
+
+
+# ------------------------------------------------- W4A4 (NVFP4 activations)
+def e4m3_rne(v: float) -> int:
+    """fp32 value in [0, 448] -> nearest E4M3 code, ties to the even mantissa."""
+    return int(_load().oracle_e4m3_rne(float(v)))
+
+
+def e2m1_rne(v: float) -> int:
+    """fp32 value -> nearest E2M1 code (sign bit 3), ties to even, saturating at +-6."""
+    return int(_load().oracle_e2m1_rne(float(v)))
+
+
+def quant_nvfp4(v) -> tuple:
+    """fp32 rows [..., n] (n % 16 == 0) -> (codes uint8 [..., n/2], E4M3 scales uint8 [..., n/16]):
+    per 16 elements s = RNE_e4m3(min(amax/6, 448)), codes RNE_e2m1(v / e4m3(s)), in fp32."""
+    a = _c(v, np.float32)
+    shp = a.shape
+    n = shp[-1]
+    flat = a.reshape(-1, n)
+    codes = np.empty((flat.shape[0], n // 2), np.uint8)
+    scales = np.empty((flat.shape[0], n // 16), np.uint8)
+    lib = _load()
+    for r in range(flat.shape[0]):
+        row = np.ascontiguousarray(flat[r])
+        c = np.empty(n // 2, np.uint8)
+        sc = np.empty(n // 16, np.uint8)
+        lib.oracle_quant_nvfp4(_ptr(row), n, _ptr(c), _ptr(sc))
+        codes[r], scales[r] = c, sc
+    return codes.reshape(shp[:-1] + (n // 2,)), scales.reshape(shp[:-1] + (n // 16,))
+
+
+def w4a4_layer_rows(x_bf16, ids, w, gu, dn, rows):
+    """The W4A4 layer (x and h quantized to NVFP4, fp64 products) for a subset of tokens,
+    given the routing. -> out f64 [len(rows), H]."""
+    x = _c(x_bf16, np.uint16)
+    ids = _c(ids, np.int32)
+    w = _c(w, np.float64)
+    rows = _c(rows, np.int32)
+    T, H = x.shape
+    k = ids.shape[1]
+    I = gu[0].shape[1] // 2
+    out = np.empty((len(rows), H), np.float64)
+    a = [_c(gu[0], np.uint8), _c(gu[1], np.uint8), _c(gu[2], np.float32),
+         _c(dn[0], np.uint8), _c(dn[1], np.uint8), _c(dn[2], np.float32)]
+    _load().oracle_w4a4_layer_rows(_ptr(x), _ptr(ids), _ptr(w), *[_ptr(v) for v in a], H, I, k,
+                                   _ptr(rows), len(rows), _ptr(out))
+    return out

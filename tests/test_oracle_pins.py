@@ -336,3 +336,88 @@ def test_router_logits_order_fixture():
     assert got[0, 0] == np.float32(16777224.0)
     got_b = orc.router_logits(_bf16_bits(x), _bf16_bits(w), np.array([-(2.0 ** 24)], np.float32))
     assert got_b[0, 0] == np.float32(8.0)
+
+
+# ------------------------------------------------- W4A4 activation quantizer
+def _e4m3_values():
+    """Values of the non-negative finite E4M3 codes 0x00..0x7E by torch's float8 decode."""
+    c = torch.arange(0, 0x7F, dtype=torch.uint8)
+    return c.view(torch.float8_e4m3fn).to(torch.float64).numpy()
+
+
+def test_e4m3_rne_matches_torch_float8_conversion():
+    # torch's fp32 -> float8_e4m3fn conversion (a library routine, round to
+    # nearest even) on random values, exact codes and every midpoint (ties)
+    vals = _e4m3_values()
+    rng = np.random.default_rng(3)
+    xs = list(rng.uniform(0, 448, 3000)) + list(rng.uniform(0, 2 ** -5, 1000)) + list(vals)
+    xs += list((vals[1:] + vals[:-1]) / 2)             # ties between neighbours
+    xs = np.array(xs, np.float32)
+    ref = torch.from_numpy(xs).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    got = np.array([orc.e4m3_rne(v) for v in xs], np.uint8)
+    assert np.array_equal(got, ref)
+
+
+def test_e2m1_rne_nearest_with_ties_to_even(golden):
+    # brute force over the typed OCP E2M1 table: the nearest magnitude, ties to
+    # the code with the even mantissa bit, saturating at 6, sign applied
+    table = {int(c, 16) if c.startswith("0x") else int(c): float(v) for c, v in golden("e2m1_values.txt")}
+    mags = sorted((v, c) for c, v in table.items() if c < 8)
+    grid = np.concatenate([np.linspace(-7, 7, 2801), [0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0, -5.0, -0.25]])
+    for v in grid.astype(np.float32):
+        a = min(abs(float(v)), 6.0)
+        best = min(mags, key=lambda mc: (abs(mc[0] - a), mc[1] & 1))
+        want = best[1] | (8 if (v < 0 and best[1] != 0) else 0)
+        assert orc.e2m1_rne(v) == want, (v, orc.e2m1_rne(v), want)
+
+
+def test_quant_nvfp4_round_trips_representable_blocks():
+    # a block whose largest code is 6 and whose scale is an E4M3 value comes
+    # back unchanged: amax / 6 is that scale exactly, every element on the grid
+    rng = np.random.default_rng(5)
+    vals = _e4m3_values()
+    e2m1 = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]
+    for _ in range(200):
+        s = int(rng.integers(0x08, 0x7E))
+        mags = rng.choice(e2m1, 16)
+        mags[rng.integers(16)] = 6.0
+        sign = rng.choice([-1.0, 1.0], 16)
+        v = (sign * mags * vals[s]).astype(np.float32)
+        codes, scales = orc.quant_nvfp4(v)
+        assert scales[0] == s
+        back = _torch_dequant(codes[None], scales[None], 1.0)[0]
+        assert np.array_equal(back, v.astype(np.float64))
+
+
+def test_quant_nvfp4_error_within_half_a_grid_step():
+    rng = np.random.default_rng(6)
+    v = (rng.standard_normal((64, 256)) * np.exp(rng.uniform(-6, 6, (64, 1)))).astype(np.float32)
+    codes, scales = orc.quant_nvfp4(v)
+    back = _torch_dequant(codes, scales, 1.0)
+    sc = torch.from_numpy(scales).view(torch.float8_e4m3fn).to(torch.float64).numpy().repeat(16, axis=1)
+    # the scale is the E4M3 value nearest amax/6; relative to it the grid step
+    # is at most 2 (between 4 and 6), and elements beyond 6 * scale saturate
+    amax = np.abs(v.reshape(64, 16, 16)).max(axis=2).repeat(16, axis=1)
+    assert np.all(np.abs(sc - amax / 6) <= (amax / 6) * 2 ** -4 + 2 ** -10)
+    err = np.abs(back - v)
+    assert np.all(err <= sc * 1.0 + np.maximum(np.abs(v) - 6 * sc, 0) + 1e-30)
+
+
+def test_w4a4_single_expert_equals_dense_ffn_on_quantized_activations():
+    # E = 1, k = 1: the W4A4 layer equals a torch fp64 SwiGLU FFN on the
+    # quantized x, with h rounded to fp32 and quantized by the (pinned)
+    # quantizer above
+    d, gu, dn = _small_layer(T=6, H=128, I=64, E=1, k=1, seed=23)
+    xb = _bits(d["x"])
+    ids = np.zeros((6, 1), np.int32)
+    w = np.ones((6, 1))
+    got = orc.w4a4_layer_rows(xb, ids, w, gu, dn, np.arange(6, dtype=np.int32))
+    xc, xs = orc.quant_nvfp4(d["x"].to(torch.float32).numpy())
+    xq = torch.from_numpy(_torch_dequant(xc, xs, 1.0))
+    Wgu = torch.from_numpy(_torch_dequant(gu[0][0], gu[1][0], float(gu[2][0])))
+    Wd = torch.from_numpy(_torch_dequant(dn[0][0], dn[1][0], float(dn[2][0])))
+    g, u = xq @ Wgu[:64].T, xq @ Wgu[64:].T
+    h = (torch.nn.functional.silu(g) * u).to(torch.float32).numpy()
+    hc, hs = orc.quant_nvfp4(h)
+    ref = torch.from_numpy(_torch_dequant(hc, hs, 1.0)) @ Wd.T
+    assert np.allclose(got, ref.numpy(), rtol=1e-12, atol=1e-12)
