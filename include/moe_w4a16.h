@@ -304,6 +304,58 @@ int moe_host_plan_create(const uint16_t *host_x, const float *host_logits, moe_w
 int moe_host_plan_run(moe_host_plan *plan);
 int moe_host_plan_destroy(moe_host_plan *plan);
 
+/* ------------------------------------------------------------------------
+ * W4A4: the block-scaled FP4 variant of the layer.  GB300 multiplies NVFP4
+ * by NVFP4 natively (tcgen05.mma kind::mxf4nvf4), which the Atlas article's
+ * GB10 lacks (section «编译时内核选择和W4A16 Grouped GEMM»: it falls back to
+ * W4A16 there); the ATOM article (section «8.2 量化并非单一格式，而是一套执行契约»)
+ * treats a 4-bit-activation format as its own execution contract.  Here the
+ * activations entering each projection (x before gate_up, h before down) are
+ * quantized to NVFP4 -- per 16 consecutive elements an E4M3 scale
+ * s = RNE_e4m3(min(amax16 / 6, 448)) and E2M1 codes RNE_e2m1(v / e4m3(s)),
+ * ties to the even mantissa, saturating at +-6, every step in fp32, no global
+ * scale -- and both projections run as E2M1 x E2M1 products with both
+ * sides' block scales applied by the MMA, fp32 accumulation, the weights'
+ * global scale in the epilogue.  Different numerics from the W4A16 layer
+ * (the activations lose precision): results are checked against the W4A4
+ * definition, not the W4A16 one.
+ * Weights in the natural NVFP4 layout (no prepack): */
+typedef struct {
+    const uint8_t *codes;        /* [E][N][K/2], device, 16-byte aligned */
+    const uint8_t *scales;       /* [E][N][K/16] E4M3, device, 16-byte aligned */
+    const float *global_scale;   /* [E], device */
+} moe_w4n;
+
+/* Workspace of moe_layer_forward_w4a4 (0 if d is invalid).  Supported: the
+ * W4A16 limits and additionally H % 256 == 0, I % 256 == 0. */
+size_t moe_w4a4_workspace_bytes(moe_dims d);
+
+/* The W4A4 layer: route -> group -> quantize and gather x -> gate_up +
+ * SwiGLU (h quantized in the epilogue) -> down -> combine, as
+ * moe_layer_forward with the activation quantization above.  out bf16 [T][H];
+ * topk_ids / topk_w as for moe_layer_forward (may be NULL).  Needs
+ * moe_w4a4_workspace_bytes(d) of ws (its first 4 bytes the status word). */
+int moe_layer_forward_w4a4(const uint16_t *x, const float *logits, moe_w4n w_gate_up, moe_w4n w_down,
+                           moe_dims d, uint16_t *out, int32_t *topk_ids, float *topk_w, void *ws,
+                           size_t ws_bytes, void *stream);
+
+/* The activation quantizer alone: row r of the output is the NVFP4 form of
+ * row rows_of[r] of x (bf16 [*][K]; row r when rows_of is NULL), r < n:
+ * codes uint8 [n][K/2] (element 2i in the low nibble), scales E4M3 [n][K/16].
+ * K % 16 == 0; x, codes, scales 16-byte aligned. */
+int moe_quantize_nvfp4(const uint16_t *x, const int32_t *rows_of, int32_t n, int32_t K, uint8_t *codes,
+                       uint8_t *scales, void *stream);
+
+/* Test hook: one W4A4 projection over grouped, already quantized activation
+ * rows.  mode 0: gate_up + SwiGLU, act [T*k][H/2] codes + [T*k][H/16] scales,
+ * w the gate_up weights (N = 2I, K = H), out = h codes [T*k][I/2] and
+ * out_scales = h scales [T*k][I/16]; mode 1: down, act = h's NVFP4 form, w
+ * the down weights (N = H, K = I), out = y float [T*k][H].  offsets [E+1] as
+ * from moe_permute; ws: a status word.  Same limits as moe_layer_forward_w4a4. */
+int moe_debug_w4a4_gemm(int32_t mode, const uint8_t *act_codes, const uint8_t *act_scales,
+                        const int32_t *offsets, moe_w4n w, moe_dims d, void *out, uint8_t *out_scales,
+                        void *ws, void *stream);
+
 /* Synchronises `stream`, then reads and clears the device status word in ws
  * (any workspace passed to the calls above).  Returns MOE_OK,
  * MOE_ERR_DEVICE_TIMEOUT, or MOE_ERR_CUDA. */

@@ -42,6 +42,11 @@ class W4(ctypes.Structure):
     _fields_ = [("packed", ctypes.c_void_p), ("global_scale", ctypes.c_void_p)]
 
 
+class W4N(ctypes.Structure):
+    """Natural-layout NVFP4 weights (the W4A4 entry points)."""
+    _fields_ = [("codes", ctypes.c_void_p), ("scales", ctypes.c_void_p), ("global_scale", ctypes.c_void_p)]
+
+
 _lib = None
 P = ctypes.c_void_p
 SZ = ctypes.c_size_t
@@ -76,6 +81,10 @@ _SIGS = {
     "moe_debug_timeout_probe": (INT, [P, ctypes.c_uint64, P]),
     "moe_debug_counter_timeout_probe": (INT, [P, ctypes.c_uint64, P]),
     "moe_debug_stream_read": (INT, [P, SZ, P, P]),
+    "moe_w4a4_workspace_bytes": (SZ, [Dims]),
+    "moe_layer_forward_w4a4": (INT, [P, P, W4N, W4N, Dims, P, P, P, P, SZ, P]),
+    "moe_quantize_nvfp4": (INT, [P, P, I32, I32, P, P, P]),
+    "moe_debug_w4a4_gemm": (INT, [I32, P, P, P, W4N, Dims, P, P, P, P]),
     "moe_debug_layer_forward_config": (INT, [P, P, W4, W4, Dims, P, P, P, P, SZ, I32, I32, P, P]),
 }
 
@@ -275,3 +284,27 @@ def moe_debug_layer_forward_config(x, logits, w_gate_up: W4, w_down: W4, d, out,
     _check(load().moe_debug_layer_forward_config(_p(x), _p(logits), w_gate_up, w_down, d, _p(out), _p(topk_ids),
                                                  _p(topk_w), _p(ws), ws_bytes, int(token_tile), int(schedule),
                                                  _s(stream), arr), "moe_debug_layer_forward_config")
+
+
+def w4n(codes: torch.Tensor, scales: torch.Tensor, global_scale: torch.Tensor) -> W4N:
+    return W4N(codes.data_ptr(), scales.data_ptr(), global_scale.data_ptr())
+
+
+def moe_w4a4_workspace_bytes(d: Dims) -> int:
+    return int(load().moe_w4a4_workspace_bytes(d))
+
+
+def moe_layer_forward_w4a4(x, logits, w_gate_up: W4N, w_down: W4N, d, out, topk_ids, topk_w, ws, ws_bytes,
+                           stream=None):
+    _check(load().moe_layer_forward_w4a4(_p(x), _p(logits), w_gate_up, w_down, d, _p(out), _p(topk_ids),
+                                         _p(topk_w), _p(ws), ws_bytes, _s(stream)), "moe_layer_forward_w4a4")
+
+
+def moe_quantize_nvfp4(x, rows_of, n: int, K: int, codes, scales, stream=None):
+    _check(load().moe_quantize_nvfp4(_p(x), _p(rows_of), int(n), int(K), _p(codes), _p(scales), _s(stream)),
+           "moe_quantize_nvfp4")
+
+
+def moe_debug_w4a4_gemm(mode: int, act_codes, act_scales, offsets, w: W4N, d, out, out_scales, ws, stream=None):
+    _check(load().moe_debug_w4a4_gemm(int(mode), _p(act_codes), _p(act_scales), _p(offsets), w, d, _p(out),
+                                      _p(out_scales), _p(ws), _s(stream)), "moe_debug_w4a4_gemm")

@@ -157,3 +157,33 @@ class HostPlan:
             self.close()
         except Exception:
             pass
+
+
+class W4A4Layer:
+    """The block-scaled FP4 layer (NVFP4 weights and NVFP4 activations) for up to T_max tokens:
+    weights stay in their natural NVFP4 layout on the device."""
+
+    def __init__(self, gu, dn, H: int, I: int, E: int, k: int, T_max: int, device="cuda"):
+        self.H, self.I, self.E, self.k, self.T_max = H, I, E, k, T_max
+        self.device = torch.device(device)
+        self.gu = tuple(t.to(self.device).contiguous() for t in gu[:2]) + (gu[2].to(self.device, torch.float32),)
+        self.dn = tuple(t.to(self.device).contiguous() for t in dn[:2]) + (dn[2].to(self.device, torch.float32),)
+        self.ws_bytes = _lib.moe_w4a4_workspace_bytes(_lib.dims(T_max, H, I, E, k))
+        if self.ws_bytes == 0:
+            raise _lib.MoeError(_lib.MOE_ERR_UNSUPPORTED_SHAPE, "W4A4Layer")
+        self.ws = torch.zeros(self.ws_bytes, dtype=torch.uint8, device=self.device)
+        self._abi = (_lib.w4n(*self.gu), _lib.w4n(*self.dn))
+
+    def forward(self, x: torch.Tensor, logits: torch.Tensor, out: torch.Tensor | None = None,
+                topk_ids: torch.Tensor | None = None, topk_w: torch.Tensor | None = None, stream=None):
+        T = x.shape[0]
+        if T > self.T_max:
+            raise ValueError(f"T={T} > T_max={self.T_max}")
+        if out is None:
+            out = torch.empty(T, self.H, dtype=torch.bfloat16, device=self.device)
+        _lib.moe_layer_forward_w4a4(x, logits, self._abi[0], self._abi[1], _lib.dims(T, self.H, self.I, self.E, self.k),
+                                    out, topk_ids, topk_w, self.ws, self.ws_bytes, stream)
+        return out
+
+    def device_status(self, stream=None) -> int:
+        return _lib.moe_get_device_status(self.ws, stream)
