@@ -14,8 +14,9 @@ ours:      inputs resident in HBM; each timed step is moe_layer_forward_profiled
            outside the events.  `e2e` runs a caller-owned host plan (moe_host_plan_run):
            pinned host x / logits in, host out back, copies inside the timed region.
            The other workloads of the metric (grouped: the Atlas article's 800 tokens x
-           256 experts; prefill; skewed) are timed the same way after the headline one and
-           reported under "workloads".
+           256 experts; prefill; skewed), and all four through the block-scaled FP4
+           (W4A4) layer (keys ending in _w4a4), are timed the same way after the
+           headline one and reported under "workloads".
 reference: the fp64 CPU oracle (single thread) on a bounded token sample of the
            same workload; rank 0 only.
 N > 1 ranks run independent replicas (the path needs no exchange between GPUs);
@@ -245,7 +246,7 @@ def oracle_baseline(d, wl, budget_s: float):
 
 
 NOMINAL_HBM_GBS = 7900.0  # GB300 nominal HBM3e bandwidth, for context beside the measured copy peak
-EXTRA_WORKLOADS = ("grouped", "prefill", "skewed")
+EXTRA_WORKLOADS = ("grouped", "prefill", "skewed", "decode:w4a4", "grouped:w4a4", "prefill:w4a4", "skewed:w4a4")
 
 
 def bench_config(wl, world: int) -> dict:
@@ -507,6 +508,61 @@ class DeviceBench:
         torch.cuda.empty_cache()
 
 
+FP4_OVER_BF16 = 13.5 / 2.25  # nominal dense FP4 / BF16 tensor rate of GB300
+
+
+class W4A4Bench(DeviceBench):
+    """The same measurement for the block-scaled FP4 layer (NVFP4 activations,
+    tcgen05 kind::mxf4nvf4); its roofline is taken against the FP4 tensor peak
+    (the measured bf16 peak times the nominal FP4 / BF16 ratio)."""
+
+    def __init__(self, wl, dev, rank):
+        from moe_layer_bit_gb300 import _lib
+        from moe_layer_bit_gb300.layer import W4A4Layer
+        self.lib = _lib
+        self.wl, self.dev = wl, dev
+        self.d = wk.generate(wl, seed=wl.seed + rank)
+        self.layer = W4A4Layer(self.d["gu"], self.d["dn"], wl.H, wl.I, wl.E, wl.k, wl.T, dev)
+        self.x = self.d["x"].to(dev)
+        self.logits = self.d["logits"].to(dev)
+        self.out = torch.empty(wl.T, wl.H, dtype=torch.bfloat16, device=dev)
+        self.ids = torch.empty(wl.T, wl.k, dtype=torch.int32, device=dev)
+        self.tw = torch.empty(wl.T, wl.k, dtype=torch.float32, device=dev)
+        self.dims = _lib.dims(wl.T, wl.H, wl.I, wl.E, wl.k)
+        l2 = getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 126 * 2 ** 20)
+        self.flush = torch.empty(2 * l2 // 4 + 1024, dtype=torch.float32, device=dev)
+        self.clean = torch.ones(2 * l2 // 4 + 1024, dtype=torch.float32, device=dev)
+        self.stream = torch.cuda.current_stream(dev)
+
+    def step(self, evs):
+        self.lib.moe_layer_forward_w4a4_profiled(self.x, self.logits, self.layer._abi[0], self.layer._abi[1],
+                                                 self.dims, self.out, self.ids, self.tw, self.layer.ws,
+                                                 self.layer.ws_bytes, evs, self.stream)
+
+    def measure(self, steps, warmup, dist, world):
+        m = super().measure(steps, warmup, dist, world)
+        m["gpu_launches"] = None
+        m["stages_ms"] = dict(zip(["route_group", "quantize_gather", "gate_up_swiglu", "down", "combine"],
+                                  m["stages_ms"].values()))
+        return m
+
+    def roofline(self, stage_ms, touched):
+        wl = self.wl
+        n = wl.T * wl.k
+        _, tf_peak, tf_sus, peak_kind = _peaks()
+        fp4_peak, fp4_sus = tf_peak * FP4_OVER_BF16, tf_sus * FP4_OVER_BF16
+        gu_ms, dn_ms = float(stage_ms[:, 2].mean()), float(stage_ms[:, 3].mean())
+        gu_flops, dn_flops = 4 * n * wl.H * wl.I, 2 * n * wl.H * wl.I
+        a = gu_flops / (gu_ms * 1e-3) / 1e12
+        return {"bound": "tensor", "achieved": a, "peak": fp4_peak, "unit": "TFLOP/s", "frac": a / fp4_peak,
+                "frac_sustained_peak": a / fp4_sus,
+                "peak_kind": f"{peak_kind} burst cuBLAS bf16 GEMM x {FP4_OVER_BF16:g} (nominal dense FP4 / BF16)",
+                "algorithmic_flops_per_launch": gu_flops, "launch_ms": gu_ms,
+                "kernel": "w4a4_gemm_kernel (gate_up + SwiGLU + NVFP4 quantization of h)", "traffic": None,
+                "down": {"launch_ms": dn_ms, "achieved_tflops": dn_flops / (dn_ms * 1e-3) / 1e12,
+                         "frac_tensor_fp4": dn_flops / (dn_ms * 1e-3) / 1e12 / fp4_peak}}
+
+
 def run_ours(args, wl, dist, rank, world, local_rank):
     from moe_layer_bit_gb300 import _lib, build
 
@@ -541,13 +597,14 @@ def run_ours(args, wl, dist, rank, world, local_rank):
     extra = {}
     names = [n for n in (EXTRA_WORKLOADS if args.workloads is None else args.workloads.split(",")) if n]
     for name in names:
-        xwl = wk.by_name(name)
-        if xwl.name == wl.name:
+        w4a4 = name.endswith(":w4a4")
+        xwl = wk.by_name(name.split(":")[0])
+        if xwl.name == wl.name and not w4a4:
             continue
-        xb = DeviceBench(xwl, dev, rank)
+        xb = (W4A4Bench if w4a4 else DeviceBench)(xwl, dev, rank)
         xm = xb.measure(args.steps, args.warmup, dist, world)
-        xm["config"] = bench_config(xwl, world)
-        extra[xwl.name] = xm
+        xm["config"] = dict(bench_config(xwl, world), path="w4a4" if w4a4 else "w4a16")
+        extra[xwl.name + ("_w4a4" if w4a4 else "")] = xm
         xb.close()
 
     if rank != 0:

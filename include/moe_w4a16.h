@@ -339,6 +339,14 @@ int moe_layer_forward_w4a4(const uint16_t *x, const float *logits, moe_w4n w_gat
                            moe_dims d, uint16_t *out, int32_t *topk_ids, float *topk_w, void *ws,
                            size_t ws_bytes, void *stream);
 
+/* moe_layer_forward_w4a4 with per-stage timing: stage_events points to 6
+ * cudaEvent_t handles (any may be NULL), recorded on `stream` before routing
+ * + grouping (0), the quantize-and-gather of x (1), gate_up + SwiGLU (2),
+ * down (3), the combine (4), and after it (5).  Same results and launches. */
+int moe_layer_forward_w4a4_profiled(const uint16_t *x, const float *logits, moe_w4n w_gate_up, moe_w4n w_down,
+                                    moe_dims d, uint16_t *out, int32_t *topk_ids, float *topk_w, void *ws,
+                                    size_t ws_bytes, void *stream, void *const *stage_events);
+
 /* The activation quantizer alone: row r of the output is the NVFP4 form of
  * row rows_of[r] of x (bf16 [*][K]; row r when rows_of is NULL), r < n:
  * codes uint8 [n][K/2] (element 2i in the low nibble), scales E4M3 [n][K/16].

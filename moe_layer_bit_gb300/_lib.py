@@ -83,6 +83,7 @@ _SIGS = {
     "moe_debug_stream_read": (INT, [P, SZ, P, P]),
     "moe_w4a4_workspace_bytes": (SZ, [Dims]),
     "moe_layer_forward_w4a4": (INT, [P, P, W4N, W4N, Dims, P, P, P, P, SZ, P]),
+    "moe_layer_forward_w4a4_profiled": (INT, [P, P, W4N, W4N, Dims, P, P, P, P, SZ, P, P]),
     "moe_quantize_nvfp4": (INT, [P, P, I32, I32, P, P, P]),
     "moe_debug_w4a4_gemm": (INT, [I32, P, P, P, W4N, Dims, P, P, P, P]),
     "moe_debug_layer_forward_config": (INT, [P, P, W4, W4, Dims, P, P, P, P, SZ, I32, I32, P, P]),
@@ -308,3 +309,12 @@ def moe_quantize_nvfp4(x, rows_of, n: int, K: int, codes, scales, stream=None):
 def moe_debug_w4a4_gemm(mode: int, act_codes, act_scales, offsets, w: W4N, d, out, out_scales, ws, stream=None):
     _check(load().moe_debug_w4a4_gemm(int(mode), _p(act_codes), _p(act_scales), _p(offsets), w, d, _p(out),
                                       _p(out_scales), _p(ws), _s(stream)), "moe_debug_w4a4_gemm")
+
+
+def moe_layer_forward_w4a4_profiled(x, logits, w_gate_up: W4N, w_down: W4N, d, out, topk_ids, topk_w, ws, ws_bytes,
+                                    events, stream=None):
+    """events: 6 torch.cuda.Event(enable_timing=True) (or None entries)."""
+    arr = (ctypes.c_void_p * 6)(*[(e.cuda_event if e is not None else None) for e in events])
+    _check(load().moe_layer_forward_w4a4_profiled(_p(x), _p(logits), w_gate_up, w_down, d, _p(out), _p(topk_ids),
+                                                  _p(topk_w), _p(ws), ws_bytes, _s(stream), arr),
+           "moe_layer_forward_w4a4_profiled")

@@ -639,8 +639,19 @@ size_t moe_w4a4_workspace_bytes(moe_dims d) {
   return layout4(d).total;
 }
 
+int moe_layer_forward_w4a4_profiled(const uint16_t* x, const float* logits, moe_w4n w_gate_up, moe_w4n w_down,
+                                    moe_dims d, uint16_t* out, int32_t* topk_ids, float* topk_w, void* ws,
+                                    size_t ws_bytes, void* stream, void* const* ev);
+
 int moe_layer_forward_w4a4(const uint16_t* x, const float* logits, moe_w4n w_gate_up, moe_w4n w_down, moe_dims d,
                            uint16_t* out, int32_t* topk_ids, float* topk_w, void* ws, size_t ws_bytes, void* stream) {
+  return moe_layer_forward_w4a4_profiled(x, logits, w_gate_up, w_down, d, out, topk_ids, topk_w, ws, ws_bytes, stream,
+                                         nullptr);
+}
+
+int moe_layer_forward_w4a4_profiled(const uint16_t* x, const float* logits, moe_w4n w_gate_up, moe_w4n w_down,
+                                    moe_dims d, uint16_t* out, int32_t* topk_ids, float* topk_w, void* ws,
+                                    size_t ws_bytes, void* stream, void* const* ev) {
   const int rc = check4(d);
   if (rc != MOE_OK) return rc;
   if (d.T == 0) return MOE_OK;
@@ -661,12 +672,18 @@ int moe_layer_forward_w4a4(const uint16_t* x, const float* logits, moe_w4n w_gat
   int32_t* sorted = reinterpret_cast<int32_t*>(w + L.sorted);
   int32_t* inv = reinterpret_cast<int32_t*>(w + L.inv);
   const int rows = d.T * d.k;
-  int e = cuda_rc(moe::launch_route_group(logits, d.T, d.E, d.k, false, ids, wts,
+  auto mark = [&](int i) -> int {
+    if (ev == nullptr || ev[i] == nullptr) return MOE_OK;
+    return cuda_rc(cudaEventRecord(reinterpret_cast<cudaEvent_t>(ev[i]), s));
+  };
+  int e = mark(0);
+  if (e != MOE_OK) return e;
+  e = cuda_rc(moe::launch_route_group(logits, d.T, d.E, d.k, false, ids, wts,
                                           reinterpret_cast<int32_t*>(w + L.counts), offs, sorted, inv,
                                           reinterpret_cast<int32_t*>(w + L.perm), nullptr, s));
-  if (e != MOE_OK) return e;
+  if (e != MOE_OK || (e = mark(1)) != MOE_OK) return e;
   e = cuda_rc(moe::launch_quant_gather(x, sorted, rows, d.H, w + L.xc, w + L.xs, s));
-  if (e != MOE_OK) return e;
+  if (e != MOE_OK || (e = mark(2)) != MOE_OK) return e;
   moe::W4a4Args a{};
   a.w_codes = static_cast<const uint8_t*>(w_gate_up.codes);
   a.w_scales = static_cast<const uint8_t*>(w_gate_up.scales);
@@ -684,7 +701,7 @@ int moe_layer_forward_w4a4(const uint16_t* x, const float* logits, moe_w4n w_gat
   a.I = d.I;
   a.out_ld = d.I;
   e = cuda_rc(moe::launch_w4a4(0, a, s));
-  if (e != MOE_OK) return e;
+  if (e != MOE_OK || (e = mark(3)) != MOE_OK) return e;
   moe::W4a4Args b = a;
   b.w_codes = static_cast<const uint8_t*>(w_down.codes);
   b.w_scales = static_cast<const uint8_t*>(w_down.scales);
@@ -697,8 +714,10 @@ int moe_layer_forward_w4a4(const uint16_t* x, const float* logits, moe_w4n w_gat
   b.K = d.I;
   b.out_ld = d.H;
   e = cuda_rc(moe::launch_w4a4(1, b, s));
+  if (e != MOE_OK || (e = mark(4)) != MOE_OK) return e;
+  e = cuda_rc(moe::launch_combine(reinterpret_cast<const float*>(w + L.y), inv, wts, d.T, d.H, d.k, false, out, s));
   if (e != MOE_OK) return e;
-  return cuda_rc(moe::launch_combine(reinterpret_cast<const float*>(w + L.y), inv, wts, d.T, d.H, d.k, false, out, s));
+  return mark(5);
 }
 
 int moe_quantize_nvfp4(const uint16_t* x, const int32_t* rows_of, int32_t n, int32_t K, uint8_t* codes,

@@ -126,3 +126,21 @@ def test_w4a4_rejects_shapes_below_its_stage():
     with pytest.raises(_lib.MoeError) as exc:
         _lib.moe_layer_forward_w4a4(z, z, wn, wn, d, z, None, None, z, 16)
     assert exc.value.status == _lib.MOE_ERR_UNSUPPORTED_SHAPE
+
+
+def test_w4a4_profiled_entry_equals_plain_entry():
+    wl = TINY
+    d = wk.generate(wl)
+    layer = W4A4Layer(d["gu"], d["dn"], wl.H, wl.I, wl.E, wl.k, wl.T, DEV)
+    x, lg = d["x"].to(DEV), d["logits"].to(DEV)
+    ref = layer.forward(x, lg)
+    out = torch.empty_like(ref)
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(6)]
+    for e in evs:
+        e.record()  # torch creates its events lazily; the library records them again
+    _lib.moe_layer_forward_w4a4_profiled(x, lg, layer._abi[0], layer._abi[1], _lib.dims(wl.T, wl.H, wl.I, wl.E, wl.k),
+                                         out, None, None, layer.ws, layer.ws_bytes, evs)
+    torch.cuda.synchronize()
+    assert layer.device_status() == _lib.MOE_OK
+    assert np.array_equal(bits(out), bits(ref))
+    assert evs[0].elapsed_time(evs[5]) > 0
