@@ -399,8 +399,9 @@ void oracle_layer(const uint16_t *x, const float *logits,
  * NVFP4 format without a global scale: per 16 consecutive elements one E4M3
  * scale s = RNE_e4m3(min(amax16 / 6, 448)) and codes RNE_e2m1(v / e4m3(s)),
  * ties to the even mantissa, saturating at +-6 (all codes 0 when e4m3(s) is
- * 0), every step of that decision taken in fp32.  h is quantized from its
- * value rounded to fp32. */
+ * 0); the scale from amax16 / 6 computed in fp32, the codes by rounding
+ * the exact quotient v / e4m3(s) (each code is the grid value c with c *
+ * e4m3(s) nearest to v).  h is quantized from its value rounded to fp32. */
 
 /* fp32 -> E4M3 code, round to nearest even, for 0 <= v <= 448 (finite). */
 unsigned oracle_e4m3_rne(float v)
@@ -437,6 +438,23 @@ unsigned oracle_e2m1_rne(float v)
     return (best != 0 && v < 0.0f) ? (best | 8u) : best;
 }
 
+/* E2M1 code of the exact quotient v / d (d > 0): the grid magnitude g whose
+ * g * d is nearest to |v|, ties to the even mantissa, saturating at 6. */
+static unsigned e2m1_of_quotient(float v, float d)
+{
+    double a = fabs((double)v);
+    unsigned best = 0;
+    double bd = INFINITY;
+    for (unsigned c = 0; c < 8; ++c) {
+        double dist = fabs(oracle_dec_e2m1(c) * (double)d - a);
+        if (dist < bd || (dist == bd && (c & 1u) == 0u && (best & 1u) == 1u)) {
+            bd = dist;
+            best = c;
+        }
+    }
+    return (best != 0 && v < 0.0f) ? (best | 8u) : best;
+}
+
 /* Quantize n fp32 values (n a multiple of 16) to NVFP4: codes [n/2] (element
  * 2i in the low nibble), E4M3 scales [n/16]. */
 void oracle_quant_nvfp4(const float *v, int n, uint8_t *codes, uint8_t *scales)
@@ -455,8 +473,8 @@ void oracle_quant_nvfp4(const float *v, int n, uint8_t *codes, uint8_t *scales)
         for (int i = 0; i < 16; i += 2) {
             unsigned c0 = 0, c1 = 0;
             if (d != 0.0f) {
-                c0 = oracle_e2m1_rne(v[16 * b + i] / d);
-                c1 = oracle_e2m1_rne(v[16 * b + i + 1] / d);
+                c0 = e2m1_of_quotient(v[16 * b + i], d);
+                c1 = e2m1_of_quotient(v[16 * b + i + 1], d);
             }
             codes[8 * b + i / 2] = (uint8_t)(c0 | (c1 << 4));
         }

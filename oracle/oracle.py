@@ -267,7 +267,8 @@ def e2m1_rne(v: float) -> int:
 
 def quant_nvfp4(v) -> tuple:
     """fp32 rows [..., n] (n % 16 == 0) -> (codes uint8 [..., n/2], E4M3 scales uint8 [..., n/16]):
-    per 16 elements s = RNE_e4m3(min(amax/6, 448)), codes RNE_e2m1(v / e4m3(s)), in fp32."""
+    per 16 elements s = RNE_e4m3(min(amax/6, 448)) (amax/6 in fp32), codes RNE_e2m1 of the exact
+    quotient v / e4m3(s)."""
     a = _c(v, np.float32)
     shp = a.shape
     n = shp[-1]

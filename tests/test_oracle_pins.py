@@ -421,3 +421,45 @@ def test_w4a4_single_expert_equals_dense_ffn_on_quantized_activations():
     hc, hs = orc.quant_nvfp4(h)
     ref = torch.from_numpy(_torch_dequant(hc, hs, 1.0)) @ Wd.T
     assert np.allclose(got, ref.numpy(), rtol=1e-12, atol=1e-12)
+
+
+def test_quant_nvfp4_codes_round_the_exact_quotient():
+    # brute force in fp64 (exact here): each code is the grid value whose
+    # product with the block scale is nearest to the element, ties to the
+    # even mantissa; elements straddling the grid midpoints by one fp32 ulp
+    # are included, where an fp32 quotient would round onto the midpoint
+    vals = _e4m3_values()
+    grid = np.array([0, .5, 1, 1.5, 2, 3, 4, 6])
+    rng = np.random.default_rng(8)
+    for _ in range(100):
+        s = int(rng.integers(0x10, 0x70))
+        d = vals[s]
+        mids = np.array([.25, .75, 1.25, 1.75, 2.5, 3.5, 5.0]) * d
+        pick = rng.choice(mids, 15)
+        v = np.concatenate([[6 * d], pick * (1 + rng.choice([-1, 0, 1], 15) * 2.0 ** -23)]).astype(np.float32)
+        v *= rng.choice([-1, 1], 16).astype(np.float32)
+        codes, scales = orc.quant_nvfp4(v)
+        assert scales[0] == s
+        got = np.stack([codes & 15, codes >> 4], -1).reshape(-1)
+        for i, x in enumerate(v.astype(np.float64)):
+            dist = np.abs(grid * d - abs(x))
+            best = min(range(8), key=lambda c: (dist[c], c & 1))
+            want = best | (8 if (x < 0 and best) else 0)
+            assert got[i] == want, (s, x, got[i], want)
+
+
+def test_quant_nvfp4_exact_quotient_equals_fp32_division():
+    # the block scale has at most 4 significant bits and every E2M1 midpoint
+    # at most 3, so an fp32 quotient never rounds onto a midpoint that the
+    # exact quotient misses: both readings give the same codes
+    rng = np.random.default_rng(21)
+    v = (rng.standard_normal((400, 64)) * np.exp(rng.standard_normal((400, 1)) * 4)).astype(np.float32)
+    codes, scales = orc.quant_nvfp4(v)
+    got = np.stack([codes & 15, codes >> 4], -1).reshape(400, 64)
+    for r in range(0, 400, 7):
+        for b in range(4):
+            d = np.float32(orc.dec_e4m3(int(scales[r, b])))
+            for i in range(16):
+                x = v[r, 16 * b + i]
+                want = orc.e2m1_rne(float(np.float32(x / d))) if d != 0 else 0
+                assert got[r, 16 * b + i] == want
