@@ -312,9 +312,10 @@ int moe_host_plan_destroy(moe_host_plan *plan);
  * treats a 4-bit-activation format as its own execution contract.  Here the
  * activations entering each projection (x before gate_up, h before down) are
  * quantized to NVFP4 -- per 16 consecutive elements an E4M3 scale
- * s = RNE_e4m3(min(amax16 / 6, 448)) and E2M1 codes RNE_e2m1(v / e4m3(s)),
- * ties to the even mantissa, saturating at +-6, every step in fp32, no global
- * scale -- and both projections run as E2M1 x E2M1 products with both
+ * s = RNE_e4m3(min(amax16 / 6, 448)) (amax16 / 6 in fp32) and the E2M1
+ * codes of the exact quotient v / e4m3(s) rounded to nearest, ties to the
+ * even mantissa, saturating at +-6, no global scale; h is quantized from its
+ * fp32 value -- and both projections run as E2M1 x E2M1 products with both
  * sides' block scales applied by the MMA, fp32 accumulation, the weights'
  * global scale in the epilogue.  Different numerics from the W4A16 layer
  * (the activations lose precision): results are checked against the W4A4
@@ -353,6 +354,11 @@ int moe_layer_forward_w4a4_profiled(const uint16_t *x, const float *logits, moe_
  * K % 16 == 0; x, codes, scales 16-byte aligned. */
 int moe_quantize_nvfp4(const uint16_t *x, const int32_t *rows_of, int32_t n, int32_t K, uint8_t *codes,
                        uint8_t *scales, void *stream);
+
+/* moe_quantize_nvfp4 for fp32 rows x [*][K] (the precision h has when the
+ * layer quantizes it): the same quantizer, arguments and errors. */
+int moe_quantize_nvfp4_f32(const float *x, const int32_t *rows_of, int32_t n, int32_t K, uint8_t *codes,
+                           uint8_t *scales, void *stream);
 
 /* Test hook: one W4A4 projection over grouped, already quantized activation
  * rows.  mode 0: gate_up + SwiGLU, act [T*k][H/2] codes + [T*k][H/16] scales,

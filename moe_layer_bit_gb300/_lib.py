@@ -85,6 +85,7 @@ _SIGS = {
     "moe_layer_forward_w4a4": (INT, [P, P, W4N, W4N, Dims, P, P, P, P, SZ, P]),
     "moe_layer_forward_w4a4_profiled": (INT, [P, P, W4N, W4N, Dims, P, P, P, P, SZ, P, P]),
     "moe_quantize_nvfp4": (INT, [P, P, I32, I32, P, P, P]),
+    "moe_quantize_nvfp4_f32": (INT, [P, P, I32, I32, P, P, P]),
     "moe_debug_w4a4_gemm": (INT, [I32, P, P, P, W4N, Dims, P, P, P, P]),
     "moe_debug_layer_forward_config": (INT, [P, P, W4, W4, Dims, P, P, P, P, SZ, I32, I32, P, P]),
 }
@@ -304,6 +305,11 @@ def moe_layer_forward_w4a4(x, logits, w_gate_up: W4N, w_down: W4N, d, out, topk_
 def moe_quantize_nvfp4(x, rows_of, n: int, K: int, codes, scales, stream=None):
     _check(load().moe_quantize_nvfp4(_p(x), _p(rows_of), int(n), int(K), _p(codes), _p(scales), _s(stream)),
            "moe_quantize_nvfp4")
+
+
+def moe_quantize_nvfp4_f32(x, rows_of, n: int, K: int, codes, scales, stream=None):
+    _check(load().moe_quantize_nvfp4_f32(_p(x), _p(rows_of), int(n), int(K), _p(codes), _p(scales), _s(stream)),
+           "moe_quantize_nvfp4_f32")
 
 
 def moe_debug_w4a4_gemm(mode: int, act_codes, act_scales, offsets, w: W4N, d, out, out_scales, ws, stream=None):

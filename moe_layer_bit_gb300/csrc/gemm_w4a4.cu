@@ -7,9 +7,10 @@
 // treats a 4-bit-activation format as an execution contract of its own).
 //
 // Activation quantizer (x before gate_up, h before down): per 16 consecutive
-// elements s = RNE_e4m3(min(amax16 / 6, 448)) and codes RNE_e2m1(v / e4m3(s)),
-// ties to the even mantissa, saturating at +-6, all codes 0 when e4m3(s) is 0,
-// every step in fp32; no global scale.  Weights keep their NVFP4 format in the
+// elements s = RNE_e4m3(min(amax16 / 6, 448)) (amax16 / 6 in fp32) and the
+// codes RNE_e2m1 of the exact quotient v / e4m3(s), ties to the even
+// mantissa, saturating at +-6, all codes 0 when e4m3(s) is 0; no global
+// scale.  h is quantized from its fp32 value.  Weights keep their NVFP4 format in the
 // natural layout (codes [E][N][K/2], scales [E][N][K/16], global scale [E]),
 // read by TMA straight from it; the fp32 global scale is applied in the
 // epilogue.
@@ -34,14 +35,58 @@
 namespace moe {
 
 // ------------------------------------------------------------- quantizer
-// fp32 value -> E2M1 code (sign bit 3): nearest of the grid, ties to the even
-// mantissa, saturating at 6.  The thresholds are the midpoints of the grid
-// 0, .5, 1, 1.5, 2, 3, 4, 6, each tie going to the even neighbour.
-__device__ __forceinline__ uint32_t e2m1_rne(float v) {
-  const float a = fabsf(v);
-  const uint32_t idx = (uint32_t)(a > 0.25f) + (uint32_t)(a >= 0.75f) + (uint32_t)(a > 1.25f) +
-                       (uint32_t)(a >= 1.75f) + (uint32_t)(a > 2.5f) + (uint32_t)(a >= 3.5f) + (uint32_t)(a > 5.0f);
-  return (idx != 0u && v < 0.0f) ? (idx | 8u) : idx;
+// One 16-element block of NVFP4 (no global scale): the E4M3 scale s =
+// RNE_e4m3(min(amax / 6, 448)) and the E2M1 codes of v / e4m3(s), each the
+// grid value nearest to the exact quotient, ties to the even mantissa,
+// saturating at 6, all codes 0 when e4m3(s) is 0.
+
+// RNE_e4m3(min(amax / 6, 448)).  The quotient is amax * RN(1/6) corrected by
+// one FMA on the exact remainder, within half an ulp (plus 2^-24 ulp) of
+// amax / 6.  An E4M3 rounding midpoint m has 5 significant bits, so 6 m is
+// exact in fp32 and amax / 6 is either m itself (the corrected quotient is
+// then m) or at least 2/3 ulp away from it: the E4M3 rounding of the
+// corrected quotient is that of amax / 6, and of an IEEE division.
+__device__ __forceinline__ uint32_t e4m3_scale_of_amax(float amax) {
+  constexpr float kSixth = 0.16666667f;
+  const float q0 = amax * kSixth;
+  const float q = fmaf(fmaf(-6.0f, q0, amax), kSixth, q0);
+  return (uint32_t)__nv_cvt_float_to_fp8(fminf(q, 448.0f), __NV_SATFINITE, __NV_E4M3);
+}
+
+__device__ __forceinline__ float rcp_approx(float x) {
+  float r;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+  return r;
+}
+
+// Quotient v / d rounded to E2M1 by the hardware conversion.  d (an E4M3
+// value) has at most 4 significant bits: with rc within an ulp of 1 / d, q0 =
+// v rc is within a few ulps of v / d, so the remainder v - d q0 is exact and
+// q = q0 + (v - d q0) rc lies within half an ulp (plus 2^-22 ulp) of v / d.
+// Each E2M1 midpoint t has at most 3 significant bits, so t d is exact in
+// fp32 and v / d is either t (q is then t) or more than 0.53 ulp from it:
+// rounding q to E2M1 rounds v / d.
+__device__ __forceinline__ float e2m1_quotient(float v, float d, float rc) {
+  const float q0 = v * rc;
+  return fmaf(fmaf(-d, q0, v), rc, q0);
+}
+
+// Eight quotients -> one word of E2M1 codes, element i in bits 4i..4i+3;
+// codes of magnitude 0 carry no sign.
+__device__ __forceinline__ uint32_t e2m1x8(const float (&q)[16], int o) {
+  uint32_t w;
+  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b0, %2, %1;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b1, %4, %3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b2, %6, %5;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b3, %8, %7;\n\t"
+      "mov.b32 %0, {b0, b1, b2, b3};\n\t}"
+      : "=r"(w)
+      : "f"(q[o]), "f"(q[o + 1]), "f"(q[o + 2]), "f"(q[o + 3]), "f"(q[o + 4]), "f"(q[o + 5]), "f"(q[o + 6]),
+        "f"(q[o + 7]));
+  const uint32_t mag = w & 0x77777777u;
+  const uint32_t nonzero = (mag + 0x77777777u) & 0x88888888u;  // bit 3 of a nibble: magnitude != 0
+  return mag | (w & nonzero);
 }
 
 // One 16-element block: the E4M3 scale byte and 8 code bytes (element 2i in
@@ -55,29 +100,47 @@ __device__ __forceinline__ Nvfp4Block quant_block16(const float (&v)[16]) {
   float amax = 0.0f;
 #pragma unroll
   for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(v[i]));
-  float q = __fdiv_rn(amax, 6.0f);
-  q = fminf(q, 448.0f);
-  const __nv_fp8_storage_t s = __nv_cvt_float_to_fp8(q, __NV_SATFINITE, __NV_E4M3);
-  const float d = __half2float(__nv_cvt_fp8_to_halfraw(s, __NV_E4M3));
   Nvfp4Block b;
-  b.scale = (uint32_t)s;
-  b.codes[0] = b.codes[1] = 0u;
-  if (d != 0.0f) {
+  b.scale = e4m3_scale_of_amax(amax);
+  const float d = __half2float(__nv_cvt_fp8_to_halfraw((__nv_fp8_storage_t)b.scale, __NV_E4M3));
+  const float rc = rcp_approx(d);
+  float q[16];
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      const uint32_t c = e2m1_rne(__fdiv_rn(v[i], d));
-      b.codes[i >> 3] |= c << (4 * (i & 7));
-    }
-  }
+  for (int i = 0; i < 16; ++i) q[i] = e2m1_quotient(v[i], d, rc);
+  b.codes[0] = b.scale != 0u ? e2m1x8(q, 0) : 0u;
+  b.codes[1] = b.scale != 0u ? e2m1x8(q, 8) : 0u;
   return b;
 }
 
 // Quantize and gather: row p of the grouped view gets the NVFP4 form of
-// x[src[p]] (or x[p] when src is null).  One thread per 16-element block;
-// codes [n][H/2], scales [n][H/16].
-__global__ void __launch_bounds__(256) quant_gather_kernel(const uint16_t* __restrict__ x,
-                                                            const int32_t* __restrict__ src, long long nblocks,
-                                                            int bpr, uint8_t* __restrict__ codes,
+// x[src[p]] (or x[p] when src is null), x bf16 or fp32.  One thread per
+// 16-element block; codes [n][K/2], scales [n][K/16].
+__device__ __forceinline__ void load_block16(const uint16_t* xp, float (&v)[16]) {
+  const uint4* p = reinterpret_cast<const uint4*>(xp);
+  const uint4 w0 = p[0], w1 = p[1];
+  const uint32_t wd[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    v[2 * i] = __uint_as_float(wd[i] << 16);
+    v[2 * i + 1] = __uint_as_float(wd[i] & 0xFFFF0000u);
+  }
+}
+
+__device__ __forceinline__ void load_block16(const float* xp, float (&v)[16]) {
+  const float4* p = reinterpret_cast<const float4*>(xp);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float4 f = p[i];
+    v[4 * i] = f.x;
+    v[4 * i + 1] = f.y;
+    v[4 * i + 2] = f.z;
+    v[4 * i + 3] = f.w;
+  }
+}
+
+template <typename T>
+__global__ void __launch_bounds__(256) quant_gather_kernel(const T* __restrict__ x, const int32_t* __restrict__ src,
+                                                            long long nblocks, int bpr, uint8_t* __restrict__ codes,
                                                             uint8_t* __restrict__ scales) {
   pdl_wait();
   pdl_trigger();
@@ -86,46 +149,43 @@ __global__ void __launch_bounds__(256) quant_gather_kernel(const uint16_t* __res
     const long long p = g / bpr;
     const int b = (int)(g - p * bpr);
     const long long row = src != nullptr ? (long long)src[p] : p;
-    const uint4* xp = reinterpret_cast<const uint4*>(x + row * (long long)bpr * 16 + b * 16);
-    const uint4 w0 = xp[0], w1 = xp[1];
-    const uint32_t wd[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
     float v[16];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      v[2 * i] = __uint_as_float(wd[i] << 16);
-      v[2 * i + 1] = __uint_as_float(wd[i] & 0xFFFF0000u);
-    }
+    load_block16(x + row * (long long)bpr * 16 + b * 16, v);
     const Nvfp4Block q = quant_block16(v);
     *reinterpret_cast<uint2*>(codes + p * (long long)bpr * 8 + b * 8) = make_uint2(q.codes[0], q.codes[1]);
     scales[p * (long long)bpr + b] = (uint8_t)q.scale;
   }
 }
 
-cudaError_t launch_quant_gather(const uint16_t* x, const int32_t* src, int n, int K, uint8_t* codes, uint8_t* scales,
+template <typename T>
+cudaError_t launch_quant_gather(const T* x, const int32_t* src, int n, int K, uint8_t* codes, uint8_t* scales,
                                 cudaStream_t s) {
   if (n == 0) return cudaSuccess;
   const int bpr = K / 16;
   const long long nblocks = (long long)n * bpr;
   long long blocks = (nblocks + 255) / 256;
   if (blocks > 8192) blocks = 8192;
-  return launch_pdl(quant_gather_kernel, dim3((unsigned)blocks), dim3(256), 0, s, x, src, nblocks, bpr, codes,
+  return launch_pdl(quant_gather_kernel<T>, dim3((unsigned)blocks), dim3(256), 0, s, x, src, nblocks, bpr, codes,
                     scales);
 }
 
-// ------------------------------------------------------------- the GEMM
+// ------------------------------------------------------------- the GEMMs
 // Persistent, one CTA per SM, static tile stride (u = blockIdx.x, +
-// gridDim.x, ...) over the tile list of gemm_common.cuh.  Warp roles:
-//   0..3  epilogue (TMEM lane quadrant = warp): global scale, then SwiGLU and
-//         the NVFP4 quantization of h (gate_up), or fp32 y (down);
+// gridDim.x, ...) over the tile list of gemm_common.cuh.  A stage is K 256:
+// 128 code bytes (128-byte swizzled) and 16 scale bytes per row of A and B,
+// consumed by 4 block-scaled MMAs of K 64 (M 128, N = NB).  Warp roles:
+//   0..3  epilogue (TMEM lane quadrant = warp);
 //   4..7  scale factors: per stage, the E4M3 scales of A (rows 32q..32q+31)
 //         and a copy of B's, read from the stage in shared memory and stored
 //         into the warp's lane quadrant of a TMEM slot in the MMA's layout;
-//   8     TMA producer: A (weight codes and scales, natural layout; gate_up
-//         rows interleaved in 16-row boxes: rows 32q..32q+15 gate features,
-//         the next 16 the matching up features) and B (activation codes and
-//         scales); codes 128-byte swizzled; one stage = K 256 (128 code bytes
-//         and 16 scale bytes per row);
-//   9     TMEM owner and MMA issue (4 MMAs of K 64 per stage).
+//   8     TMA producer;
+//   9     TMEM owner and MMA issue.
+// gate_up (MODE 0) puts the tokens in the accumulator's lanes: A = TT
+// activation rows (the MMA still reads 128; rows TT.. of its result are not
+// used), B = 64 gate rows then the 64 matching up rows of the expert, so one
+// epilogue thread holds whole 16-feature blocks of h (gate columns 16 b..,
+// up columns 64 + 16 b..) and quantizes them without exchanging data.  down
+// (MODE 1) puts 128 weight rows (output features) in A and TT tokens in B.
 constexpr int kW4Warps = 10;
 constexpr int kW4Threads = kW4Warps * 32;
 constexpr int kW4WarpSf0 = 4;
@@ -133,26 +193,26 @@ constexpr int kW4WarpTma = 8;
 constexpr int kW4WarpMma = 9;
 constexpr int kW4StageK = 256;
 constexpr uint32_t kW4TmemCols = 512;
+constexpr int kGuFeat = 64;  // h features of a gate_up tile (MMA N = 2 * 64)
 
-template <int BN>
+template <int NB>
 struct Cfg4 {
-  // a stage: A codes (128 rows x 128 B, swizzled), B codes (BN rows x 128 B,
-  // swizzled), A scales (128 rows x 16 B), B scales (BN rows x 16 B)
+  // a stage: A codes (128 rows x 128 B, swizzled), B codes (NB rows x 128 B,
+  // swizzled), A scales (128 rows x 16 B), B scales (NB rows x 16 B)
   static constexpr int kA = 128 * 128;
-  static constexpr int kB = BN * 128;
+  static constexpr int kB = NB * 128;
   static constexpr int kOffAs = kA + kB;
   static constexpr int kOffBs = kOffAs + 128 * 16;
-  static constexpr int kBytes = kOffBs + BN * 16;      // bytes a stage's copies deliver
-  static constexpr int kStage = ((kBytes + 1023) / 1024) * 1024;
+  static constexpr int kStage = ((kOffBs + NB * 16 + 1023) / 1024) * 1024;
   static constexpr int NS0 = (200 * 1024) / kStage;
   static constexpr int NS = NS0 > 8 ? 8 : NS0;
   static constexpr int ND = 2;
-  static constexpr int kSfbPerMma = BN / 32 > 0 ? BN / 32 : 1;  // SFB columns an MMA reads
+  static constexpr int kSfbPerMma = NB / 32 > 0 ? NB / 32 : 1;  // SFB columns an MMA reads
   // every MMA's scale vectors start on a 4-column (128-bit) boundary
   static constexpr int kSfbStride = ((kSfbPerMma + 3) / 4) * 4;
   static constexpr int kSfSlot = 16 + 4 * kSfbStride;  // SFA (4 MMAs x 4 columns) + SFB
-  static_assert(kSfSlot % 4 == 0 && (ND * BN) % 4 == 0, "scale vectors on 4-column boundaries");
-  static constexpr int NSF0 = (int)(512 - ND * BN) / kSfSlot;
+  static_assert(kSfSlot % 4 == 0 && (ND * NB) % 4 == 0, "scale vectors on 4-column boundaries");
+  static constexpr int NSF0 = (int)(512 - ND * NB) / kSfSlot;
   static constexpr int NSF = NSF0 > 6 ? 6 : NSF0;
   static_assert(NSF >= 2 && NS >= 2, "rings need two slots");
   static constexpr int kOffBar = NS * kStage;
@@ -196,14 +256,16 @@ struct W4a4Launch {
   int I;                      // the expert intermediate size (gate_up: N = 2I)
 };
 
-
-// MODE 0: gate_up + SwiGLU, h quantized to NVFP4; MODE 1: down, fp32 y.
-template <int BN, int MODE>
+// MODE 0: gate_up + SwiGLU, h quantized to NVFP4; MODE 1: down, fp32 y.  TT
+// is the token tile.
+template <int MODE, int TT>
 __global__ void __launch_bounds__(kW4Threads, 1)
     w4a4_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_as,
                      const __grid_constant__ CUtensorMap tm_b, const __grid_constant__ CUtensorMap tm_bs,
                      const __grid_constant__ W4a4Launch L) {
-  using C = Cfg4<BN>;
+  constexpr int NB = MODE == 0 ? 2 * kGuFeat : TT;  // MMA N
+  constexpr int kRowsA = MODE == 0 ? TT : kTileM;   // rows of A a stage delivers
+  using C = Cfg4<NB>;
   constexpr int NS = C::NS, NSF = C::NSF, ND = C::ND;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -253,24 +315,25 @@ __global__ void __launch_bounds__(kW4Threads, 1)
   }
   pdl_wait();
   pdl_trigger();
-  build_tile_table(L.offsets, E, BN, s_off, s_tprefix, misc + 2);
+  build_tile_table(L.offsets, E, TT, s_off, s_tprefix, misc + 2);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = misc[0];
   const int ntok = (int)misc[2];
-  const int MT = L.N / kTileM;
+  const int MT = MODE == 0 ? L.I / kGuFeat : L.N / kTileM;  // weight tiles per expert
   const int total = ntok * MT;
   const int KS = L.K / kW4StageK;
-  const uint32_t sf_col0 = (uint32_t)(ND * BN);  // scale-factor slots after the accumulators
+  const uint32_t sf_col0 = (uint32_t)(ND * NB);  // scale-factor slots after the accumulators
 
   if (warp == kW4WarpTma) {
     // ------------------------------------------------------------ producer
+    constexpr uint32_t kTx = (uint32_t)((kRowsA + NB) * (128 + 16));
     int i = 0;
     bool ok = true;
     for (int u = blockIdx.x; u < total && ok; u += gridDim.x) {
       const TileCoord c = decode_tile(u, s_tprefix, E, MT);
-      const int p0 = s_off[c.e] + c.nt * BN;
+      const int p0 = s_off[c.e] + c.nt * TT;
       for (int ks = 0; ks < KS; ++ks, ++i) {
         const int s = i % NS;
         if (!__all_sync(0xFFFFFFFFu, mbar_wait(empty_bar(s), ((uint32_t)(i / NS) & 1u) ^ 1u, abort_flag, status))) {
@@ -279,25 +342,25 @@ __global__ void __launch_bounds__(kW4Threads, 1)
         }
         if (elect_one_sync()) {
           const uint32_t st = sbase + (uint32_t)(s * C::kStage);
-          mbar_arrive_expect_tx(full_bar(s), (uint32_t)C::kBytes);
+          mbar_arrive_expect_tx(full_bar(s), kTx);
           if (MODE == 0) {
-            // rows 32g..32g+15: gate features 64 mt + 16 g .., rows 32g+16..: the matching up features
-#pragma unroll
-            for (int g = 0; g < 4; ++g) {
-              const int gate_row = c.e * L.N + c.mt * 64 + 16 * g;
-              const int up_row = gate_row + L.I;
-              tma_load_2d(st + (uint32_t)(32 * g * 128), &tm_a, ks * 128, gate_row, full_bar(s));
-              tma_load_2d(st + (uint32_t)((32 * g + 16) * 128), &tm_a, ks * 128, up_row, full_bar(s));
-              tma_load_2d(st + C::kOffAs + (uint32_t)(32 * g * 16), &tm_as, ks * 16, gate_row, full_bar(s));
-              tma_load_2d(st + C::kOffAs + (uint32_t)((32 * g + 16) * 16), &tm_as, ks * 16, up_row, full_bar(s));
-            }
+            // A: the tile's activation rows; B: gate rows 64 mt.. of expert e,
+            // then the matching up rows (I further on)
+            const int gate_row = c.e * L.N + c.mt * kGuFeat;
+            const int up_row = gate_row + L.I;
+            tma_load_2d(st, &tm_a, ks * 128, p0, full_bar(s));
+            tma_load_2d(st + C::kOffAs, &tm_as, ks * 16, p0, full_bar(s));
+            tma_load_2d(st + C::kA, &tm_b, ks * 128, gate_row, full_bar(s));
+            tma_load_2d(st + C::kA + (uint32_t)(kGuFeat * 128), &tm_b, ks * 128, up_row, full_bar(s));
+            tma_load_2d(st + C::kOffBs, &tm_bs, ks * 16, gate_row, full_bar(s));
+            tma_load_2d(st + C::kOffBs + (uint32_t)(kGuFeat * 16), &tm_bs, ks * 16, up_row, full_bar(s));
           } else {
-            const int row = c.e * L.N + c.mt * 128;
+            const int row = c.e * L.N + c.mt * kTileM;
             tma_load_2d(st, &tm_a, ks * 128, row, full_bar(s));
             tma_load_2d(st + C::kOffAs, &tm_as, ks * 16, row, full_bar(s));
+            tma_load_2d(st + C::kA, &tm_b, ks * 128, p0, full_bar(s));
+            tma_load_2d(st + C::kOffBs, &tm_bs, ks * 16, p0, full_bar(s));
           }
-          tma_load_2d(st + C::kA, &tm_b, ks * 128, p0, full_bar(s));
-          tma_load_2d(st + C::kOffBs, &tm_bs, ks * 16, p0, full_bar(s));
         }
         __syncwarp();
       }
@@ -306,11 +369,11 @@ __global__ void __launch_bounds__(kW4Threads, 1)
       mbar_wait(full_bar(j % NS), (uint32_t)(j / NS) & 1u, nullptr, status, kDrainTimeoutNs);
   } else if (warp >= kW4WarpSf0 && warp < kW4WarpSf0 + 4) {
     // ------------------------------------------------------- scale factors
-    // Row m = 32 q + lane of A (a weight row) and column n = 32 cb + lane of
-    // B (an activation row): the 4 scale bytes of MMA j (K elements 64 j ..
-    // 64 j + 63 of the stage) form one 32-bit word, stored at lane m, column
-    // slot + 4 j + q (A) and lane 32 q + n % 32, column slot + 16 +
-    // j * kSfbStride + n / 32 (B, one copy per lane quadrant).
+    // Row m = 32 q + lane of A and column n = 32 cb + lane of B: the 4 scale
+    // bytes of MMA j (K elements 64 j .. 64 j + 63 of the stage) form one
+    // 32-bit word, stored at lane m, column slot + 4 j + q (A; zero for the
+    // rows a stage does not deliver) and lane 32 q + n % 32, column slot + 16
+    // + j * kSfbStride + n / 32 (B, one copy per lane quadrant).
     const int q = warp - kW4WarpSf0;
     const uint32_t t_lane = tmem_base + ((uint32_t)(32 * q) << 16);
     int i = 0;
@@ -326,24 +389,23 @@ __global__ void __launch_bounds__(kW4Threads, 1)
         }
         tc_fence_after();
         const uint8_t* st = smem + s * C::kStage;
-        const uint4 wa = *reinterpret_cast<const uint4*>(st + C::kOffAs + (32 * q + lane) * 16);
+        uint4 wa = make_uint4(0u, 0u, 0u, 0u);
+        if (32 * q < kRowsA) wa = *reinterpret_cast<const uint4*>(st + C::kOffAs + (32 * q + lane) * 16);
         const uint32_t col = sf_col0 + (uint32_t)(f * C::kSfSlot);
         tmem_st1(t_lane + col + 0u + q, wa.x);
         tmem_st1(t_lane + col + 4u + q, wa.y);
         tmem_st1(t_lane + col + 8u + q, wa.z);
         tmem_st1(t_lane + col + 12u + q, wa.w);
-        {
 #pragma unroll
-          for (int cb = 0; cb < C::kSfbPerMma; ++cb) {
-            const int n = 32 * cb + lane;
-            uint4 wb = make_uint4(0u, 0u, 0u, 0u);
-            if (n < BN) wb = *reinterpret_cast<const uint4*>(st + C::kOffBs + n * 16);
-            const uint32_t cbase = col + 16u + (uint32_t)cb;
-            tmem_st1(t_lane + cbase + 0u * C::kSfbStride, wb.x);
-            tmem_st1(t_lane + cbase + 1u * C::kSfbStride, wb.y);
-            tmem_st1(t_lane + cbase + 2u * C::kSfbStride, wb.z);
-            tmem_st1(t_lane + cbase + 3u * C::kSfbStride, wb.w);
-          }
+        for (int cb = 0; cb < C::kSfbPerMma; ++cb) {
+          const int n = 32 * cb + lane;
+          uint4 wb = make_uint4(0u, 0u, 0u, 0u);
+          if (n < NB) wb = *reinterpret_cast<const uint4*>(st + C::kOffBs + n * 16);
+          const uint32_t cbase = col + 16u + (uint32_t)cb;
+          tmem_st1(t_lane + cbase + 0u * C::kSfbStride, wb.x);
+          tmem_st1(t_lane + cbase + 1u * C::kSfbStride, wb.y);
+          tmem_st1(t_lane + cbase + 2u * C::kSfbStride, wb.z);
+          tmem_st1(t_lane + cbase + 3u * C::kSfbStride, wb.w);
         }
         tc_wait_st();
         tc_fence_before();
@@ -353,7 +415,7 @@ __global__ void __launch_bounds__(kW4Threads, 1)
     }
   } else if (warp == kW4WarpMma) {
     // ------------------------------------------------------------ MMA issue
-    constexpr uint32_t idesc = idesc_mxf4(kTileM, BN);
+    constexpr uint32_t idesc = idesc_mxf4(kTileM, NB);
     int i = 0, it = 0;
     bool ok = true;
     for (int u = blockIdx.x; u < total && ok; u += gridDim.x, ++it) {
@@ -361,7 +423,7 @@ __global__ void __launch_bounds__(kW4Threads, 1)
       if (!__all_sync(0xFFFFFFFFu, mbar_wait(dempty_bar(d), ((uint32_t)(it / ND) & 1u) ^ 1u, abort_flag, status)))
         break;
       tc_fence_after();
-      const uint32_t d_tmem = tmem_base + (uint32_t)(d * BN);
+      const uint32_t d_tmem = tmem_base + (uint32_t)(d * NB);
       for (int ks = 0; ks < KS; ++ks, ++i) {
         const int s = i % NS, f = i % NSF;
         const bool got = mbar_wait(full_bar(s), (uint32_t)(i / NS) & 1u, abort_flag, status) &&
@@ -401,61 +463,67 @@ __global__ void __launch_bounds__(kW4Threads, 1)
       const int d = it % ND;
       if (!__all_sync(0xFFFFFFFFu, mbar_wait(dfull_bar(d), (uint32_t)(it / ND) & 1u, abort_flag, status))) break;
       tc_fence_after();
-      const int p0 = s_off[c.e] + c.nt * BN;
-      const int nvalid = min(BN, s_off[c.e + 1] - p0);
+      const int p0 = s_off[c.e] + c.nt * TT;
+      const int nvalid = min(TT, s_off[c.e + 1] - p0);
       const float gsc = __ldg(L.gscale + c.e);
-      const uint32_t t_acc = tmem_base + ((uint32_t)(32 * q) << 16) + (uint32_t)(d * BN);
-#pragma unroll 1
-      for (int cc = 0; cc < BN / 16; ++cc) {
-        uint32_t v[16];
-        tmem_ld16(t_acc + (uint32_t)(cc * 16), v);
-        tc_wait_ld();
-        if (cc * 16 >= nvalid) continue;
-        if (MODE == 0) {
-          // lanes 0..15: gate features f0 + lane, lanes 16..31: the same up
-          // features; after the exchange lanes 0..15 hold column 16 cc + j and
-          // lanes 16..31 column 16 cc + j + 8, each half one 16-feature block
-          const int f0 = c.mt * 64 + 16 * q;
-          const bool is_gate = lane < 16;
-          uint8_t* hc = reinterpret_cast<uint8_t*>(L.out);
+      const uint32_t t_acc = tmem_base + ((uint32_t)(32 * q) << 16) + (uint32_t)(d * NB);
+      if (MODE == 0) {
+        // this thread's token: row r of the tile; h block b = SwiGLU of gate
+        // columns 16 b.. and up columns 64 + 16 b.., then its NVFP4 form
+        const int r = 32 * q + lane;
+        uint32_t words[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
+        uint32_t sc = 0u;
+        if (32 * q < TT && 32 * q < nvalid) {
 #pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            const float a = __uint_as_float(v[j]);
-            const float b = __uint_as_float(v[j + 8]);
-            const float recv = __shfl_xor_sync(0xFFFFFFFFu, is_gate ? b : a, 16);
-            const float g = (is_gate ? a : recv) * gsc;
-            const float up = (is_gate ? recv : b) * gsc;
-            const float hv = g / (1.0f + __expf(-g)) * up;
-            // the block's scale: amax over the half warp, in fp32
-            float amax = fabsf(hv);
+          for (int b = 0; b < kGuFeat / 16; ++b) {
+            uint32_t vg[16], vu[16];
+            tmem_ld16(t_acc + (uint32_t)(16 * b), vg);
+            tmem_ld16(t_acc + (uint32_t)(kGuFeat + 16 * b), vu);
+            tc_wait_ld();
+            float h[16];
 #pragma unroll
-            for (int o = 1; o < 16; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
-            const float qs = fminf(__fdiv_rn(amax, 6.0f), 448.0f);
-            const __nv_fp8_storage_t sc = __nv_cvt_float_to_fp8(qs, __NV_SATFINITE, __NV_E4M3);
-            const float dd = __half2float(__nv_cvt_fp8_to_halfraw(sc, __NV_E4M3));
-            const uint32_t code = dd != 0.0f ? e2m1_rne(__fdiv_rn(hv, dd)) : 0u;
-            const uint32_t other = __shfl_xor_sync(0xFFFFFFFFu, code, 1);
-            const int col = cc * 16 + j + (is_gate ? 0 : 8);
-            const int fi = lane & 15;
-            if (col < nvalid) {
-              const size_t row = (size_t)(p0 + col);
-              if ((fi & 1) == 0) hc[row * (L.out_ld / 2) + (f0 + fi) / 2] = (uint8_t)(code | (other << 4));
-              if (fi == 0) L.out_scales[row * (L.out_ld / 16) + f0 / 16] = (uint8_t)sc;
+            for (int j = 0; j < 16; ++j) {
+              const float g = __uint_as_float(vg[j]) * gsc;
+              const float up = __uint_as_float(vu[j]) * gsc;
+              h[j] = __fdividef(g, 1.0f + __expf(-g)) * up;
             }
+            const Nvfp4Block nb = quant_block16(h);
+            words[2 * b] = nb.codes[0];
+            words[2 * b + 1] = nb.codes[1];
+            sc |= nb.scale << (8 * b);
           }
-        } else {
-          const int n = c.mt * kTileM + 32 * q + lane;
-          float* y = reinterpret_cast<float*>(L.out);
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(dempty_bar(d));
+        if (r < nvalid) {
+          const size_t p = (size_t)(p0 + r);
+          uint4* hc = reinterpret_cast<uint4*>(static_cast<uint8_t*>(L.out) + p * (size_t)(L.out_ld / 2) +
+                                               (size_t)c.mt * (kGuFeat / 2));
+          hc[0] = make_uint4(words[0], words[1], words[2], words[3]);
+          hc[1] = make_uint4(words[4], words[5], words[6], words[7]);
+          *reinterpret_cast<uint32_t*>(L.out_scales + p * (size_t)(L.out_ld / 16) + (size_t)c.mt * (kGuFeat / 16)) =
+              sc;
+        }
+      } else {
+        const int n = c.mt * kTileM + 32 * q + lane;
+        float* y = reinterpret_cast<float*>(L.out);
+#pragma unroll 1
+        for (int cc = 0; cc < NB / 16; ++cc) {
+          uint32_t v[16];
+          tmem_ld16(t_acc + (uint32_t)(cc * 16), v);
+          tc_wait_ld();
+          if (cc * 16 >= nvalid) continue;
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
             const int col = cc * 16 + j;
             if (col < nvalid) y[(size_t)(p0 + col) * L.out_ld + n] = __uint_as_float(v[j]) * gsc;
           }
         }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(dempty_bar(d));
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(dempty_bar(d));
     }
   }
   // warps 4..7 (scale factors) and the producer are done; everyone meets here
@@ -511,16 +579,23 @@ struct W4a4Args {
   int rows, E, N, K, I, out_ld;
 };
 
-template <int BN, int MODE>
+template <int MODE, int TT>
 static cudaError_t launch_w4a4_cfg(const W4a4Args& a, cudaStream_t s) {
-  using C = Cfg4<BN>;
+  constexpr int NB = MODE == 0 ? 2 * kGuFeat : TT;
+  using C = Cfg4<NB>;
   CUtensorMap tm[4];
-  const int arows = MODE == 0 ? 16 : 128;
-  if (!encode_u8(&tm[0], a.w_codes, a.K / 2, (long long)a.E * a.N, 128, arows, true) ||
-      !encode_u8(&tm[1], a.w_scales, a.K / 16, (long long)a.E * a.N, 16, arows, false) ||
-      !encode_u8(&tm[2], a.a_codes, a.K / 2, a.rows, 128, BN, true) ||
-      !encode_u8(&tm[3], a.a_scales, a.K / 16, a.rows, 16, BN, false))
-    return cudaErrorInvalidValue;
+  const long long wrows = (long long)a.E * a.N;
+  // MODE 0: A = activations (TT-row boxes), B = weights (64-row boxes);
+  // MODE 1: A = weights (128-row boxes), B = activations (TT-row boxes)
+  const bool ok = MODE == 0 ? encode_u8(&tm[0], a.a_codes, a.K / 2, a.rows, 128, TT, true) &&
+                                  encode_u8(&tm[1], a.a_scales, a.K / 16, a.rows, 16, TT, false) &&
+                                  encode_u8(&tm[2], a.w_codes, a.K / 2, wrows, 128, kGuFeat, true) &&
+                                  encode_u8(&tm[3], a.w_scales, a.K / 16, wrows, 16, kGuFeat, false)
+                            : encode_u8(&tm[0], a.w_codes, a.K / 2, wrows, 128, kTileM, true) &&
+                                  encode_u8(&tm[1], a.w_scales, a.K / 16, wrows, 16, kTileM, false) &&
+                                  encode_u8(&tm[2], a.a_codes, a.K / 2, a.rows, 128, TT, true) &&
+                                  encode_u8(&tm[3], a.a_scales, a.K / 16, a.rows, 16, TT, false);
+  if (!ok) return cudaErrorInvalidValue;
   W4a4Launch L;
   L.gscale = a.gscale;
   L.offsets = a.offsets;
@@ -539,17 +614,18 @@ static cudaError_t launch_w4a4_cfg(const W4a4Args& a, cudaStream_t s) {
   err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (err != cudaSuccess) return err;
   const long long n = a.rows;
-  const long long max_tiles = (long long)(a.N / kTileM) * (n / BN + (n < a.E ? n : a.E));
+  const long long mt = MODE == 0 ? a.I / kGuFeat : a.N / kTileM;
+  const long long max_tiles = mt * (n / TT + (n < a.E ? n : a.E));
   const int grid = (int)(max_tiles < sms ? max_tiles : sms);
   if (grid <= 0) return cudaSuccess;
   const int smem = C::bytes(a.E);
-  auto kern = w4a4_gemm_kernel<BN, MODE>;
+  auto kern = w4a4_gemm_kernel<MODE, TT>;
   err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (err != cudaSuccess) return err;
   return launch_pdl(kern, dim3(grid), dim3(kW4Threads), smem, s, tm[0], tm[1], tm[2], tm[3], L);
 }
 
-// Token tile of the W4A4 GEMM: 32, 64 or 128 rows, about twice the mean rows per expert.
+// Token tile of the W4A4 GEMMs: 32, 64 or 128 rows, about twice the mean rows per expert.
 int w4a4_token_tile(int rows, int E) {
   const long long mean2 = 2LL * rows / (E > 0 ? E : 1);
   return mean2 <= 32 ? 32 : mean2 <= 64 ? 64 : 128;
@@ -558,12 +634,12 @@ int w4a4_token_tile(int rows, int E) {
 cudaError_t launch_w4a4(int mode, const W4a4Args& a, cudaStream_t s) {
   if (a.rows == 0) return cudaSuccess;
   switch (w4a4_token_tile(a.rows, a.E) * 2 + mode) {
-    case 64: return launch_w4a4_cfg<32, 0>(a, s);
-    case 65: return launch_w4a4_cfg<32, 1>(a, s);
-    case 128: return launch_w4a4_cfg<64, 0>(a, s);
-    case 129: return launch_w4a4_cfg<64, 1>(a, s);
-    case 256: return launch_w4a4_cfg<128, 0>(a, s);
-    default: return launch_w4a4_cfg<128, 1>(a, s);
+    case 64: return launch_w4a4_cfg<0, 32>(a, s);
+    case 65: return launch_w4a4_cfg<1, 32>(a, s);
+    case 128: return launch_w4a4_cfg<0, 64>(a, s);
+    case 129: return launch_w4a4_cfg<1, 64>(a, s);
+    case 256: return launch_w4a4_cfg<0, 128>(a, s);
+    default: return launch_w4a4_cfg<1, 128>(a, s);
   }
 }
 
@@ -729,6 +805,15 @@ int moe_quantize_nvfp4(const uint16_t* x, const int32_t* rows_of, int32_t n, int
   return cuda_rc(moe::launch_quant_gather(x, rows_of, n, K, codes, scales, reinterpret_cast<cudaStream_t>(stream)));
 }
 
+int moe_quantize_nvfp4_f32(const float* x, const int32_t* rows_of, int32_t n, int32_t K, uint8_t* codes,
+                           uint8_t* scales, void* stream) {
+  if (n < 0 || K <= 0 || K % 16 != 0) return MOE_ERR_INVALID_ARG;
+  if (n == 0) return MOE_OK;
+  if (x == nullptr || codes == nullptr || scales == nullptr) return MOE_ERR_INVALID_ARG;
+  if (!al16(x) || !al16(codes) || !al16(scales)) return MOE_ERR_MISALIGNED;
+  return cuda_rc(moe::launch_quant_gather(x, rows_of, n, K, codes, scales, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 }  // extern "C"
 
 extern "C" int moe_debug_w4a4_gemm(int32_t mode, const uint8_t* act_codes, const uint8_t* act_scales,
@@ -741,6 +826,9 @@ extern "C" int moe_debug_w4a4_gemm(int32_t mode, const uint8_t* act_codes, const
       w.scales == nullptr || w.global_scale == nullptr || out == nullptr || ws == nullptr ||
       (mode == 0 && out_scales == nullptr))
     return MOE_ERR_INVALID_ARG;
+  if (!al16(act_codes) || !al16(act_scales) || !al16(w.codes) || !al16(w.scales) || !al16(out) ||
+      (mode == 0 && !al16(out_scales)))
+    return MOE_ERR_MISALIGNED;
   moe::W4a4Args a{};
   a.w_codes = w.codes;
   a.w_scales = w.scales;

@@ -58,6 +58,49 @@ def test_quantizer_bit_exact_with_edge_blocks():
     assert np.array_equal(gc, rc[rows]) and np.array_equal(gs, rs[rows])
 
 
+def _ulps(x, k):
+    # the fp32 value k ulps above (k > 0) or below (k < 0) x > 0
+    x = np.float32(x)
+    for _ in range(abs(int(k))):
+        x = np.nextafter(x, np.float32(np.inf) if k > 0 else np.float32(0), dtype=np.float32)
+    return np.float32(x)
+
+
+def test_fp32_quantizer_bit_exact_around_every_midpoint():
+    # fp32 blocks (the precision of h), one block per row: for every E4M3
+    # scale s, blocks whose amax 6 e4m3(s) makes s their scale and whose other
+    # elements sit on, or 1..3 ulps either side of, an E2M1 midpoint times
+    # e4m3(s); then blocks whose amax is 6 x an E4M3 midpoint, or 1..2 ulps
+    # either side of it
+    e4 = np.array([orc.dec_e4m3(c) for c in range(127)])
+    mids = np.array([.25, .75, 1.25, 1.75, 2.5, 3.5, 5.0])
+    rng = np.random.default_rng(5)
+    rows = []
+    for s in range(1, 127):
+        d = e4[s]
+        for _ in range(4):
+            v = np.empty(16, np.float32)
+            v[0] = np.float32(6 * d)
+            for j in range(1, 16):
+                v[j] = _ulps(rng.choice(mids) * d, rng.integers(-3, 4))
+            rows.append(v * rng.choice([-1, 1], 16).astype(np.float32))
+    for s in range(126):
+        for k in (-2, -1, 0, 1, 2):
+            a = _ulps(3 * (e4[s] + e4[s + 1]), k)  # 6 x the midpoint, exact in fp32
+            v = np.clip(rng.standard_normal(16).astype(np.float32) * np.float32(a / 4), -a, a)
+            v[int(rng.integers(16))] = -a if k % 2 else a
+            rows.append(v)
+    X = torch.from_numpy(np.stack(rows).astype(np.float32))
+    n, K = X.shape
+    codes = torch.empty(n, K // 2, dtype=torch.uint8, device=DEV)
+    scales = torch.empty(n, K // 16, dtype=torch.uint8, device=DEV)
+    _lib.moe_quantize_nvfp4_f32(X.to(DEV), None, n, K, codes, scales)
+    torch.cuda.synchronize()
+    rc, rs = orc.quant_nvfp4(X.numpy())
+    assert np.array_equal(scales.cpu().numpy(), rs)
+    assert np.array_equal(codes.cpu().numpy(), rc)
+
+
 def _deq(codes, scales):
     e2m1 = np.array([0, .5, 1, 1.5, 2, 3, 4, 6, -0., -.5, -1, -1.5, -2, -3, -4, -6])
     v = e2m1[np.stack([codes & 15, codes >> 4], -1).reshape(codes.shape[0], -1)]
@@ -92,6 +135,48 @@ def test_down_projection_matches_fp64_products(T, H, I, E):
     got = y.cpu().numpy().astype(np.float64)
     # fp32 accumulation of I exact products: relative error ~ sqrt(I) * 2^-24
     assert np.linalg.norm(got - ref) / np.linalg.norm(ref) < 4 * np.sqrt(I) * 2.0 ** -24
+
+
+@pytest.mark.parametrize("T,H,I,E", [(40, 256, 256, 3), (300, 512, 512, 5)])
+def test_gate_up_projection_h_codes(T, H, I, E):
+    # the gate_up GEMM alone (ragged expert groups, several token and feature
+    # tiles): h = SwiGLU of exact-product sums, quantized.  The kernel's h is
+    # fp32 (fp32 accumulation, fast exp): its NVFP4 form may differ from the
+    # fp64 one only where h lies within a few ulps of a rounding boundary
+    rng = np.random.default_rng(T + I)
+    ac = rng.integers(0, 256, (T, H // 2), dtype=np.uint8)
+    asc = rng.integers(0x18, 0x28, (T, H // 16), dtype=np.uint8)
+    wc = rng.integers(0, 256, (E, 2 * I, H // 2), dtype=np.uint8)
+    wsc = rng.integers(0x18, 0x28, (E, 2 * I, H // 16), dtype=np.uint8)
+    gs = rng.uniform(0.5, 2, E).astype(np.float32)
+    counts = np.bincount(rng.integers(0, E, T), minlength=E)
+    offs = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+    hc = torch.empty(T, I // 2, dtype=torch.uint8, device=DEV)
+    hs = torch.empty(T, I // 16, dtype=torch.uint8, device=DEV)
+    st = torch.zeros(64, dtype=torch.int32, device=DEV)
+    w = [torch.from_numpy(a).to(DEV) for a in (wc, wsc, gs)]
+    _lib.moe_debug_w4a4_gemm(0, torch.from_numpy(ac).to(DEV), torch.from_numpy(asc).to(DEV),
+                             torch.from_numpy(offs).to(DEV), _lib.w4n(*w), _lib.dims(T, H, I, E, 1), hc, hs, st)
+    assert _lib.moe_get_device_status(st) == _lib.MOE_OK
+    A = _deq(ac, asc)
+    h = np.empty((T, I))
+    for e in range(E):
+        W = _deq(wc[e], wsc[e]) * float(gs[e])
+        g = A[offs[e]:offs[e + 1]] @ W[:I].T
+        u = A[offs[e]:offs[e + 1]] @ W[I:].T
+        h[offs[e]:offs[e + 1]] = g / (1 + np.exp(-g)) * u
+    rc, rs = orc.quant_nvfp4(h.astype(np.float32))
+    gc, gsc = hc.cpu().numpy(), hs.cpu().numpy()
+    assert (gsc != rs).mean() < 2e-3
+    nib = lambda c: np.stack([c & 15, c >> 4], -1)
+    assert (nib(gc) != nib(rc)).mean() < 2e-3
+    # every element of a block below the scale's saturation (amax <= 6 x 448)
+    # within one grid step (2 x its scale) of the fp64 h
+    got = _deq(gc, gsc)
+    step = np.repeat(np.array([orc.dec_e4m3(int(c)) for c in range(256)])[gsc], 16, axis=1) * 2
+    inside = np.repeat(np.abs(h).reshape(T, -1, 16).max(-1) <= 6 * 448, 16, axis=1)
+    assert inside.mean() > 0.9
+    assert np.all((np.abs(got - h) <= step + 1e-6 * np.abs(h))[inside])
 
 
 @pytest.mark.parametrize("name", list(CASES))
