@@ -25,6 +25,7 @@ from __future__ import annotations
 
 import dataclasses
 import math
+import re
 
 import numpy as np
 import torch
@@ -65,9 +66,15 @@ WORKLOADS = [
 
 
 def by_name(name: str) -> Workload:
+    """A workload of WORKLOADS by its name or its first word, or an arbitrary
+    shape named custom_T<T>_H<H>_I<I>_E<E>_k<k> (normal router, seed 2000)."""
     for w in WORKLOADS:
         if w.name == name or w.name.split("_")[0] == name:
             return w
+    m = re.fullmatch(r"custom_T(\d+)_H(\d+)_I(\d+)_E(\d+)_k(\d+)", name)
+    if m:
+        T, H, I, E, k = (int(g) for g in m.groups())
+        return Workload(name, T, H, I, E, k, "normal", 2000)
     raise KeyError(name)
 
 
