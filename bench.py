@@ -541,7 +541,9 @@ class W4A4Bench(DeviceBench):
 
     def measure(self, steps, warmup, dist, world):
         m = super().measure(steps, warmup, dist, world)
-        m["gpu_launches"] = None
+        m["gpu_launches"] = self.lib.moe_w4a4_kernel_launches(self.dims) * steps
+        lr = m["layer_roofline"]
+        lr["frac_tensor_fp4"] = lr.pop("frac_tensor") / FP4_OVER_BF16
         m["stages_ms"] = dict(zip(["route_group", "quantize_gather", "gate_up_swiglu", "down", "combine"],
                                   m["stages_ms"].values()))
         return m

@@ -331,6 +331,11 @@ typedef struct {
  * W4A16 limits and additionally H % 256 == 0, I % 256 == 0. */
 size_t moe_w4a4_workspace_bytes(moe_dims d);
 
+/* Host-only: the number of kernels one moe_layer_forward_w4a4 call launches
+ * (the routing + grouping launches, then quantize-and-gather, gate_up, down
+ * and combine); 0 for T == 0, minus the moe_status for invalid dims. */
+int moe_w4a4_kernel_launches(moe_dims d);
+
 /* The W4A4 layer: route -> group -> quantize and gather x -> gate_up +
  * SwiGLU (h quantized in the epilogue) -> down -> combine, as
  * moe_layer_forward with the activation quantization above.  out bf16 [T][H];

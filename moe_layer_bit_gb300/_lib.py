@@ -82,6 +82,7 @@ _SIGS = {
     "moe_debug_counter_timeout_probe": (INT, [P, ctypes.c_uint64, P]),
     "moe_debug_stream_read": (INT, [P, SZ, P, P]),
     "moe_w4a4_workspace_bytes": (SZ, [Dims]),
+    "moe_w4a4_kernel_launches": (ctypes.c_int, [Dims]),
     "moe_layer_forward_w4a4": (INT, [P, P, W4N, W4N, Dims, P, P, P, P, SZ, P]),
     "moe_layer_forward_w4a4_profiled": (INT, [P, P, W4N, W4N, Dims, P, P, P, P, SZ, P, P]),
     "moe_quantize_nvfp4": (INT, [P, P, I32, I32, P, P, P]),
@@ -294,6 +295,10 @@ def w4n(codes: torch.Tensor, scales: torch.Tensor, global_scale: torch.Tensor) -
 
 def moe_w4a4_workspace_bytes(d: Dims) -> int:
     return int(load().moe_w4a4_workspace_bytes(d))
+
+
+def moe_w4a4_kernel_launches(d: Dims) -> int:
+    return int(load().moe_w4a4_kernel_launches(d))
 
 
 def moe_layer_forward_w4a4(x, logits, w_gate_up: W4N, w_down: W4N, d, out, topk_ids, topk_w, ws, ws_bytes,

@@ -715,6 +715,14 @@ size_t moe_w4a4_workspace_bytes(moe_dims d) {
   return layout4(d).total;
 }
 
+int moe_w4a4_kernel_launches(moe_dims d) {
+  const int rc = check4(d);
+  if (rc != MOE_OK) return -rc;
+  if (d.T == 0) return 0;
+  // routing + grouping, quantize + gather of x, gate_up, down, combine
+  return moe::route_group_launches(d.T, d.E, d.k, false) + 4;
+}
+
 int moe_layer_forward_w4a4_profiled(const uint16_t* x, const float* logits, moe_w4n w_gate_up, moe_w4n w_down,
                                     moe_dims d, uint16_t* out, int32_t* topk_ids, float* topk_w, void* ws,
                                     size_t ws_bytes, void* stream, void* const* ev);

@@ -132,3 +132,13 @@ def test_host_plan_argument_checks(lib):
                                     ctypes.byref(plan)) == _lib.MOE_ERR_UNSUPPORTED_SHAPE
     assert lib.moe_host_plan_run(None) == _lib.MOE_ERR_INVALID_ARG
     assert lib.moe_host_plan_destroy(None) == _lib.MOE_OK
+
+
+@pytest.mark.parametrize("dims,launches", [
+    ((0, 2048, 768, 128, 8), 0),
+    ((32, 2048, 768, 128, 8), 5),       # routing + grouping block, quantize + gather, gate_up, down, combine
+    ((800, 2048, 512, 256, 8), 8),      # chunked grouping (4 launches) + 4
+    ((16, 256, 128, 8, 2), -_lib.MOE_ERR_UNSUPPORTED_SHAPE),  # I below the W4A4 stage of 256
+])
+def test_w4a4_kernel_launch_count(lib, dims, launches):
+    assert _lib.moe_w4a4_kernel_launches(_lib.dims(*dims)) == launches
