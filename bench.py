@@ -284,18 +284,22 @@ def run_reference(args, wl, dist, rank, world):
 
 
 # ------------------------------------------------------------------ ours
-def _kernel_hash() -> str:
+W4A16_SOURCES = ("gemm_w4a16.cu", "gemm_common.cuh", "device_common.cuh")
+W4A4_SOURCES = ("gemm_w4a4.cu", "gemm_common.cuh", "device_common.cuh")
+
+
+def _kernel_hash(files=W4A16_SOURCES) -> str:
     h = hashlib.sha256()
-    for f in ("gemm_w4a16.cu", "gemm_common.cuh", "device_common.cuh"):
+    for f in files:
         with open(os.path.join(ROOT, "moe_layer_bit_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
 
 
-def _traffic_from_profile(wl):
+def _traffic_from_profile(wl, prefix="gemm_", files=W4A16_SOURCES):
     """Per-launch DRAM bytes of the dominant GEMM launch from the committed ncu summary, or None
     if the summary is missing or was taken on a different kernel source."""
-    p = os.path.join(ROOT, "profiles", f"gemm_{wl.name}.txt")
+    p = os.path.join(ROOT, "profiles", f"{prefix}{wl.name}.txt")
     if not os.path.exists(p):
         return None
     kv = {}
@@ -304,7 +308,7 @@ def _traffic_from_profile(wl):
             if ":" in line and not line.startswith("#"):
                 k, v = line.split(":", 1)
                 kv[k.strip()] = v.strip()
-    if kv.get("kernel_source_sha256_16") != _kernel_hash():
+    if kv.get("kernel_source_sha256_16") != _kernel_hash(files):
         return None
     try:
         return float(kv["dram_bytes_per_launch"])
@@ -553,16 +557,31 @@ class W4A4Bench(DeviceBench):
         n = wl.T * wl.k
         _, tf_peak, tf_sus, peak_kind = _peaks()
         fp4_peak, fp4_sus = tf_peak * FP4_OVER_BF16, tf_sus * FP4_OVER_BF16
+        hbm_peak = _peaks()[0]
         gu_ms, dn_ms = float(stage_ms[:, 2].mean()), float(stage_ms[:, 3].mean())
         gu_flops, dn_flops = 4 * n * wl.H * wl.I, 2 * n * wl.H * wl.I
+        # NVFP4 weights of the touched experts, x's NVFP4 rows read, h's written (9/16 B per element)
+        gu_bytes = touched * (2 * wl.I * wl.H * 9 // 16 + 4) + n * wl.H * 9 // 16 + n * wl.I * 9 // 16
+        dn_bytes = touched * (wl.H * wl.I * 9 // 16 + 4) + n * wl.I * 9 // 16 + n * wl.H * 4
         a = gu_flops / (gu_ms * 1e-3) / 1e12
-        return {"bound": "tensor", "achieved": a, "peak": fp4_peak, "unit": "TFLOP/s", "frac": a / fp4_peak,
-                "frac_sustained_peak": a / fp4_sus,
-                "peak_kind": f"{peak_kind} burst cuBLAS bf16 GEMM x {FP4_OVER_BF16:g} (nominal dense FP4 / BF16)",
-                "algorithmic_flops_per_launch": gu_flops, "launch_ms": gu_ms,
-                "kernel": "w4a4_gemm_kernel (gate_up + SwiGLU + NVFP4 quantization of h)", "traffic": None,
-                "down": {"launch_ms": dn_ms, "achieved_tflops": dn_flops / (dn_ms * 1e-3) / 1e12,
-                         "frac_tensor_fp4": dn_flops / (dn_ms * 1e-3) / 1e12 / fp4_peak}}
+        ab = gu_bytes / (gu_ms * 1e-3) / 1e9
+        if a / fp4_peak > ab / hbm_peak:
+            r = {"bound": "tensor", "achieved": a, "peak": fp4_peak, "unit": "TFLOP/s", "frac": a / fp4_peak,
+                 "frac_sustained_peak": a / fp4_sus,
+                 "peak_kind": f"{peak_kind} burst cuBLAS bf16 GEMM x {FP4_OVER_BF16:g} (nominal dense FP4 / BF16)",
+                 "algorithmic_flops_per_launch": gu_flops}
+        else:
+            r = {"bound": "hbm", "achieved": ab, "peak": hbm_peak, "unit": "GB/s", "frac": ab / hbm_peak,
+                 "peak_kind": f"{peak_kind} burst copy bandwidth", "frac_nominal_7900": ab / NOMINAL_HBM_GBS,
+                 "algorithmic_bytes_per_launch": gu_bytes}
+        r.update({"launch_ms": gu_ms, "kernel": "w4a4_gemm_kernel (gate_up + SwiGLU + NVFP4 quantization of h)",
+                  "traffic": _traffic_from_profile(wl, "gemm_w4a4_", W4A4_SOURCES),
+                  "other_roof_frac": (ab / hbm_peak) if r["bound"] == "tensor" else (a / fp4_peak),
+                  "down": {"launch_ms": dn_ms, "achieved_gbs": dn_bytes / (dn_ms * 1e-3) / 1e9,
+                           "frac_hbm": dn_bytes / (dn_ms * 1e-3) / 1e9 / hbm_peak,
+                           "achieved_tflops": dn_flops / (dn_ms * 1e-3) / 1e12,
+                           "frac_tensor_fp4": dn_flops / (dn_ms * 1e-3) / 1e12 / fp4_peak}})
+        return r
 
 
 def run_ours(args, wl, dist, rank, world, local_rank):

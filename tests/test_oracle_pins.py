@@ -426,8 +426,8 @@ def test_w4a4_single_expert_equals_dense_ffn_on_quantized_activations():
 def test_quant_nvfp4_codes_round_the_exact_quotient():
     # brute force in fp64 (exact here): each code is the grid value whose
     # product with the block scale is nearest to the element, ties to the
-    # even mantissa; elements straddling the grid midpoints by one fp32 ulp
-    # are included, where an fp32 quotient would round onto the midpoint
+    # even mantissa; elements on, and one fp32 ulp either side of, the grid
+    # midpoints times the scale are included
     vals = _e4m3_values()
     grid = np.array([0, .5, 1, 1.5, 2, 3, 4, 6])
     rng = np.random.default_rng(8)
