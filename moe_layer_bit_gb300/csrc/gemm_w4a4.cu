@@ -313,8 +313,10 @@ __global__ void __launch_bounds__(kW4Threads, 1)
     tmem_alloc(sbase + C::kOffMisc, kW4TmemCols);
     tmem_relinquish();
   }
-  pdl_wait();
-  pdl_trigger();
+  // The expert offsets come from the routing kernel, which had completed
+  // before the kernel this one depends on got past its own dependency wait
+  // (every kernel of the layer waits on its predecessor before it lets its
+  // dependents launch), so the tile table is built before this kernel's wait.
   build_tile_table(L.offsets, E, TT, s_off, s_tprefix, misc + 2);
   tc_fence_before();
   __syncthreads();
@@ -325,10 +327,60 @@ __global__ void __launch_bounds__(kW4Threads, 1)
   const int total = ntok * MT;
   const int KS = L.K / kW4StageK;
   const uint32_t sf_col0 = (uint32_t)(ND * NB);  // scale-factor slots after the accumulators
+  constexpr uint32_t kTx = (uint32_t)((kRowsA + NB) * (128 + 16));  // bytes a stage's copies deliver
+
+  // the weight rows of stage ks of tile c (MODE 0: 64 gate rows 64 mt.. of
+  // expert e, then the matching up rows, I further on; MODE 1: 128 rows), and
+  // the tile's activation rows p0..
+  auto load_weights = [&](uint32_t st, const TileCoord& c, int ks, uint32_t bar) {
+    if (MODE == 0) {
+      const int gate_row = c.e * L.N + c.mt * kGuFeat;
+      const int up_row = gate_row + L.I;
+      tma_load_2d(st + C::kA, &tm_b, ks * 128, gate_row, bar);
+      tma_load_2d(st + C::kA + (uint32_t)(kGuFeat * 128), &tm_b, ks * 128, up_row, bar);
+      tma_load_2d(st + C::kOffBs, &tm_bs, ks * 16, gate_row, bar);
+      tma_load_2d(st + C::kOffBs + (uint32_t)(kGuFeat * 16), &tm_bs, ks * 16, up_row, bar);
+    } else {
+      const int row = c.e * L.N + c.mt * kTileM;
+      tma_load_2d(st, &tm_a, ks * 128, row, bar);
+      tma_load_2d(st + C::kOffAs, &tm_as, ks * 16, row, bar);
+    }
+  };
+  auto load_activations = [&](uint32_t st, int p0, int ks, uint32_t bar) {
+    if (MODE == 0) {
+      tma_load_2d(st, &tm_a, ks * 128, p0, bar);
+      tma_load_2d(st + C::kOffAs, &tm_as, ks * 16, p0, bar);
+    } else {
+      tma_load_2d(st + C::kA, &tm_b, ks * 128, p0, bar);
+      tma_load_2d(st + C::kOffBs, &tm_bs, ks * 16, p0, bar);
+    }
+  };
+
+  // Before the dependency wait the producer issues the weight half of the
+  // first NS stages (the weights do not come from the kernels before; their
+  // slots are free in a fresh ring), so the weight stream starts while the
+  // kernel before is still finishing.  The activation half follows the wait.
+  int npre = 0;
+  if (warp == kW4WarpTma) {
+    for (int u = blockIdx.x; u < total && npre < NS; u += gridDim.x) {
+      const TileCoord c = decode_tile(u, s_tprefix, E, MT);
+      for (int ks = 0; ks < KS && npre < NS; ++ks, ++npre) {
+        if (elect_one_sync()) {
+          mbar_arrive_expect_tx(full_bar(npre), kTx);
+          load_weights(sbase + (uint32_t)(npre * C::kStage), c, ks, full_bar(npre));
+        }
+        __syncwarp();
+      }
+    }
+  }
+  pdl_wait();
+  pdl_trigger();
 
   if (warp == kW4WarpTma) {
     // ------------------------------------------------------------ producer
-    constexpr uint32_t kTx = (uint32_t)((kRowsA + NB) * (128 + 16));
+    // (stages below npre have their weights in flight already; their empty
+    // waits pass at once, the ring being fresh, so none of them is left
+    // without its activation half)
     int i = 0;
     bool ok = true;
     for (int u = blockIdx.x; u < total && ok; u += gridDim.x) {
@@ -342,25 +394,11 @@ __global__ void __launch_bounds__(kW4Threads, 1)
         }
         if (elect_one_sync()) {
           const uint32_t st = sbase + (uint32_t)(s * C::kStage);
-          mbar_arrive_expect_tx(full_bar(s), kTx);
-          if (MODE == 0) {
-            // A: the tile's activation rows; B: gate rows 64 mt.. of expert e,
-            // then the matching up rows (I further on)
-            const int gate_row = c.e * L.N + c.mt * kGuFeat;
-            const int up_row = gate_row + L.I;
-            tma_load_2d(st, &tm_a, ks * 128, p0, full_bar(s));
-            tma_load_2d(st + C::kOffAs, &tm_as, ks * 16, p0, full_bar(s));
-            tma_load_2d(st + C::kA, &tm_b, ks * 128, gate_row, full_bar(s));
-            tma_load_2d(st + C::kA + (uint32_t)(kGuFeat * 128), &tm_b, ks * 128, up_row, full_bar(s));
-            tma_load_2d(st + C::kOffBs, &tm_bs, ks * 16, gate_row, full_bar(s));
-            tma_load_2d(st + C::kOffBs + (uint32_t)(kGuFeat * 16), &tm_bs, ks * 16, up_row, full_bar(s));
-          } else {
-            const int row = c.e * L.N + c.mt * kTileM;
-            tma_load_2d(st, &tm_a, ks * 128, row, full_bar(s));
-            tma_load_2d(st + C::kOffAs, &tm_as, ks * 16, row, full_bar(s));
-            tma_load_2d(st + C::kA, &tm_b, ks * 128, p0, full_bar(s));
-            tma_load_2d(st + C::kOffBs, &tm_bs, ks * 16, p0, full_bar(s));
+          if (i >= npre) {
+            mbar_arrive_expect_tx(full_bar(s), kTx);
+            load_weights(st, c, ks, full_bar(s));
           }
+          load_activations(st, p0, ks, full_bar(s));
         }
         __syncwarp();
       }

@@ -202,6 +202,37 @@ def test_w4a4_layer_parity(name):
     check_layer(bits(out)[rows], ref, f"W4A4 {name}")
 
 
+@pytest.mark.parametrize("T,H,I,E,k", [
+    (1, 256, 256, 4, 2),        # one token: 32-row token tiles with one valid row; one K stage per tile
+    (37, 512, 512, 5, 5),       # k = E, ragged T: every expert holds all 37 tokens (128-row tiles)
+    (64, 256, 768, 1, 1),       # one dense expert; down K = 768 (three stages)
+    (300, 1024, 256, 64, 4),    # 64-row tiles, ragged groups, experts without tokens
+    (40, 256, 256, 1024, 32),   # 1024 experts, k = 32: 1-3 rows per expert, a large tile table
+])
+def test_w4a4_layer_edge_shapes(T, H, I, E, k):
+    d = wk.generate_dims(T, H, I, E, k, seed=T + E)
+    gu, dn = numpy_weights(d)
+    layer = W4A4Layer(d["gu"], d["dn"], H, I, E, k, T, DEV)
+    ids = torch.empty(T, k, dtype=torch.int32, device=DEV)
+    w = torch.empty(T, k, dtype=torch.float32, device=DEV)
+    out = layer.forward(d["x"].to(DEV), d["logits"].to(DEV), topk_ids=ids, topk_w=w)
+    assert layer.device_status() == _lib.MOE_OK
+    rids, rw = orc.route(d["logits"].numpy(), k)
+    assert np.array_equal(ids.cpu().numpy(), rids)
+    ref = orc.w4a4_layer_rows(bits(d["x"]), rids, rw, gu, dn, np.arange(T, dtype=np.int32))
+    check_layer(bits(out), ref, f"W4A4 T={T} H={H} I={I} E={E} k={k}")
+
+
+def test_w4a4_zero_tokens():
+    wl = TINY
+    d = wk.generate(wl)
+    layer = W4A4Layer(d["gu"], d["dn"], wl.H, wl.I, wl.E, wl.k, wl.T, DEV)
+    out = layer.forward(d["x"][:0].to(DEV), d["logits"][:0].to(DEV))
+    torch.cuda.synchronize()
+    assert out.shape == (0, wl.H) and layer.device_status() == _lib.MOE_OK
+    assert _lib.moe_w4a4_kernel_launches(_lib.dims(0, wl.H, wl.I, wl.E, wl.k)) == 0
+
+
 def test_w4a4_rejects_shapes_below_its_stage():
     # I = 128 is below the 256-element K stage: refused before any launch
     d = _lib.dims(16, 256, 128, 8, 2)
