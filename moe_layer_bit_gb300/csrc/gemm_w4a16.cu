@@ -735,7 +735,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float up = (is_gate ? recv : own) * gsc;
             const int col = cc * 16 + j + (is_gate ? 0 : 8);
             if (col < nvalid) {
-              const float hv = g / (1.0f + __expf(-g)) * up;
+              // silu(g) * up with the fast exponential and the fast, branch-free
+              // division: an IEEE division's slow-path branch kept the loop's
+              // iterations from overlapping, and the epilogue then bounded
+              // short tiles (skewed gate_up 438 -> 340 us)
+              const float hv = __fdividef(g, 1.0f + __expf(-g)) * up;
               h[(size_t)(p0 + col) * P.out_ld + f] = __bfloat16_as_ushort(__float2bfloat16_rn(hv));
             }
           }
