@@ -102,8 +102,10 @@ struct Cfg {
   // the other group's stage, not on its own (measured faster on decode than
   // three groups of 4 warps on three slots).  32-row tiles (SB = 4) measured
   // the other way round: three groups of 4 warps beat two of 8 (grouped
-  // layer 175 vs 163 us of GEMM).
-  static constexpr int kSplit = (BN == 16 && SB == 4) ? 2 : 1;
+  // layer 175 vs 163 us of GEMM).  64/128-row tiles (SB = 4, two TMEM slots
+  // next to the two accumulators): two groups of 8 warps (prefill layer
+  // 2,414 -> 2,102 us against SB = 2 with four groups of 4).
+  static constexpr int kSplit = ((BN == 16 || BN >= 64) && SB == 4) ? 2 : 1;
   static constexpr int kGroupWarps = 4 * kSplit;
   static constexpr int kGroups0 = kDqWarps / kGroupWarps;
   static constexpr int G = kGroups0 < NA ? kGroups0 : NA;
@@ -115,9 +117,10 @@ struct Cfg {
   // activation stage is then released kBInFlight stages after it was issued,
   // so that ring is deeper: 10 stages of 8 KiB for 16-row tiles, 6 of 16 KiB
   // for 32-row ones (which keeps 6 weight stages in flight next to it).
-  // Wider tiles read permuted rows with TMA.
+  // Wider tiles read permuted rows with TMA: 2 stages of 32 or 64 KiB at SB = 4
+  // (K 256 per stage), 4 at smaller SB.
   static constexpr bool kGatherB = BN <= 32;
-  static constexpr int NSB = kGatherB ? (BN <= 16 ? 8 : 4) + kBInFlight : 4;
+  static constexpr int NSB = kGatherB ? (BN <= 16 ? 8 : 4) + kBInFlight : (SB == 4 ? 2 : 4);
   static_assert(!kGatherB || NSB > kBInFlight, "the gathering producer must not wait on a stage it has not released");
   static constexpr int NSW0 = (kSmemBudget - NSB * kBTile) / kWBytes;
   static constexpr int NSW1 = NSW0 > 12 ? 12 : NSW0;
@@ -859,25 +862,24 @@ static cudaError_t launch_gemm_cfg(const GemmLaunch& L, int rows, int T, cudaStr
   return launch_pdl(kern, dim3(grid), dim3(kThreads), smem, s, tmap, L);
 }
 
-// Token tile width from the mean number of rows per expert m = T*k/E: 16
-// rows up to m = 8 (a decode step: one tile per expert), 32 up to m = 32
-// (the grouped 800-token layer, m = 25: the one-launch layer with its own
-// row gather, measured 185 us against 193 us with 64-row tiles), else 128
-// (prefill).  64-row tiles lost to 32 or 128 on every measured workload; a
-// caller can still force them (moe_debug_layer_forward_config).
+// Token tile width: the smallest of 16/32/64/128 that covers about twice the
+// mean number of rows per expert (T*k/E), so a decode step is one tile per
+// expert, the grouped 800-token layer (25 rows per expert) takes 64-row tiles
+// and prefill the widest.  Measured on all four workloads (every width x
+// schedule): the choice is the fastest or within 1% of it.
 static int pick_bn(int rows, int E) {
-  const long long m = (long long)rows / (E > 0 ? E : 1);
-  if (2 * m <= 16) return 16;
-  if (m <= 32) return 32;
+  const long long mean2 = 2LL * rows / (E > 0 ? E : 1);
+  if (mean2 <= 16) return 16;
+  if (mean2 <= 32) return 32;
+  if (mean2 <= 64) return 64;
   return 128;
 }
 
-// K blocks per stage: 4 for the narrow token tiles (16 and 32 rows: amortise
-// the MMA warp's per-stage cost), 2 otherwise (keeps enough TMEM A slots next to the
-// 2 x BN accumulator columns and a deep enough shared-memory ring), fewer when
-// a phase's K/64 is not a multiple.
-static int pick_sb(int bn, const int* kb, int nph) {
-  int sb = bn <= 32 ? 4 : 2;
+// K blocks per stage: 4 (K 256 per stage amortises the per-stage handoffs
+// between the dequant groups and the MMA warp: measured faster for every
+// token-tile width), or 2 or 1 when a phase's K/64 is not a multiple of 4.
+static int pick_sb(const int* kb, int nph) {
+  int sb = 4;
   for (;;) {
     bool ok = true;
     for (int p = 0; p < nph; ++p) ok = ok && kb[p] % sb == 0;
@@ -890,8 +892,8 @@ template <int BN, int MODE>
 static cudaError_t launch_gemm_mode(const GemmLaunch& L, int rows, int T, cudaStream_t s) {
   int kb[2];
   for (int p = 0; p < L.nph; ++p) kb[p] = L.ph[p].K / kBlockK;
-  switch (pick_sb(BN, kb, L.nph)) {
-    case 4: return launch_gemm_cfg<BN, (BN <= 32 ? 4 : 2), MODE>(L, rows, T, s);
+  switch (pick_sb(kb, L.nph)) {
+    case 4: return launch_gemm_cfg<BN, 4, MODE>(L, rows, T, s);
     case 2: return launch_gemm_cfg<BN, 2, MODE>(L, rows, T, s);
     default: return launch_gemm_cfg<BN, 1, MODE>(L, rows, T, s);
   }

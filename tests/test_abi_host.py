@@ -77,7 +77,7 @@ def test_bad_dims_are_rejected_before_launch(lib, dims, code):
     ((0, 2048, 768, 128, 8), 0, False),     # nothing to do
     ((32, 2048, 768, 128, 8), 3, True),     # routing + grouping block; both projections in one GEMM launch
     ((64, 256, 128, 1024, 4), 4, True),     # T*E too large for the fused block: routing, then grouping
-    ((800, 2048, 512, 256, 8), 6, True),    # chunked grouping (4 launches); 32-row tiles: one GEMM launch that gathers
+    ((800, 2048, 512, 256, 8), 8, False),   # chunked grouping (4 launches), row gather, two 64-row-tile GEMMs
     ((16, 128, 64, 8, 2), 3, True),         # narrow tiles at any K
     ((2048, 256, 128, 64, 2), 8, False),    # 128-row tiles read a permuted copy: row gather kernel
 ])
