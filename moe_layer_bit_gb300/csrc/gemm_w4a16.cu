@@ -115,12 +115,13 @@ struct Cfg {
   // Narrow token tiles (BN <= 32: decode-sized batches) gather their
   // activation rows with cp.async (row sorted_token[p] of x, or row p); an
   // activation stage is then released kBInFlight stages after it was issued,
-  // so that ring is deeper: 10 stages of 8 KiB for 16-row tiles, 6 of 16 KiB
-  // for 32-row ones (which keeps 6 weight stages in flight next to it).
-  // Wider tiles read permuted rows with TMA: 2 stages of 32 or 64 KiB at SB = 4
-  // (K 256 per stage), 4 at smaller SB.
+  // so that ring is deeper: 6 stages of 8 KiB (16-row tiles) or 16 KiB
+  // (32-row tiles), which leaves room for 8 weight stages (16-row tiles: a
+  // 10-stage activation ring with 6 weight stages measured 1.1% slower on
+  // decode).  Wider tiles read permuted rows with TMA: 2 stages of 32 or 64
+  // KiB at SB = 4 (K 256 per stage), 4 at smaller SB.
   static constexpr bool kGatherB = BN <= 32;
-  static constexpr int NSB = kGatherB ? (BN <= 16 ? 8 : 4) + kBInFlight : (SB == 4 ? 2 : 4);
+  static constexpr int NSB = kGatherB ? 4 + kBInFlight : (SB == 4 ? 2 : 4);
   static_assert(!kGatherB || NSB > kBInFlight, "the gathering producer must not wait on a stage it has not released");
   static constexpr int NSW0 = (kSmemBudget - NSB * kBTile) / kWBytes;
   static constexpr int NSW1 = NSW0 > 12 ? 12 : NSW0;
