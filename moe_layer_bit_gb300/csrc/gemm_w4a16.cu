@@ -118,10 +118,17 @@ struct Cfg {
   // so that ring is deeper: 6 stages of 8 KiB (16-row tiles) or 16 KiB
   // (32-row tiles), which leaves room for 8 weight stages (16-row tiles: a
   // 10-stage activation ring with 6 weight stages measured 1.1% slower on
-  // decode).  Wider tiles read permuted rows with TMA: 2 stages of 32 or 64
-  // KiB at SB = 4 (K 256 per stage), 4 at smaller SB.
+  // decode).  Wider tiles read permuted rows with TMA: at SB = 4 (K 256 per
+  // stage) 3 stages of 32 KiB for 64-row tiles, next to 6 weight stages (the
+  // weight-streaming grouped shape: gate_up 97 -> 84 us against 2 activation
+  // and 8 weight stages; 4 + 4 measured 86 us), and 2 of 64 KiB for 128-row
+  // tiles; 4 at smaller SB.  An activation stage is refilled only after its
+  // MMAs complete, so with 2 stages the refill had only the next stage's MMAs
+  // to hide behind.  (Activation slots of one K block each, refilled block by
+  // block, and MMAs trimmed to a partial tile's valid rows both measured
+  // slower on every wide-tile workload.)
   static constexpr bool kGatherB = BN <= 32;
-  static constexpr int NSB = kGatherB ? 4 + kBInFlight : (SB == 4 ? 2 : 4);
+  static constexpr int NSB = kGatherB ? 4 + kBInFlight : (SB == 4 ? (BN == 64 ? 3 : 2) : 4);
   static_assert(!kGatherB || NSB > kBInFlight, "the gathering producer must not wait on a stage it has not released");
   static constexpr int NSW0 = (kSmemBudget - NSB * kBTile) / kWBytes;
   static constexpr int NSW1 = NSW0 > 12 ? 12 : NSW0;
@@ -139,6 +146,12 @@ struct Cfg {
   // (with the producer's in-order releases and NSB >= G) covers stage
   // i - NSB, and whose own arrival the release of stage i + NSB waits behind.
   static constexpr int NSW = NSW1 < G ? G : (NSW1 / G) * G;
+  // TMA stages with as many activation stages as TMEM A slots (64- and
+  // 128-row tiles at SB = 4): stage i takes activation stage i % NSB and A
+  // slot i % NA, both free once the stage's MMAs complete, so the A slot's
+  // barrier frees both and the MMA warp commits once per stage (prefill
+  // gate_up -1.5%, grouped -2%).
+  static constexpr bool kOneFreeBar = !kGatherB && NSB == NA;
   static_assert(G <= NA && NSW % G == 0 && (!kGatherB || NSB >= G), "dequant groups must fit the rings");
   // The tile ring: the weight producer publishes each tile of the CTA's
   // schedule (phase, expert, weight tile, token tile) into entry j % kRing;
@@ -446,7 +459,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int row0 = s_off[tr.c.e] + tr.c.nt * BN;
       for (int ks = 0; ks < KS; ++ks, ++i) {
         const int s = i % NSB;
-        if (!__all_sync(0xFFFFFFFFu, mbar_wait(emptyb_bar(s), ((uint32_t)(i / NSB) & 1u) ^ 1u, abort_flag, status))) {
+        const uint32_t freed = C::kOneFreeBar ? aempty_bar(s) : emptyb_bar(s);
+        if (!__all_sync(0xFFFFFFFFu, mbar_wait(freed, ((uint32_t)(i / NSB) & 1u) ^ 1u, abort_flag, status))) {
           ok = false;
           break;
         }
@@ -632,7 +646,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               tc_mma_ts(d_tmem, a_tmem + (uint32_t)(32 * b + 8 * kk),
                         b_desc + (uint64_t)((b * C::kBSub + kk * 32) >> 4), idesc, (ks | b | kk) != 0);
           tc_commit(aempty_bar(a));
-          tc_commit(emptyb_bar(s));
+          if (!C::kOneFreeBar) tc_commit(emptyb_bar(s));
         }
         __syncwarp();
       }
@@ -717,12 +731,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int nvalid = min(BN, s_off[c.e + 1] - p0);
       const float gsc = __ldg(c.e < P.E_routed ? P.gscale + c.e : P.shared_gscale) * 128.0f;
       const uint32_t t_acc = tmem_base + ((uint32_t)(32 * q) << 16) + (uint32_t)(d * BN);
+      // only the accumulator columns of valid rows are read (a partial tile
+      // of a 128-row width loaded all 8 column chunks before: skewed gate_up
+      // 366 -> 345 us)
 #pragma unroll 1
-      for (int cc = 0; cc < BN / 16; ++cc) {
+      for (int cc = 0; cc * 16 < nvalid; ++cc) {
         uint32_t v[16];
         tmem_ld16(t_acc + (uint32_t)(cc * 16), v);
         tc_wait_ld();
-        if (cc * 16 >= nvalid) continue;
         if ((MODE == 2 ? P.mode : MODE) == 0) {
           // rows 32q..32q+15 hold gate features f, rows 32q+16.. the matching up rows
           const int f = c.mt * 64 + 16 * q + (lane & 15);
