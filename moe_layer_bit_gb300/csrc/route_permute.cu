@@ -378,17 +378,34 @@ __global__ void __launch_bounds__(kPermChunk) route_permute_small_kernel(
 
 static size_t small_smem_bytes(int E) { return (size_t)(E + kPermChunk) * sizeof(int32_t) + rank_table_bytes(E); }
 
-// x_perm[p] = x[sorted_token[p]]: one thread per 16-byte vector (H % 8 == 0).
+// x_perm[p] = x[sorted_token[p]] (H % 8 == 0): one warp copies a row at a
+// time, its lanes taking the row's 16-byte vectors c = lane, lane + 32, ...,
+// kGatherUnroll loads in flight per lane before their stores; warps stride
+// over the rows (no per-vector index division).
+constexpr int kGatherUnroll = 8;
 __global__ void __launch_bounds__(256) perm_gather_kernel(const uint16_t* __restrict__ x,
-                                                          const int32_t* __restrict__ sorted_token, long long nvec,
+                                                          const int32_t* __restrict__ sorted_token, int n,
                                                           int vec_per_row, uint16_t* __restrict__ x_perm) {
   pdl_wait();
   pdl_trigger();
-  for (long long v = (long long)blockIdx.x * blockDim.x + threadIdx.x; v < nvec; v += (long long)gridDim.x * blockDim.x) {
-    const long long p = v / vec_per_row;
-    const int c = (int)(v - p * vec_per_row);
-    const int t = sorted_token[p];
-    reinterpret_cast<uint4*>(x_perm)[v] = reinterpret_cast<const uint4*>(x + (size_t)t * vec_per_row * 8)[c];
+  const int lane = threadIdx.x & 31;
+  const int nwarps = (int)(gridDim.x * blockDim.x) >> 5;
+  for (int p = (int)((blockIdx.x * blockDim.x + threadIdx.x) >> 5); p < n; p += nwarps) {
+    const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)sorted_token[p] * vec_per_row * 8);
+    uint4* dst = reinterpret_cast<uint4*>(x_perm + (size_t)p * vec_per_row * 8);
+    for (int c0 = 0; c0 < vec_per_row; c0 += 32 * kGatherUnroll) {
+      uint4 v[kGatherUnroll];
+#pragma unroll
+      for (int u = 0; u < kGatherUnroll; ++u) {
+        const int c = c0 + 32 * u + lane;
+        if (c < vec_per_row) v[u] = __ldg(src + c);
+      }
+#pragma unroll
+      for (int u = 0; u < kGatherUnroll; ++u) {
+        const int c = c0 + 32 * u + lane;
+        if (c < vec_per_row) dst[c] = v[u];
+      }
+    }
   }
 }
 
@@ -402,10 +419,15 @@ cudaError_t launch_gather(const uint16_t* x, const int32_t* sorted_token, int n,
                                  cudaStream_t s) {
   if (n == 0) return cudaSuccess;
   const int vpr = H / 8;
-  const long long nvec = (long long)n * vpr;
-  long long blocks = (nvec + 255) / 256;
-  if (blocks > 4096) blocks = 4096;
-  return launch_pdl(perm_gather_kernel, dim3((unsigned)blocks), dim3(256), 0, s, x, sorted_token, nvec, vpr, x_perm);
+  // one row per warp, at most 16 blocks of 8 warps per SM
+  int dev = 0, sms = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (err != cudaSuccess) return err;
+  long long blocks = ((long long)n + 7) / 8;
+  if (blocks > 16LL * sms) blocks = 16LL * sms;
+  return launch_pdl(perm_gather_kernel, dim3((unsigned)blocks), dim3(256), 0, s, x, sorted_token, n, vpr, x_perm);
 }
 
 // E routed experts, k routed slots, ks slots per token in the grouped view
