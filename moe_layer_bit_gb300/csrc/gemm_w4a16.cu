@@ -78,6 +78,10 @@ constexpr uint32_t kTmemCols = 512;
 constexpr int kMinSmem = 120 * 1024;  // keeps one CTA (one TMEM allocation) per SM
 constexpr int kSmemBudget = 216 * 1024;  // rings; the tile table (<= 8 KiB) and alignment slack on top
 constexpr int kBInFlight = 2;  // activation stages a gathering producer lane keeps in flight
+// 64-row (TMA) token tiles with at most 32 valid rows load and multiply only
+// their first 32 rows (a 32-row box, MMA N = 32).
+template <int BN>
+constexpr bool kHalfTiles = BN == 64;
 
 // Token-tile width BN and SB K blocks per stage: shared-memory rings of NSW
 // weight stages (SB packed blocks) and NSB activation stages (SB sub-tiles),
@@ -189,7 +193,8 @@ __device__ __forceinline__ int4 ld_shared_v4(uint32_t addr) {
 // MODE 2: the phases' own modes (the one-launch layer).
 template <int BN, int SB, int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
-    w4a16_gemm_kernel(const __grid_constant__ CUtensorMap tmap_act, const __grid_constant__ GemmLaunch L) {
+    w4a16_gemm_kernel(const __grid_constant__ CUtensorMap tmap_act, const __grid_constant__ CUtensorMap tmap_half,
+                      const __grid_constant__ GemmLaunch L) {
   using C = Cfg<BN, SB>;
   constexpr int NSW = C::NSW, NSB = C::NSB, NA = C::NA, R = C::kRing;
   extern __shared__ uint8_t smem_raw[];
@@ -252,7 +257,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     *abort_flag = 0;
     fence_barrier_init();
   }
-  if (!C::kGatherB && warp == kWarpProducerB && lane == 0) prefetch_tmap(&tmap_act);
+  if (!C::kGatherB && warp == kWarpProducerB && lane == 0) {
+    prefetch_tmap(&tmap_act);
+    if (kHalfTiles<BN>) prefetch_tmap(&tmap_half);
+  }
   if (C::kGatherB && L.sched != kSchedGrid3D && warp == kWarpProducer && lane == 0) {
     // The packed weights do not come from the kernels before, so while they
     // run this CTA pulls into L2 the weights of one likely early tile: tile
@@ -457,6 +465,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ring_read(j, tr) || tr.ph < 0) break;
       const int KS = tr.ph == 0 ? KS0 : KS1;
       const int row0 = s_off[tr.c.e] + tr.c.nt * BN;
+      const bool half = kHalfTiles<BN> && 2 * (s_off[tr.c.e + 1] - row0) <= BN;
+      const CUtensorMap* tm = half ? &tmap_half : &tmap_act;
       for (int ks = 0; ks < KS; ++ks, ++i) {
         const int s = i % NSB;
         const uint32_t freed = C::kOneFreeBar ? aempty_bar(s) : emptyb_bar(s);
@@ -465,10 +475,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         if (elect_one_sync()) {
-          mbar_arrive_expect_tx(fullb_bar(s), (uint32_t)C::kBTile);
+          mbar_arrive_expect_tx(fullb_bar(s), (uint32_t)(half ? C::kBTile / 2 : C::kBTile));
 #pragma unroll
           for (int b = 0; b < SB; ++b)
-            tma_load_2d(sB + s * C::kBTile + b * C::kBSub, &tmap_act, (ks * SB + b) * kBlockK, row0, fullb_bar(s));
+            tma_load_2d(sB + s * C::kBTile + b * C::kBSub, tm, (ks * SB + b) * kBlockK, row0, fullb_bar(s));
         }
         __syncwarp();
       }
@@ -601,6 +611,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // The whole warp waits and computes the (uniform) operands; one elected
     // lane issues the MMAs and commits.
     constexpr uint32_t idesc = idesc_bf16_f32(kTileM, BN);
+    constexpr uint32_t idesc_half = idesc_bf16_f32(kTileM, BN >= 32 ? BN / 2 : 16);
     int i = 0;
     bool ok = true;
     // one entry of lookahead: tile it + 1 is usually published when tile it
@@ -621,6 +632,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         have_nxt = ring_read(it + 1, nxt);
       const int KS = tr.ph == 0 ? KS0 : KS1;
       const int d = it % ND;
+      // a 64-row tile with at most 32 valid rows: the producer loaded only
+      // those, and the MMAs multiply them alone (both shapes compile-time)
+      const bool half = kHalfTiles<BN> && 2 * (s_off[tr.c.e + 1] - (s_off[tr.c.e] + tr.c.nt * BN)) <= BN;
       if (!__all_sync(0xFFFFFFFFu, mbar_wait(dempty_bar(d), ((uint32_t)(it / ND) & 1u) ^ 1u, abort_flag, status)))
         break;
       tc_fence_after();
@@ -639,12 +653,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t a_tmem = tmem_base + (uint32_t)(C::A0 + C::kSlotCols * a);
         const uint64_t b_desc = smem_desc_sw128(sB + s * C::kBTile);
         if (elect_one_sync()) {
+          if (half) {
 #pragma unroll
-          for (int b = 0; b < SB; ++b)
+            for (int b = 0; b < SB; ++b)
 #pragma unroll
-            for (int kk = 0; kk < kBlockK / 16; ++kk)
-              tc_mma_ts(d_tmem, a_tmem + (uint32_t)(32 * b + 8 * kk),
-                        b_desc + (uint64_t)((b * C::kBSub + kk * 32) >> 4), idesc, (ks | b | kk) != 0);
+              for (int kk = 0; kk < kBlockK / 16; ++kk)
+                tc_mma_ts(d_tmem, a_tmem + (uint32_t)(32 * b + 8 * kk),
+                          b_desc + (uint64_t)((b * C::kBSub + kk * 32) >> 4), idesc_half, (ks | b | kk) != 0);
+          } else {
+#pragma unroll
+            for (int b = 0; b < SB; ++b)
+#pragma unroll
+              for (int kk = 0; kk < kBlockK / 16; ++kk)
+                tc_mma_ts(d_tmem, a_tmem + (uint32_t)(32 * b + 8 * kk),
+                          b_desc + (uint64_t)((b * C::kBSub + kk * 32) >> 4), idesc, (ks | b | kk) != 0);
+          }
           tc_commit(aempty_bar(a));
           if (!C::kOneFreeBar) tc_commit(emptyb_bar(s));
         }
@@ -831,8 +854,11 @@ static GemmPhase phase_of(int mode, const GemmArgs& a) {
 template <int BN, int SB, int MODE>
 static cudaError_t launch_gemm_cfg(const GemmLaunch& L, int rows, int T, cudaStream_t s) {
   using C = Cfg<BN, SB>;
-  CUtensorMap tmap;
+  // TMA tiles: boxes of 64 columns x BN rows (a token tile) and x BN/2 rows
+  // (a tile with at most half its rows valid, kHalfTiles)
+  CUtensorMap tmap, tmap_half;
   memset(&tmap, 0, sizeof(tmap));
+  memset(&tmap_half, 0, sizeof(tmap_half));
   if (!C::kGatherB) {
     // TMA tiles read a permuted copy, one phase per launch
     if (L.nph != 1 || L.ph[0].gather_rows != nullptr) return cudaErrorInvalidValue;
@@ -840,12 +866,15 @@ static cudaError_t launch_gemm_cfg(const GemmLaunch& L, int rows, int T, cudaStr
     if (enc == nullptr) return cudaErrorNotSupported;
     const cuuint64_t gdim[2] = {(cuuint64_t)L.ph[0].K, (cuuint64_t)rows};
     const cuuint64_t gstride[1] = {(cuuint64_t)L.ph[0].K * 2};
-    const cuuint32_t box[2] = {(cuuint32_t)kBlockK, (cuuint32_t)BN};
     const cuuint32_t estride[2] = {1, 1};
-    CUresult r = enc(&tmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(L.ph[0].act), gdim, gstride, box,
-                     estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+    for (int m = 0; m < (kHalfTiles<BN> ? 2 : 1); ++m) {
+      const cuuint32_t box[2] = {(cuuint32_t)kBlockK, (cuuint32_t)(m == 0 ? BN : BN / 2)};
+      CUresult r = enc(m == 0 ? &tmap : &tmap_half, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                       const_cast<uint16_t*>(L.ph[0].act), gdim, gstride, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                       CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                       CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+      if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+    }
   }
   const int smem = C::bytes(L.E);
   auto kern = w4a16_gemm_kernel<BN, SB, MODE>;
@@ -856,7 +885,7 @@ static cudaError_t launch_gemm_cfg(const GemmLaunch& L, int rows, int T, cudaStr
     // expert receives each token at most once, so it has at most T rows
     if (L.nph != 1 || T <= 0) return cudaErrorInvalidValue;
     const dim3 grid((unsigned)(L.ph[0].N / kTileM), (unsigned)((T + BN - 1) / BN), (unsigned)L.E);
-    return launch_pdl(kern, grid, dim3(kThreads), smem, s, tmap, L);
+    return launch_pdl(kern, grid, dim3(kThreads), smem, s, tmap, tmap_half, L);
   }
   if (L.sched == kSchedClaim && L.claim == nullptr) return cudaErrorInvalidValue;
   int dev = 0, sms = 0;
@@ -876,7 +905,7 @@ static cudaError_t launch_gemm_cfg(const GemmLaunch& L, int rows, int T, cudaStr
   // whatever the residency.  The launch is programmatic, so its CTAs start
   // on the free SMs while the kernel before finishes (a cooperative launch
   // measured about 2.4 us more per decode step).
-  return launch_pdl(kern, dim3(grid), dim3(kThreads), smem, s, tmap, L);
+  return launch_pdl(kern, dim3(grid), dim3(kThreads), smem, s, tmap, tmap_half, L);
 }
 
 // Token tile width: the smallest of 16/32/64/128 that covers about twice the
