@@ -52,9 +52,18 @@ cudaError_t launch_permute(const int32_t* ids, const uint16_t* x, int T, int H, 
 // then kSchedInts more; may be null) is zeroed.  T*(k+shared) <= 1024 with T*E <= 32768 runs as one
 // single-block launch; otherwise routing, then one grouping block or
 // histogram + scan + scatter.
+// With copy_bytes > 0 (a multiple of 16, both pointers 16-byte aligned) the
+// launch also copies copy_bytes from copy_src (e.g. mapped page-locked host
+// memory) to copy_dst, in extra blocks of the single-block launch, so the copy
+// overlaps the routing; only when route_group_copies() says that launch is
+// taken (cudaErrorInvalidValue otherwise).
 cudaError_t launch_route_group(const float* logits, int T, int E, int k, bool shared, int32_t* ids, float* w,
                                int32_t* counts, int32_t* offsets, int32_t* sorted_token, int32_t* inv_perm,
-                               int32_t* scratch, int32_t* zero_e, cudaStream_t s);
+                               int32_t* scratch, int32_t* zero_e, cudaStream_t s, const void* copy_src = nullptr,
+                               void* copy_dst = nullptr, size_t copy_bytes = 0);
+// True when launch_route_group routes and groups in its single-block launch,
+// which can carry a copy.
+bool route_group_copies(int T, int E, int k, bool shared);
 // x_perm[p] = x[sorted_token[p]] for p < n.
 cudaError_t launch_gather(const uint16_t* x, const int32_t* sorted_token, int n, int H, uint16_t* x_perm,
                           cudaStream_t s);

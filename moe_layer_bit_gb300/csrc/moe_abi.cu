@@ -246,7 +246,7 @@ namespace {
 int layer_forward_impl(const uint16_t* x, const float* logits, moe_w4 w_gate_up, moe_w4 w_down,
                        const moe_w4* shared_gu, const moe_w4* shared_dn, moe_dims d, uint16_t* out,
                        int32_t* topk_ids, float* topk_w, void* ws, size_t ws_bytes, void* stream, void* const* ev,
-                       int force_bn = -1, int force_sched = -1) {
+                       int force_bn = -1, int force_sched = -1, const uint16_t* x_copy_src = nullptr) {
   MOE_TRY(check_dims(d));
   if (d.T == 0) return MOE_OK;
   MOE_TRY(check_ptrs({x, logits, w_gate_up.packed, w_gate_up.global_scale, w_down.packed, w_down.global_scale, out,
@@ -302,8 +302,12 @@ int layer_forward_impl(const uint16_t* x, const float* logits, moe_w4 w_gate_up,
   int32_t* ready = reinterpret_cast<int32_t*>(w + L.ready);
   int32_t* claim = ready + EG;
   const moe::GemmPlan plan = moe::plan_layer(rows, EG, d.H, d.I, force_bn, force_sched);
+  // x_copy_src (host-buffer calls): x's bytes, copied to x by extra blocks of
+  // the routing launch, which the caller has checked can carry them
   MOE_TRY(cuda_status(moe::launch_route_group(logits, d.T, d.E, d.k, shared, ids, wts, counts, offs, sorted, inv,
-                                              reinterpret_cast<int32_t*>(w + L.perm), ready, s)));
+                                              reinterpret_cast<int32_t*>(w + L.perm), ready, s, x_copy_src,
+                                              const_cast<uint16_t*>(x), x_copy_src != nullptr ? (size_t)d.T * d.H * 2
+                                                                                              : 0)));
   MOE_TRY(mark(1));
   // the narrow-tile GEMM gathers the rows of x itself; the wide one reads x_perm
   if (!plan.gathers) MOE_TRY(cuda_status(moe::launch_gather(x, sorted, rows, d.H, xp, s)));
@@ -457,11 +461,20 @@ int enqueue_host_call(const uint16_t* host_x, const float* host_logits, moe_w4 w
   uint8_t* w = static_cast<uint8_t*>(ws);
   const size_t xb = (size_t)d.T * d.H * 2, lb = (size_t)d.T * d.E * sizeof(float);
   uint16_t* dx = reinterpret_cast<uint16_t*>(w + L.hx);
-  MOE_TRY(cuda_status(cudaMemcpyAsync(dx, host_x, xb, cudaMemcpyHostToDevice, s)));
   const float* ml = static_cast<const float*>(mapped_device_ptr(host_logits));
   uint16_t* mo = static_cast<uint16_t*>(mapped_device_ptr(host_out));
-  if (ml != nullptr && mo != nullptr && aligned16(ml) && aligned16(mo))
+  const uint16_t* mx = static_cast<const uint16_t*>(mapped_device_ptr(host_x));
+  if (ml != nullptr && mo != nullptr && aligned16(ml) && aligned16(mo)) {
+    // x mapped too, and routing in one launch: extra blocks of that launch
+    // copy x, so the call needs no copy of its own (it would otherwise run
+    // before the routing, on the copy engine)
+    if (mx != nullptr && aligned16(mx) && moe::route_group_copies(d.T, d.E, d.k, false))
+      return layer_forward_impl(dx, ml, w_gate_up, w_down, nullptr, nullptr, d, mo, nullptr, nullptr, ws, ws_bytes, s,
+                                nullptr, -1, -1, mx);
+    MOE_TRY(cuda_status(cudaMemcpyAsync(dx, host_x, xb, cudaMemcpyHostToDevice, s)));
     return moe_layer_forward(dx, ml, w_gate_up, w_down, d, mo, nullptr, nullptr, ws, ws_bytes, s);
+  }
+  MOE_TRY(cuda_status(cudaMemcpyAsync(dx, host_x, xb, cudaMemcpyHostToDevice, s)));
   float* dl = reinterpret_cast<float*>(w + L.hlogits);
   uint16_t* dout = reinterpret_cast<uint16_t*>(w + L.hout);
   MOE_TRY(cuda_status(cudaMemcpyAsync(dl, host_logits, lb, cudaMemcpyHostToDevice, s)));

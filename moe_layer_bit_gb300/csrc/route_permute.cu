@@ -291,11 +291,34 @@ __global__ void __launch_bounds__(kPermChunk) perm_scatter_kernel(const int32_t*
 // with logits != nullptr the block first routes its T tokens (one warp per
 // token, warps striding), writing ids / weights; then per-warp counts, the
 // scans over warps and over experts, and the stable scatter, in one launch.
+// 16-byte vectors each thread of a copy block moves (64 KiB per 1024-thread block)
+constexpr int kCopyVecPerThread = 4;
+
 template <int NV>
 __global__ void __launch_bounds__(kPermChunk) route_permute_small_kernel(
     const float* __restrict__ logits, int T, int E, int k, int ks, int32_t* __restrict__ ids, float* __restrict__ wts,
     int32_t* __restrict__ counts, int32_t* __restrict__ offsets, int32_t* __restrict__ sorted_token,
-    int32_t* __restrict__ inv_perm, int32_t* __restrict__ zero_e) {
+    int32_t* __restrict__ inv_perm, int32_t* __restrict__ zero_e, const uint4* __restrict__ copy_src,
+    uint4* __restrict__ copy_dst, long long copy_vec) {
+  if (blockIdx.x > 0) {
+    // a copy block: its share of the copy (kCopyVecPerThread 16-byte vectors
+    // per thread, loads before stores), ordered after the kernels before
+    pdl_wait();
+    pdl_trigger();
+    const long long v0 = (long long)(blockIdx.x - 1) * blockDim.x * kCopyVecPerThread + threadIdx.x;
+    uint4 v[kCopyVecPerThread];
+#pragma unroll
+    for (int u = 0; u < kCopyVecPerThread; ++u) {
+      const long long i = v0 + (long long)u * blockDim.x;
+      if (i < copy_vec) v[u] = copy_src[i];
+    }
+#pragma unroll
+    for (int u = 0; u < kCopyVecPerThread; ++u) {
+      const long long i = v0 + (long long)u * blockDim.x;
+      if (i < copy_vec) copy_dst[i] = v[u];
+    }
+    return;
+  }
   // E routed experts; the grouping sees EG = E + (ks - k) (the shared expert last)
   const int EG = E + (ks - k);
   extern __shared__ int32_t smem_i[];
@@ -432,16 +455,22 @@ cudaError_t launch_gather(const uint16_t* x, const int32_t* sorted_token, int n,
 
 // E routed experts, k routed slots, ks slots per token in the grouped view
 // (k + 1 with the shared expert, which groups as expert E).
+// Block 0 routes and groups; blocks 1.. (when copy_bytes > 0) copy.
 template <int NV>
 static cudaError_t launch_small(const float* logits, int T, int E, int k, int ks, int32_t* ids, float* w,
                                 int32_t* counts, int32_t* offsets, int32_t* sorted_token, int32_t* inv_perm,
-                                int32_t* zero_e, cudaStream_t s) {
+                                int32_t* zero_e, cudaStream_t s, const void* copy_src = nullptr,
+                                void* copy_dst = nullptr, size_t copy_bytes = 0) {
   const size_t smem = small_smem_bytes(E + (ks - k));
   auto kern = route_permute_small_kernel<NV>;
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (err != cudaSuccess) return err;
-  return launch_pdl(kern, dim3(1), dim3(kPermChunk), smem, s, logits, T, E, k, ks, ids, w, counts, offsets,
-                    sorted_token, inv_perm, zero_e);
+  const long long nvec = (long long)(copy_bytes / 16);
+  const long long per_block = (long long)kPermChunk * kCopyVecPerThread;
+  const long long copy_blocks = (nvec + per_block - 1) / per_block;
+  return launch_pdl(kern, dim3((unsigned)(1 + copy_blocks)), dim3(kPermChunk), smem, s, logits, T, E, k, ks, ids, w,
+                    counts, offsets, sorted_token, inv_perm, zero_e, static_cast<const uint4*>(copy_src),
+                    static_cast<uint4*>(copy_dst), nvec);
 }
 
 static cudaError_t launch_chunked(const int32_t* ids, int T, int E, int k, int ks, int32_t* counts, int32_t* offsets,
@@ -483,15 +512,22 @@ int route_group_launches(int T, int E, int k, bool shared) {
   return n <= kPermChunk ? 2 : 4;
 }
 
+bool route_group_copies(int T, int E, int k, bool shared) { return route_group_launches(T, E, k, shared) == 1; }
+
 cudaError_t launch_route_group(const float* logits, int T, int E, int k, bool shared, int32_t* ids, float* w,
                                int32_t* counts, int32_t* offsets, int32_t* sorted_token, int32_t* inv_perm,
-                               int32_t* scratch, int32_t* zero_e, cudaStream_t s) {
+                               int32_t* scratch, int32_t* zero_e, cudaStream_t s, const void* copy_src,
+                               void* copy_dst, size_t copy_bytes) {
   const int ks = k + (shared ? 1 : 0);
   const int n = T * ks;
   cudaError_t err;
+  if (copy_bytes > 0 && (!route_group_copies(T, E, k, shared) || copy_bytes % 16 != 0 || copy_src == nullptr ||
+                         copy_dst == nullptr || (reinterpret_cast<uintptr_t>(copy_src) & 15u) != 0 ||
+                         (reinterpret_cast<uintptr_t>(copy_dst) & 15u) != 0))
+    return cudaErrorInvalidValue;
   if (n <= kPermChunk && (long long)T * E <= kFusedRouteLogits) {
     MOE_DISPATCH_NV(route_nv(E), err = (launch_small<NV>(logits, T, E, k, ks, ids, w, counts, offsets, sorted_token,
-                                                         inv_perm, zero_e, s)));
+                                                         inv_perm, zero_e, s, copy_src, copy_dst, copy_bytes)));
     return err;
   }
   err = launch_route_topk(logits, T, E, k, ids, w, s);

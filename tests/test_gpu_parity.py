@@ -372,6 +372,31 @@ def test_layer_host_entry_pageable_and_pinned(pinned):
     assert layer.device_status() == _lib.MOE_OK
 
 
+@pytest.mark.parametrize("T,H,I,E,k", [
+    (128, 4096, 256, 32, 8),  # routing in one launch: x (1 MiB) copied by 16 extra blocks of it; 64-row tiles
+    (200, 256, 128, 16, 8),   # routing, then histogram / scan / scatter: x copied before the routing
+])
+def test_host_entry_x_copy_paths(T, H, I, E, k):
+    # page-locked buffers: x reaches the workspace through the routing launch
+    # or through a copy of its own; either way the host entry and a host plan
+    # equal the device entry bit for bit
+    d = wk.generate_dims(T, H, I, E, k, seed=T + H)
+    layer = MoELayer(d["gu"], d["dn"], H, I, E, k, T, DEV)
+    ref = layer.forward(d["x"].to(DEV), d["logits"].to(DEV))
+    torch.cuda.synchronize()
+    xh, lh = d["x"].clone().pin_memory(), d["logits"].clone().pin_memory()
+    oh = torch.full((T, H), float("nan"), dtype=torch.bfloat16).pin_memory()
+    layer.forward_host(xh, lh, oh)
+    assert np.array_equal(bits(oh), bits(ref))
+    oh.fill_(float("nan"))
+    s = torch.cuda.Stream()
+    with layer.host_plan(xh, lh, oh, s) as plan:
+        plan.run()
+        plan.run()
+    assert np.array_equal(bits(oh), bits(ref))
+    assert layer.device_status() == _lib.MOE_OK
+
+
 def test_host_plan_replays_with_new_host_contents():
     # a caller-owned plan (recorded graph) on page-locked buffers and a created
     # stream: every run must read the host inputs' current contents
