@@ -269,7 +269,11 @@ int moe_layer_forward_shared(const uint16_t *x, const float *logits, const uint1
  * When host_logits and host_out are page-locked memory the device can address
  * (mapped, 16-byte aligned), the routing kernel reads the logits and the
  * combine writes the output through their device addresses; otherwise they
- * are copied through ws as well.  Host buffers should be page-locked for full
+ * are copied through ws as well.  If host_x is mapped page-locked memory too
+ * (16-byte aligned) and the routing runs as one single-block launch
+ * (T*k <= 1024 and T*E <= 32768), extra blocks of that launch copy host_x into
+ * ws while it routes; otherwise host_x is copied before the routing.  Host
+ * buffers should be page-locked for full
  * transfer speed.  Weights stay on the device.  Needs moe_workspace_bytes(d)
  * of ws.  Every call issues its copies and launches afresh and keeps nothing
  * after it returns. */
