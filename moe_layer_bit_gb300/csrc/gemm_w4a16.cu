@@ -129,9 +129,8 @@ struct Cfg {
   // tiles; 4 at smaller SB.  An activation stage is refilled only after its
   // MMAs complete, so with 2 stages the refill had only the next stage's MMAs
   // to hide behind.  (Activation slots of one K block each, refilled block by
-  // block, measured slower on every wide-tile workload, and so did MMAs
-  // trimmed to a partial tile's rows with a run-time instruction descriptor;
-  // kHalfTiles keeps both MMA shapes compile-time.)
+  // block, and MMAs trimmed to a partial tile's valid rows both measured
+  // slower on every wide-tile workload.)
   static constexpr bool kGatherB = BN <= 32;
   static constexpr int NSB = kGatherB ? 4 + kBInFlight : (SB == 4 ? (BN == 64 ? 3 : 2) : 4);
   static_assert(!kGatherB || NSB > kBInFlight, "the gathering producer must not wait on a stage it has not released");
